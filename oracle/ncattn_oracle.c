@@ -1,0 +1,292 @@
+/*
+ * fp64 CPU oracle for causal multi-head self-attention with parameter-free
+ * QK RMSNorm and rotary position embeddings (RoPE).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code with
+ * the CUDA path: it is the plain definition written out in double precision,
+ * one loop per step, with no tiling, fusion or reordering.
+ *
+ * What it follows (the pages print no formula; the readings are the plainest
+ * ones the pages support):
+ *  - QK-norm: queries and keys are normalised (usually RMSNorm) before the dot
+ *    product -- ai.flicky.cc, "nanochat: свой ChatGPT от токенизатора до чата",
+ *    section "Модель: что изменилось со времён GPT-2" (QK-norm bullet) and
+ *    adg.csdn.net "4小时100美元！...nanochat...", section "1. 极致精简的技术架构".
+ *  - RMSNorm is x / sqrt(mean(x^2) + eps) * g and nanochat uses it without
+ *    trainable parameters (g = 1) -- same ai.flicky.cc section, RMSNorm bullet.
+ *    Read here per head vector over D.
+ *  - Rotary embeddings replace positional embeddings -- same section, first
+ *    bullet.  Read here as the original RoPE: theta_i = base^(-2i/D),
+ *    i < D/2, pair (i, i + D/2) rotated by angle p * theta_i (the "rotate-half"
+ *    pairing), norm first, then rotation.
+ *  - Causal softmax(QK^T / sqrt(D)) V per head; the log-sum-exp is natural log.
+ *  - Decode: generation with a KV cache (ai.flicky.cc, section
+ *    "Карта репозитория", engine.py row; 7minutos.es "Andrej Karpathy lanza
+ *    nanochat ...", section "Entrenamiento medio, SFT y uso de herramientas").
+ *
+ * Layout: q, k, v, o, dout, dq, dk, dv are [B, T, H, D] row-major; lse is
+ * [B, H, T]; rms factors are [B, T, H].  pos is [T] (NULL means 0..T-1).
+ * flags: bit 0 = apply RMSNorm, bit 1 = apply RoPE (both on for the method;
+ * off only to reduce to plain causal attention in the tests).
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_NORM 1
+#define ORC_ROPE 2
+
+static size_t at4(int b, int t, int h, int d, int T, int H, int D)
+{
+    return (((size_t)b * T + t) * H + h) * D + d;
+}
+
+static int position(const int *pos, int t) { return pos ? pos[t] : t; }
+
+/* RMS factor r = sqrt(mean_d(x_d^2) + eps) of one head vector. */
+static double rms_of(const double *x, int D, double eps)
+{
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) ss += x[d] * x[d];
+    return sqrt(ss / D + eps);
+}
+
+/* RoPE angle of pair i at position p: p * base^(-2i/D). */
+static double rope_angle(int p, int i, int D, double base)
+{
+    return (double)p * pow(base, -2.0 * i / D);
+}
+
+/* Rotate pair (i, i + D/2) of one head vector by +angle(p) (sign = +1) or
+ * by -angle(p) (sign = -1, the transpose used in the backward). */
+static void rotate(double *x, int p, int D, double base, int sign)
+{
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        double th = sign * rope_angle(p, i, D, base);
+        double c = cos(th), s = sin(th);
+        double a = x[i], b = x[i + half];
+        x[i] = a * c - b * s;
+        x[i + half] = a * s + b * c;
+    }
+}
+
+/* Step 1 + 2: xhat = RoPE(x / r, pos), r per head vector.
+ * xhat [B,T,H,D]; r [B,T,H] (may be NULL). */
+void orc_norm_rope(const double *x, const int *pos, int B, int T, int H, int D,
+                   double eps, double base, int flags, double *xhat, double *r)
+{
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t)
+            for (int h = 0; h < H; ++h) {
+                const double *xi = x + at4(b, t, h, 0, T, H, D);
+                double *yo = xhat + at4(b, t, h, 0, T, H, D);
+                double rr = (flags & ORC_NORM) ? rms_of(xi, D, eps) : 1.0;
+                for (int d = 0; d < D; ++d) yo[d] = xi[d] / rr;
+                if (flags & ORC_ROPE) rotate(yo, position(pos, t), D, base, +1);
+                if (r) r[((size_t)b * T + t) * H + h] = rr;
+            }
+}
+
+static double dot(const double *a, const double *b, int n)
+{
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+/* Step 3 for one (b, h): probabilities P[i][j] (j <= i, zero above the
+ * diagonal), outputs o and log-sum-exp.  P is T*T, row-major. */
+static void attend_head(const double *qh, const double *kh, const double *v,
+                        int b, int h, int T, int H, int D, double *P,
+                        double *o, double *lse)
+{
+    double scale = 1.0 / sqrt((double)D);
+    for (int i = 0; i < T; ++i) {
+        double *row = P + (size_t)i * T;
+        const double *qi = qh + at4(b, i, h, 0, T, H, D);
+        double m = -INFINITY;
+        for (int j = 0; j <= i; ++j) {
+            row[j] = dot(qi, kh + at4(b, j, h, 0, T, H, D), D) * scale;
+            if (row[j] > m) m = row[j];
+        }
+        double l = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            row[j] = exp(row[j] - m);
+            l += row[j];
+        }
+        for (int j = 0; j <= i; ++j) row[j] /= l;
+        for (int j = i + 1; j < T; ++j) row[j] = 0.0;
+        double *oi = o + at4(b, i, h, 0, T, H, D);
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j <= i; ++j) acc += row[j] * v[at4(b, j, h, d, T, H, D)];
+            oi[d] = acc;
+        }
+        if (lse) lse[((size_t)b * H + h) * T + i] = m + log(l);
+    }
+}
+
+/* Forward: o = softmax(qhat khat^T / sqrt(D) + causal mask) v; lse [B,H,T]. */
+int orc_attn_fwd(const double *q, const double *k, const double *v, const int *pos,
+                 int B, int T, int H, int D, double eps, double base, int flags,
+                 double *o, double *lse)
+{
+    size_t n = (size_t)B * T * H * D;
+    double *qh = malloc(n * sizeof(double)), *kh = malloc(n * sizeof(double));
+    if (!qh || !kh) { free(qh); free(kh); return -1; }
+    orc_norm_rope(q, pos, B, T, H, D, eps, base, flags, qh, NULL);
+    orc_norm_rope(k, pos, B, T, H, D, eps, base, flags, kh, NULL);
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            double *P = malloc((size_t)T * T * sizeof(double));
+            if (!P) { err = -1; continue; }
+            attend_head(qh, kh, v, b, h, T, H, D, P, o, lse);
+            free(P);
+        }
+    free(qh);
+    free(kh);
+    return err;
+}
+
+/* Backward of one head vector through RoPE and RMSNorm:
+ * u = R(p)^T g, then dx = (u - y <u, y> / D) / r with y = x / r (the
+ * normalised vector before rotation). */
+static void norm_rope_backward(const double *x, const double *g, int p, int D,
+                               double eps, double base, int flags, double *dx)
+{
+    double *u = malloc((size_t)D * sizeof(double));
+    memcpy(u, g, (size_t)D * sizeof(double));
+    if (flags & ORC_ROPE) rotate(u, p, D, base, -1);
+    if (flags & ORC_NORM) {
+        double r = rms_of(x, D, eps);
+        double uy = 0.0;
+        for (int d = 0; d < D; ++d) uy += u[d] * (x[d] / r);
+        for (int d = 0; d < D; ++d) dx[d] = (u[d] - (x[d] / r) * uy / D) / r;
+    } else {
+        memcpy(dx, u, (size_t)D * sizeof(double));
+    }
+    free(u);
+}
+
+/* Step 4, by hand (no autograd):
+ *   dv_j  = sum_{i>=j} P_ij do_i
+ *   dP_ij = <do_i, v_j>,  Delta_i = <do_i, o_i>
+ *   dS_ij = P_ij (dP_ij - Delta_i)
+ *   dqhat_i = sum_j dS_ij khat_j / sqrt(D),  dkhat_j = sum_i dS_ij qhat_i / sqrt(D)
+ * then back through RoPE and RMSNorm to dq, dk. */
+int orc_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
+                 const int *pos, int B, int T, int H, int D, double eps, double base,
+                 int flags, double *dq, double *dk, double *dv)
+{
+    size_t n = (size_t)B * T * H * D;
+    double *qh = malloc(n * sizeof(double)), *kh = malloc(n * sizeof(double));
+    double *o = malloc(n * sizeof(double));
+    double *dqh = calloc(n, sizeof(double)), *dkh = calloc(n, sizeof(double));
+    if (!qh || !kh || !o || !dqh || !dkh) {
+        free(qh); free(kh); free(o); free(dqh); free(dkh);
+        return -1;
+    }
+    orc_norm_rope(q, pos, B, T, H, D, eps, base, flags, qh, NULL);
+    orc_norm_rope(k, pos, B, T, H, D, eps, base, flags, kh, NULL);
+    double scale = 1.0 / sqrt((double)D);
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            double *P = malloc((size_t)T * T * sizeof(double));
+            double *dS = malloc((size_t)T * T * sizeof(double));
+            if (!P || !dS) { free(P); free(dS); err = -1; continue; }
+            attend_head(qh, kh, v, b, h, T, H, D, P, o, NULL);
+            for (int i = 0; i < T; ++i) {
+                const double *doi = dout + at4(b, i, h, 0, T, H, D);
+                double delta = dot(doi, o + at4(b, i, h, 0, T, H, D), D);
+                for (int j = 0; j < T; ++j) {
+                    double pij = P[(size_t)i * T + j];
+                    double dpij = (j <= i) ? dot(doi, v + at4(b, j, h, 0, T, H, D), D) : 0.0;
+                    dS[(size_t)i * T + j] = pij * (dpij - delta);
+                }
+            }
+            for (int j = 0; j < T; ++j)
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int i = j; i < T; ++i)
+                        acc += P[(size_t)i * T + j] * dout[at4(b, i, h, d, T, H, D)];
+                    dv[at4(b, j, h, d, T, H, D)] = acc;
+                }
+            for (int i = 0; i < T; ++i)
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int j = 0; j <= i; ++j)
+                        acc += dS[(size_t)i * T + j] * kh[at4(b, j, h, d, T, H, D)];
+                    dqh[at4(b, i, h, d, T, H, D)] = acc * scale;
+                }
+            for (int j = 0; j < T; ++j)
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int i = j; i < T; ++i)
+                        acc += dS[(size_t)i * T + j] * qh[at4(b, i, h, d, T, H, D)];
+                    dkh[at4(b, j, h, d, T, H, D)] = acc * scale;
+                }
+            for (int t = 0; t < T; ++t) {
+                size_t off = at4(b, t, h, 0, T, H, D);
+                norm_rope_backward(q + off, dqh + off, position(pos, t), D, eps, base, flags, dq + off);
+                norm_rope_backward(k + off, dkh + off, position(pos, t), D, eps, base, flags, dk + off);
+            }
+            free(P);
+            free(dS);
+        }
+    free(qh); free(kh); free(o); free(dqh); free(dkh);
+    return err;
+}
+
+/* Step 5, decode: one new query per stream b at position p = lens[b] - 1,
+ * attending over cache slots 0 .. lens[b]-1.  Keys are given RAW: slot j is
+ * normalised and rotated at position j here, exactly as a prefill over the
+ * same raw keys would have stored it; the new token's raw key sits at slot p.
+ * q [B,H,D]; k_raw, v [B,Tcap,H,D]; out [B,H,D]. */
+int orc_attn_decode(const double *q, const double *k_raw, const double *v, const int *lens,
+                    int B, int H, int D, int Tcap, double eps, double base, int flags,
+                    double *out)
+{
+    double scale = 1.0 / sqrt((double)D);
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            int L = lens[b];
+            if (L < 1 || L > Tcap) { err = -2; continue; }
+            double *qh = malloc((size_t)D * sizeof(double));
+            double *kh = malloc((size_t)D * sizeof(double));
+            double *s = malloc((size_t)L * sizeof(double));
+            const double *qi = q + ((size_t)b * H + h) * D;
+            double rq = (flags & ORC_NORM) ? rms_of(qi, D, eps) : 1.0;
+            for (int d = 0; d < D; ++d) qh[d] = qi[d] / rq;
+            if (flags & ORC_ROPE) rotate(qh, L - 1, D, base, +1);
+            double m = -INFINITY;
+            for (int j = 0; j < L; ++j) {
+                const double *kj = k_raw + at4(b, j, h, 0, Tcap, H, D);
+                double rk = (flags & ORC_NORM) ? rms_of(kj, D, eps) : 1.0;
+                for (int d = 0; d < D; ++d) kh[d] = kj[d] / rk;
+                if (flags & ORC_ROPE) rotate(kh, j, D, base, +1);
+                s[j] = dot(qh, kh, D) * scale;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < L; ++j) {
+                s[j] = exp(s[j] - m);
+                l += s[j];
+            }
+            double *oi = out + ((size_t)b * H + h) * D;
+            for (int d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h, d, Tcap, H, D)];
+                oi[d] = acc;
+            }
+            free(qh); free(kh); free(s);
+        }
+    return err;
+}
