@@ -1,0 +1,408 @@
+"""Benchmark: causal attention fwd+bwd (d20 shape) and KV-cache decode on B300.
+
+One step = one pass of the whole hot path over the d20 workload
+(B=32, T=2048, H=10, D=128): nc_attn_fwd (RoPE table, QK RMSNorm+RoPE
+prologue, tcgen05 forward) then nc_attn_bwd (backward preprocess, tcgen05
+backward with the fused dk epilogue, dq finalize).  Inputs are seeded
+synthetic bf16 Gaussians already resident in HBM; q, k, v and dout together
+are 671 MB, more than the 126 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `value` is fwd+bwd TFLOP/s under the
+algorithmic FLOP count (causal half of 2 matmuls forward, 5 backward).
+Decode (32 streams, H=10, D=128, capacity 2048, seeded lengths) is timed too
+and reported under "decode" in GB/s of algorithmic cache bytes.
+
+--impl reference times the fp64 CPU oracle (the only other implementation
+of this method there is) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our impl -----
+
+def bench_ours(args, ws_n, rank, local):
+    import causal_attention_rope_nc_b300 as nc
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.D20
+    B, T, H, D = w.B, w.T, w.H, w.D
+    eps, base = workloads.EPS, workloads.ROPE_BASE
+    # weak scaling: every rank runs its own d20 batch (seed offset by rank)
+    q, k, v, dout = workloads.attn_inputs(B, T, H, D, w.seed + 1000 * rank)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, dout))
+    out = torch.empty_like(qd)
+    qh, kh = torch.empty_like(qd, dtype=torch.float16), torch.empty_like(kd, dtype=torch.float16)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = nc.new_workspace(nc.NC_OP_FWD, B, T, H, D, dev)
+    ws_b = nc.new_workspace(nc.NC_OP_BWD, B, T, H, D, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nc.nc_attn_fwd(qd, kd, vd, None, out, lse, qh, kh, None, ws_f, eps, base, stream)
+        nc.nc_attn_bwd(qd, kd, vd, None, out, lse, qh, kh, dod, dq, dk, dv, ws_b, eps, base, stream)
+
+    def barrier():
+        if ws_n > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launch stream ----
+    nc.nc_profile_read()  # clear
+    nc.nc_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    nc.nc_profile_enable(False)
+    ms_total = ev0.elapsed_time(ev1)
+    kern = nc.nc_profile_read()
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    # max over ranks
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if ws_n > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    flops = w.fwd_bwd_flops()
+    value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
+
+    # ---- decode (same rank, own timing; L2 flushed between calls) ----
+    dec = bench_decode(nc, dev, args, rank)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = bench_e2e(nc, dev, args, q, k, v, dout, ws_f, ws_b)
+
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    launches = sum(n for n, _ in kern.values())
+    # dominant kernel by total time
+    name, (n_l, tot) = max(kern.items(), key=lambda kv: kv[1][1])
+    per_launch_ms = tot / max(n_l, 1)
+    alg = {"attn_bwd": 2.5 * w.fwd_flops(), "attn_fwd": w.fwd_flops()}
+    timed_s = ms_total * 1e-3
+    peak_t = pk["bf16_tflops_sustained"] if timed_s > 2.0 else pk["bf16_tflops"]
+    roof = None
+    if name in alg:
+        ach = alg[name] / (per_launch_ms * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_t,
+                "unit": "TFLOP/s", "frac": round(ach / peak_t, 4), "traffic": None,
+                "peak_kind": f"{pk_kind} {'sustained' if timed_s > 2.0 else 'burst'} bf16"}
+    kernels = {k_: {"launches": n_, "avg_us": round(1e3 * t_ / max(n_, 1), 2),
+                    "share": round(t_ / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
+               for k_, (n_, t_) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+    for k_ in ("attn_fwd", "attn_bwd"):
+        if k_ in kern:
+            n_, t_ = kern[k_]
+            kernels[k_]["tflops"] = round(alg[k_] / (t_ / n_ * 1e-3) / 1e12, 1)
+            kernels[k_]["frac_of_peak"] = round(kernels[k_]["tflops"] / pk["bf16_tflops"], 4)
+    line = {
+        "metric": "causal attn fwd+bwd TFLOP/s (% bf16 peak) at d20; decode GB/s (% HBM peak)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, d20 shapes)",
+        "config": {"workload": "d20 block attention fwd+bwd: B=32 T=2048 H=10 D=128, causal, "
+                               "QK RMSNorm eps=1e-6, RoPE base 10000",
+                   "B": B, "T": T, "H": H, "D": D, "parallelism": f"replicas x{ws_n} (batch shards)",
+                   "l2": "inputs 671 MB > 126 MB L2; no flush between steps"},
+        "frac_of_peak": round(value / ws_n / pk["bf16_tflops"], 4),
+        "peak_kind": pk_kind,
+        "roofline": roof,
+        "kernels": kernels,
+        "decode": dec,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+def bench_decode(nc, dev, args, rank):
+    w = workloads.D20_DECODE
+    lens, q, k_raw, v = workloads.decode_workload_inputs(w)
+    kcache = nc.qk_norm_rope(k_raw.to(dev), eps=workloads.EPS, rope_base=workloads.ROPE_BASE)
+    vcache = v.to(dev)
+    qd, lens_d = q.to(dev), lens.to(dev)
+    out = torch.empty((w.B, w.H, w.D), dtype=torch.bfloat16, device=dev)
+    ws = nc.new_workspace(nc.NC_OP_DECODE, w.B, w.Tcap, w.H, w.D, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        nc.nc_attn_decode(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
+                          workloads.ROPE_BASE, stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(max(args.steps, 5)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during decode")
+    byt = workloads.decode_bytes(lens, w.H, w.D)
+    ms = statistics.median(times)
+    pk, kind = peaks()
+    gbs = byt / (ms * 1e-3) / 1e9
+    return {"workload": "d20 decode: 32 streams, H=10, D=128, cache capacity 2048, lens ~ U[1,2048] seed 4",
+            "bytes": byt, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None},
+            "l2": "256 MB buffer written between calls", "tokens_per_s": round(w.B / (ms * 1e-3), 1)}
+
+
+def bench_e2e(nc, dev, args, q, k, v, dout, ws_f, ws_b):
+    """fwd+bwd through the public API with pinned host inputs: H2D of q, k, v,
+    dout and D2H of dq, dk, dv inside the timed region."""
+    w = workloads.D20
+    hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, dout))
+    hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+    dq_, dk_, dv_ = (torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    qd_, kd_, vd_, do_ = (torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for _ in range(4))
+    out = torch.empty_like(qd_)
+    qh, kh = torch.empty_like(qd_, dtype=torch.float16), torch.empty_like(qd_, dtype=torch.float16)
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+
+    def step():
+        for d_, h_ in ((qd_, hq), (kd_, hk), (vd_, hv), (do_, hdo)):
+            d_.copy_(h_, non_blocking=True)
+        nc.nc_attn_fwd(qd_, kd_, vd_, None, out, lse, qh, kh, None, ws_f, workloads.EPS,
+                       workloads.ROPE_BASE, stream)
+        nc.nc_attn_bwd(qd_, kd_, vd_, None, out, lse, qh, kh, do_, dq_, dk_, dv_, ws_b, workloads.EPS,
+                       workloads.ROPE_BASE, stream)
+        for h_, d_ in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            h_.copy_(d_, non_blocking=True)
+
+    n = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    nbytes = q.numel() * 2
+    return {"value": round(w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 3 * nbytes, "ms_per_step": round(ms, 3),
+            "steps": n}
+
+
+# ------------------------------------------------------ CPU oracle legs ----
+
+def oracle_sample(n_slices: int):
+    """Time the fp64 oracle on `n_slices` whole (b, h) slices of the d20
+    workload (fwd + bwd); returns (TFLOP/s, seconds, threads)."""
+    import oracle
+    w = workloads.D20
+    q, k, v, dout = workloads.workload_inputs(w)
+    picks = [(i % w.B, (i * 7) % w.H) for i in range(n_slices)]
+    qs = torch.stack([q[b, :, h] for b, h in picks]).unsqueeze(2)
+    ks = torch.stack([k[b, :, h] for b, h in picks]).unsqueeze(2)
+    vs = torch.stack([v[b, :, h] for b, h in picks]).unsqueeze(2)
+    ds = torch.stack([dout[b, :, h] for b, h in picks]).unsqueeze(2)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(qs, ks, vs, eps=workloads.EPS, base=workloads.ROPE_BASE)
+    oracle.attn_bwd(qs, ks, vs, ds, eps=workloads.EPS, base=workloads.ROPE_BASE)
+    dt = time.perf_counter() - t0
+    flops = w.fwd_bwd_flops() * n_slices / (w.B * w.H)
+    return flops / dt / 1e12, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline():
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    n = min(cores, 64)
+    tf, dt = oracle_sample(n)
+    return {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole (b,h) slices of d20 (T=2048, D=128) fwd+bwd, fp64, {dt:.1f} s"}
+
+
+def bench_reference(args, ws_n, rank):
+    if rank != 0:
+        return None
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    import oracle
+    oracle.build()
+    # one slice costs ~5 s on one core; keep the whole run to a few minutes
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    n = min(cores, 64) if budget >= 12.0 else 1
+    for _ in range(args.warmup):
+        oracle_sample(n)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        tf, dt = oracle_sample(n)
+        vals.append(tf)
+        secs += dt
+    value = args.steps / sum(1.0 / x for x in vals)
+    return {
+        "impl": "reference",
+        "metric": "causal attn fwd+bwd TFLOP/s (% bf16 peak) at d20; decode GB/s (% HBM peak)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, d20 shapes)",
+        "config": {"workload": "d20 block attention fwd+bwd: B=32 T=2048 H=10 D=128, causal, "
+                               "QK RMSNorm eps=1e-6, RoPE base 10000", "B": 32, "T": 2048, "H": 10, "D": 128},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} whole (b,h) slice(s) of d20 per step, fp64 C oracle"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws_n, rank, local = dist_env()
+    if args.impl == "reference":
+        line = bench_reference(args, ws_n, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if ws_n > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        line = bench_ours(args, ws_n, rank, local)
+        if line is not None:
+            if ws_n == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline()
+            print(json.dumps(line), flush=True)
+    finally:
+        if ws_n > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

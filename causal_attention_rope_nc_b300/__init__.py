@@ -1,0 +1,209 @@
+"""B300 (sm_103a) causal attention with QK RMSNorm and RoPE -- Python binding.
+
+This module only marshals torch tensors to the C ABI of ``libncattn.so``
+(declared in ``include/ncattn.h``); every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+the import fails, and every call checks the status the library returns.
+
+The functions named ``nc_*`` mirror the C entry points one to one (torch
+tensors in place of pointers, the current CUDA stream by default).  The
+``attn_*`` helpers allocate outputs and workspaces with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libncattn.so")
+
+NC_OK, NC_EINVAL, NC_EUNSUPPORTED, NC_ELAUNCH, NC_EDEVICE = 0, -1, -2, -3, -4
+NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE = 0, 1, 2, 3
+
+EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
+            "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
+            "nc_attn_decode", "nc_profile_enable", "nc_profile_read")
+
+
+class NcError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        extra = ""
+        if code == NC_ELAUNCH:
+            extra = f" (cudaError {lib.nc_last_cuda_error()})"
+        super().__init__(f"{what}: {lib.nc_strerror(code).decode()} [{code}]{extra}")
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, F, S, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    L.nc_version.restype = I
+    L.nc_strerror.argtypes = [I]
+    L.nc_strerror.restype = ctypes.c_char_p
+    L.nc_last_cuda_error.restype = I
+    L.nc_device_status.argtypes = [S, ctypes.POINTER(ctypes.c_uint)]
+    L.nc_device_status.restype = I
+    L.nc_attn_workspace_size.argtypes = [I, I, I, I, I]
+    L.nc_attn_workspace_size.restype = SZ
+    L.nc_qk_norm_rope.argtypes = [P, P, P, P, P, SZ, I, I, I, I, F, F, S]
+    L.nc_qk_norm_rope.restype = I
+    L.nc_attn_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, S]
+    L.nc_attn_fwd.restype = I
+    L.nc_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, S]
+    L.nc_attn_bwd.restype = I
+    L.nc_attn_decode.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, S]
+    L.nc_attn_decode.restype = I
+    L.nc_profile_enable.argtypes = [I]
+    L.nc_profile_enable.restype = I
+    L.nc_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, ctypes.POINTER(I)]
+    L.nc_profile_read.restype = I
+    return L
+
+
+lib = _load()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, what: str):
+    if rc != NC_OK:
+        raise NcError(rc, what)
+
+
+def _bf16(t, name, dtype=torch.bfloat16):
+    if t is None:
+        return
+    if t.dtype != dtype or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def _f16(t, name):
+    _bf16(t, name, torch.float16)
+
+
+def workspace_size(op: int, B: int, T: int, H: int, D: int) -> int:
+    return int(lib.nc_attn_workspace_size(op, B, T, H, D))
+
+
+def new_workspace(op: int, B: int, T: int, H: int, D: int, device=None) -> torch.Tensor:
+    """Zero-filled workspace (torch allocations are 256-byte aligned)."""
+    n = max(workspace_size(op, B, T, H, D), 1)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def device_status(stream=None) -> int:
+    st = ctypes.c_uint(0)
+    _check(lib.nc_device_status(_stream(stream), ctypes.byref(st)), "nc_device_status")
+    return st.value
+
+
+def nc_profile_enable(on: bool):
+    _check(lib.nc_profile_enable(1 if on else 0), "nc_profile_enable")
+
+
+def nc_profile_read() -> dict:
+    """{kernel name: (launches, total ms)} since the last read."""
+    buf = (KernelTime * 64)()
+    n = ctypes.c_int(0)
+    _check(lib.nc_profile_read(buf, 64, ctypes.byref(n)), "nc_profile_read")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, 64))}
+
+
+# ------------------------------------------------------ C entry points 1:1 --
+
+def nc_qk_norm_rope(x, pos, xhat, rstd, workspace, eps, rope_base, stream=None):
+    _bf16(x, "x"), _f16(xhat, "xhat")
+    B, T, H, D = x.shape
+    _check(lib.nc_qk_norm_rope(_ptr(x), _ptr(pos), _ptr(xhat), _ptr(rstd), _ptr(workspace),
+                               workspace.numel(), B, T, H, D, eps, rope_base, _stream(stream)),
+           "nc_qk_norm_rope")
+
+
+def nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, stream=None):
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _bf16(t, n)
+    _f16(qhat, "qhat"), _f16(khat, "khat")
+    B, T, H, D = q.shape
+    _check(lib.nc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat),
+                           _ptr(khat), _ptr(rstd), _ptr(workspace), workspace.numel(), B, T, H, D,
+                           eps, rope_base, _stream(stream)), "nc_attn_fwd")
+
+
+def nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base,
+                stream=None):
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout), ("dq", dq), ("dk", dk),
+                 ("dv", dv)):
+        _bf16(t, n)
+    _f16(qhat, "qhat"), _f16(khat, "khat")
+    B, T, H, D = q.shape
+    _check(lib.nc_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat),
+                           _ptr(khat), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                           workspace.numel(), B, T, H, D, eps, rope_base, _stream(stream)),
+           "nc_attn_bwd")
+
+
+def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, stream=None):
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
+        _bf16(t, n)
+    _f16(kcache, "kcache")
+    B, Tcap, H, D = kcache.shape
+    _check(lib.nc_attn_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                              _ptr(lens), _ptr(out), _ptr(workspace), workspace.numel(), B, H, D, Tcap,
+                              eps, rope_base, _stream(stream)), "nc_attn_decode")
+
+
+# -------------------------------------------------------- allocating helpers --
+
+def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, stream=None):
+    """Returns (out, lse, qhat, khat)."""
+    B, T, H, D = q.shape
+    out = torch.empty_like(q)
+    qhat = torch.empty_like(q, dtype=torch.float16)
+    khat = torch.empty_like(k, dtype=torch.float16)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    ws = workspace if workspace is not None else new_workspace(NC_OP_FWD, B, T, H, D, q.device)
+    nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, stream)
+    return out, lse, qhat, khat
+
+
+def attn_bwd(q, k, v, out, lse, qhat, khat, dout, pos=None, eps=1e-6, rope_base=10000.0,
+             workspace=None, stream=None):
+    """Returns (dq, dk, dv)."""
+    B, T, H, D = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace if workspace is not None else new_workspace(NC_OP_BWD, B, T, H, D, q.device)
+    nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, stream)
+    return dq, dk, dv
+
+
+def qk_norm_rope(x, pos=None, eps=1e-6, rope_base=10000.0, stream=None):
+    B, T, H, D = x.shape
+    xhat = torch.empty_like(x, dtype=torch.float16)
+    ws = new_workspace(NC_OP_NORM_ROPE, B, T, H, D, x.device)
+    nc_qk_norm_rope(x, pos, xhat, None, ws, eps, rope_base, stream)
+    return xhat
+
+
+def attn_decode(q, kcache, vcache, lens, k_new=None, v_new=None, eps=1e-6, rope_base=10000.0,
+                workspace=None, stream=None):
+    B, Tcap, H, D = kcache.shape
+    out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
+    ws = workspace if workspace is not None else new_workspace(NC_OP_DECODE, B, Tcap, H, D, q.device)
+    nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, stream)
+    return out

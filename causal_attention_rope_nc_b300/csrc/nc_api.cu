@@ -1,0 +1,482 @@
+// C ABI of the attention library: argument checks, TMA descriptors and
+// kernel launches.  See include/ncattn.h for the contract of each call.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ncattn.h"
+#include "nc_bwd.cuh"
+#include "nc_common.cuh"
+#include "nc_decode.cuh"
+#include "nc_fwd.cuh"
+#include "nc_rowops.cuh"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+// Per-device one-time set-up: architecture check and shared-memory opt-in.
+int device_ready() {
+    static std::mutex mu;
+    static int state[kMaxDevices];  // 0 unknown, 1 ready, <0 error code
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        t_last_cuda_error = static_cast<int>(e);
+        return NC_EDEVICE;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (state[dev] != 0) return state[dev] == 1 ? NC_OK : state[dev];
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+        state[dev] = NC_EUNSUPPORTED;
+        return NC_EUNSUPPORTED;
+    }
+    if (!encode_fn()) {
+        state[dev] = NC_EDEVICE;
+        return NC_EDEVICE;
+    }
+    cudaError_t r = cudaSuccess;
+    auto optin = [&](const void* f, int bytes) {
+        cudaError_t x = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (x != cudaSuccess) r = x;
+    };
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64>), nc::fwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128>), nc::fwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_kernel<64>), nc::bwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_kernel<128>), nc::bwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<64>), nc::dec::MAX_SMEM);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<128>), nc::dec::MAX_SMEM);
+    if (r != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(r);
+        state[dev] = NC_ELAUNCH;
+        return NC_ELAUNCH;
+    }
+    state[dev] = 1;
+    return NC_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return NC_ELAUNCH;
+    }
+    return NC_OK;
+}
+
+// ---- optional per-kernel timing: CUDA events around every launch ----
+struct ProfRec {
+    const char* name;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Brackets one kernel launch on `s` when timing is enabled.
+struct ProfScope {
+    const char* name;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr;
+    ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
+        if (!g_prof_on) return;
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        a = prof_event();
+        cudaEventRecord(a, s);
+    }
+    ~ProfScope() {
+        if (!a) return;
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        cudaEvent_t b = prof_event();
+        cudaEventRecord(b, s);
+        g_prof_recs.push_back({name, a, b});
+    }
+};
+
+constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+
+// [B][T][H][D] 16-bit tensor, boxes of 64 head-dim values x `rows` tokens of
+// one (b, h), 128-byte swizzled.  Rows past T read as zero.
+int make_tmap(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D, int rows,
+              CUtensorMapDataType dt = kBF16) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                   static_cast<cuuint64_t>(T) * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode_fn()(tm, dt, 4, const_cast<void*>(ptr), dims, strides, box,
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
+bool shape_ok(int B, int T, int H, int D) {
+    return B >= 0 && T >= 0 && H >= 0 && (D == 64 || D == 128) && B <= 65535 && H <= 65535 &&
+           T <= (1 << 24);
+}
+
+bool params_ok(float eps, float base) { return std::isfinite(eps) && eps >= 0.f && std::isfinite(base) && base > 0.f; }
+
+size_t tab_bytes(int T, int D) { return up256(static_cast<size_t>(T) * (D / 2) * sizeof(float2)); }
+int tpad_of(int T) { return ((T + nc::bwd::BM - 1) / nc::bwd::BM) * nc::bwd::BM; }
+
+int rows_grid(long long rows, int D) {
+    const long long groups = 256 / (D / 8);
+    long long g = (rows + groups - 1) / groups;
+    if (g > 148LL * 16) g = 148LL * 16;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base, cudaStream_t s) {
+    const long long n = static_cast<long long>(T) * (D / 2);
+    int grid = static_cast<int>((n + 255) / 256);
+    if (grid > 148 * 8) grid = 148 * 8;
+    ProfScope ps("rope_table", s);
+    nc::rope_table_kernel<<<grid, 256, (D / 2) * sizeof(double), s>>>(tab, pos, T, D, std::log2(double(base)));
+    return launch_status();
+}
+
+template <int D>
+int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_bf16* qh, nc_bf16* kh, float* rstd,
+                     int B, int T, int H, float eps, cudaStream_t s) {
+    const long long rows = static_cast<long long>(B) * T * H;
+    ProfScope ps("qk_norm_rope", s);
+    nc::qk_norm_rope_kernel<D><<<rows_grid(rows * (k ? 2 : 1), D), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
+        reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, rows, T, H, eps);
+    return launch_status();
+}
+
+template <int D>
+int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
+             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, float eps, float base,
+             cudaStream_t s) {
+    float2* tab = reinterpret_cast<float2*>(ws);
+    int rc = launch_rope_table(tab, pos, T, D, base, s);
+    if (rc) return rc;
+    rc = launch_norm_rope<D>(q, k, tab, qhat, khat, rstd, B, T, H, eps, s);
+    if (rc) return rc;
+    CUtensorMap tq, tk, tv;
+    if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::fwd::BN, kF16) ||
+        make_tmap(&tv, v, B, T, H, D, nc::fwd::BN))
+        return NC_EINVAL;
+    const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
+    const double scale = 1.0 / std::sqrt(double(D));
+    const double log2e = 1.4426950408889634;
+    const double mfix = std::sqrt(double(D)) * 1.0079;
+    dim3 grid(n_qt, H, B);
+    ProfScope ps("attn_fwd", s);
+    nc::fwd::attn_fwd_kernel<D><<<grid, nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
+        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, n_qt, float(scale * log2e),
+        float(mfix * log2e), float(mfix));
+    return launch_status();
+}
+
+template <int D>
+int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
+             const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+             nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, float eps, float base, cudaStream_t s) {
+    const int Tpad = tpad_of(T);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    float2* tab = reinterpret_cast<float2*>(w);
+    w += tab_bytes(T, D);
+    float* delta = reinterpret_cast<float*>(w);
+    w += up256(static_cast<size_t>(B) * H * Tpad * 4);
+    float* lse2 = reinterpret_cast<float*>(w);
+    w += up256(static_cast<size_t>(B) * H * Tpad * 4);
+    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||out_t||
+    w += 256;
+    float* dq_acc = reinterpret_cast<float*>(w);
+    int rc = launch_rope_table(tab, pos, T, D, base, s);
+    if (rc) return rc;
+    if (cudaMemsetAsync(gmax, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    const long long rows = static_cast<long long>(B) * T * H;
+    {
+        ProfScope ps("attn_bwd_pre", s);
+        nc::bwd_pre_kernel<D><<<rows_grid(rows, D), 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout), lse, delta,
+            lse2, dq_acc, gmax, B, T, H, Tpad);
+    }
+    if ((rc = launch_status())) return rc;
+    CUtensorMap tq, tk, tv, tdo;
+    if (make_tmap(&tq, qhat, B, T, H, D, nc::bwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::bwd::BN, kF16) ||
+        make_tmap(&tv, v, B, T, H, D, nc::bwd::BN) || make_tmap(&tdo, dout, B, T, H, D, nc::bwd::BM))
+        return NC_EINVAL;
+    const int n_kt = (T + nc::bwd::BN - 1) / nc::bwd::BN;
+    const double scale = 1.0 / std::sqrt(double(D));
+    dim3 grid(n_kt, H, B);
+    {
+        ProfScope ps("attn_bwd", s);
+        nc::bwd::attn_bwd_kernel<D><<<grid, nc::bwd::NUM_THREADS, nc::bwd::Smem<D>::ALLOC, s>>>(
+            tq, tk, tv, tdo, lse2, delta, dq_acc, gmax, reinterpret_cast<const __nv_bfloat16*>(k), tab,
+            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, Tpad, float(scale),
+            float(scale * 1.4426950408889634), eps);
+    }
+    if ((rc = launch_status())) return rc;
+    {
+        ProfScope ps("attn_dq_finalize", s);
+        nc::dq_finalize_kernel<D><<<rows_grid(rows, D), 256, 0, s>>>(
+            dq_acc, reinterpret_cast<const __nv_bfloat16*>(q), tab, reinterpret_cast<__nv_bfloat16*>(dq), rows, T,
+            H, eps);
+    }
+    return launch_status();
+}
+
+struct DecodeWs {
+    float* part_o;
+    float* part_ml;
+    unsigned int* counters;
+};
+
+size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base) {
+    const int nch = (Tcap + nc::dec::CHUNK - 1) / nc::dec::CHUNK;
+    const size_t o_bytes = up256(static_cast<size_t>(B) * nch * H * D * 4);
+    const size_t ml_bytes = up256(static_cast<size_t>(B) * nch * H * 2 * 4);
+    const size_t c_bytes = up256(static_cast<size_t>(B) * 4);
+    if (out) {
+        uint8_t* w = reinterpret_cast<uint8_t*>(base);
+        out->counters = reinterpret_cast<unsigned int*>(w);
+        out->part_ml = reinterpret_cast<float*>(w + c_bytes);
+        out->part_o = reinterpret_cast<float*>(w + c_bytes + ml_bytes);
+    }
+    return c_bytes + ml_bytes + o_bytes;
+}
+
+template <int D>
+int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
+                const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
+                cudaStream_t s) {
+    const int nch = (Tcap + nc::dec::CHUNK - 1) / nc::dec::CHUNK;
+    const int xt = nc::dec::Shape<D>::xthreads(H);
+    const int ks = nc::dec::Shape<D>::slices(H);
+    dim3 block(xt, ks);
+    dim3 grid(nch, B);
+    const size_t smem = static_cast<size_t>(H) * D * 4 + (D / 2) * 8 + static_cast<size_t>(ks) * xt * 10 * 4;
+    const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
+    ProfScope ps("attn_decode", s);
+    nc::dec::attn_decode_kernel<D><<<grid, block, smem, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
+        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
+        reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
+        ws.part_ml, ws.counters, H, Tcap, nch, eps, std::log2(double(base)), float(scale_log2));
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int nc_version(void) { return (0 << 16) | 1; }
+
+const char* nc_strerror(int code) {
+    switch (code) {
+        case NC_OK: return "ok";
+        case NC_EINVAL: return "invalid argument";
+        case NC_EUNSUPPORTED: return "unsupported device (needs sm_103)";
+        case NC_ELAUNCH: return "CUDA launch failed";
+        case NC_EDEVICE: return "CUDA device unavailable";
+        default: return "unknown error";
+    }
+}
+
+int nc_last_cuda_error(void) { return t_last_cuda_error; }
+
+int nc_profile_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_on = on != 0;
+    return NC_OK;
+}
+
+int nc_profile_read(nc_kernel_time* out, int max_entries, int* n_entries) {
+    if (!n_entries || (max_entries > 0 && !out)) return NC_EINVAL;
+    std::vector<ProfRec> recs;
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        recs.swap(g_prof_recs);
+    }
+    std::vector<nc_kernel_time> acc;
+    int rc = NC_OK;
+    for (const ProfRec& r : recs) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+        if (e != cudaSuccess) {
+            t_last_cuda_error = static_cast<int>(e);
+            rc = NC_ELAUNCH;
+        }
+        size_t i = 0;
+        while (i < acc.size() && std::strcmp(acc[i].name, r.name) != 0) ++i;
+        if (i == acc.size()) {
+            nc_kernel_time z;
+            std::memset(&z, 0, sizeof(z));
+            std::strncpy(z.name, r.name, sizeof(z.name) - 1);
+            acc.push_back(z);
+        }
+        acc[i].launches += 1;
+        acc[i].total_ms += ms;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        for (const ProfRec& r : recs) {
+            g_prof_pool.push_back(r.a);
+            g_prof_pool.push_back(r.b);
+        }
+    }
+    const int n = static_cast<int>(acc.size());
+    for (int i = 0; i < n && i < max_entries; ++i) out[i] = acc[i];
+    *n_entries = n;
+    return rc;
+}
+
+int nc_device_status(nc_stream_t stream, unsigned int* status) {
+    if (!status) return NC_EINVAL;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    unsigned int v = 0, zero = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, nc::g_dev_status, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(nc::g_dev_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return NC_ELAUNCH;
+    }
+    *status = v;
+    return NC_OK;
+}
+
+size_t nc_attn_workspace_size(int op, int B, int T, int H, int D) {
+    if (!shape_ok(B, T, H, D)) return 0;
+    switch (op) {
+        case NC_OP_NORM_ROPE:
+        case NC_OP_FWD: return tab_bytes(T, D);
+        case NC_OP_BWD: {
+            const int Tpad = tpad_of(T);
+            return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256 +
+                   up256(static_cast<size_t>(B) * T * H * D * 4);
+        }
+        case NC_OP_DECODE: return decode_ws_layout(B, H, D, T, nullptr, nullptr);
+        default: return 0;
+    }
+}
+
+int nc_qk_norm_rope(const nc_bf16* x, const int32_t* pos, nc_bf16* xhat, float* rstd, void* workspace,
+                    size_t workspace_bytes, int B, int T, int H, int D, float eps, float rope_base,
+                    nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    if (B == 0 || T == 0 || H == 0) return NC_OK;
+    if (!x || !xhat || !workspace || !aligned16(x) || !aligned16(xhat) || !aligned256(workspace)) return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_NORM_ROPE, B, T, H, D)) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float2* tab = reinterpret_cast<float2*>(workspace);
+    if ((rc = launch_rope_table(tab, pos, T, D, rope_base, s))) return rc;
+    return D == 64 ? launch_norm_rope<64>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, eps, s)
+                   : launch_norm_rope<128>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, eps, s);
+}
+
+int nc_attn_fwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
+                float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
+                int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    if (B == 0 || T == 0 || H == 0) return NC_OK;
+    if (!q || !k || !v || !out || !lse || !qhat || !khat || !workspace) return NC_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(qhat) || !aligned16(khat) ||
+        !aligned256(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_FWD, B, T, H, D)) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return D == 64 ? fwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, s)
+                   : fwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, s);
+}
+
+int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
+                const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+                nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
+                float eps, float rope_base, nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    if (B == 0 || T == 0 || H == 0) return NC_OK;
+    if (!q || !k || !v || !out || !lse || !qhat || !khat || !dout || !dq || !dk || !dv || !workspace)
+        return NC_EINVAL;
+    const void* b16[] = {q, k, v, out, qhat, khat, dout, dq, dk, dv};
+    for (const void* p : b16)
+        if (!aligned16(p)) return NC_EINVAL;
+    if (!aligned256(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_BWD, B, T, H, D)) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return D == 64 ? bwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
+                                  rope_base, s)
+                   : bwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
+                                   rope_base, s);
+}
+
+int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
+                   const int32_t* lens, nc_bf16* out, void* workspace, size_t workspace_bytes, int B, int H, int D,
+                   int Tcap, float eps, float rope_base, nc_stream_t stream) {
+    if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    if (B == 0 || H == 0 || Tcap == 0) return NC_OK;
+    if (!q || !kcache || !vcache || !lens || !out || !workspace) return NC_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return NC_EINVAL;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out) || !aligned256(workspace) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (reinterpret_cast<uintptr_t>(lens) & 3u))
+        return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D)) return NC_EINVAL;
+    const int ks = D == 64 ? nc::dec::Shape<64>::slices(H) : nc::dec::Shape<128>::slices(H);
+    if (ks == 0) return NC_EINVAL;  // H*D/8 > 512: too many heads for one CTA per chunk
+    int rc = device_ready();
+    if (rc) return rc;
+    DecodeWs ws;
+    decode_ws_layout(B, H, D, Tcap, &ws, workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,283 @@
+// Memory-bound per-row kernels of the attention path.
+//
+// Every kernel here treats a head vector of D bf16 values as one "row" and
+// gives it D/8 consecutive lanes (16 bytes per lane), so a warp streams
+// whole 256-byte rows with 16-byte loads and the per-row reductions are
+// lane shuffles.  The rotate-half RoPE partner of element i (i + D/2) is
+// held by the lane D/16 positions away, one xor-shuffle from it.
+#pragma once
+
+#include "nc_common.cuh"
+
+namespace nc {
+
+template <int D>
+struct RowLanes {
+    static constexpr int LPR = D / 8;        // lanes per row
+    static constexpr int HALF = LPR / 2;     // lane distance to the RoPE partner
+    static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = unpack_bf16x2(w[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float (&x)[8]) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+__device__ __forceinline__ uint4 f32x8_to_f16(const float (&x)[8]) {
+    return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                      pack_f16x2(x[6], x[7]));
+}
+
+__device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = unpack_f16x2(w[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// Sum over the LPR lanes of a row group (groups are aligned, so the xor
+// partners never leave the group).
+template <int LPR>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------ RoPE table --
+// tab[t][i] = (cos, sin) of angle pos[t] * base^(-2i/D), t < T, i < D/2.
+// pos == nullptr means pos[t] = t.
+__global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restrict__ pos, int T, int D,
+                                  double log2_base) {
+    extern __shared__ double s_theta[];  // D/2 entries
+    const int half = D / 2;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) s_theta[i] = rope_theta(i, D, log2_base);
+    __syncthreads();
+    const long long n = static_cast<long long>(T) * half;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(e / half), i = static_cast<int>(e % half);
+        const int p = pos ? pos[t] : t;
+        tab[e] = rope_cos_sin(p, s_theta[i]);
+    }
+}
+
+// ------------------------------------------------- QK RMSNorm + RoPE (K1) --
+// qhat = RoPE(q / sqrt(mean(q^2) + eps)), same for k (k may be null: one
+// tensor only), stored as IEEE fp16: the norm bounds every element by
+// sqrt(D) <= 11.4, well inside fp16's range, and fp16 keeps 3 more mantissa
+// bits than bf16 for the score products.  Rows are enumerated q rows first,
+// then k rows, each in memory order ((b*T + t)*H + h).  rstd (optional)
+// receives 1/r, laid out [2][B][T][H] (q then k).
+template <int D>
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
+                                                           const __nv_bfloat16* __restrict__ k,
+                                                           const float2* __restrict__ tab,
+                                                           __half* __restrict__ qhat,
+                                                           __half* __restrict__ khat,
+                                                           float* __restrict__ rstd, long long rows_per_tensor,
+                                                           int T, int H, float eps) {
+    using L = RowLanes<D>;
+    const int sub = threadIdx.x % L::LPR;
+    const long long groups = blockDim.x / L::LPR;
+    const long long nrows = (k ? 2 : 1) * rows_per_tensor;
+    // every lane of a warp runs the same number of iterations (shuffles)
+    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
+    const long long stride = static_cast<long long>(gridDim.x) * groups;
+    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
+    for (long long base = warp_first, row = first; base < nrows; base += stride, row += stride) {
+        const bool valid = row < nrows;
+        const bool is_k = valid && row >= rows_per_tensor;
+        const long long r = valid ? (is_k ? row - rows_per_tensor : row) : 0;
+        const int t = static_cast<int>((r / H) % T);
+        float x[8];
+        if (valid) {
+            const __nv_bfloat16* src = (is_k ? k : q) + r * D + sub * 8;
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(src), x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        ss = group_sum<L::LPR>(ss);
+        const float rs = rsqrtf(ss / D + eps);
+        float y[8], o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= rs;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], L::HALF);
+        const int i0 = (sub % L::HALF) * 8;
+        const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
+        const bool lo = sub < L::HALF;
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+            const float4 cs = valid ? cs4[e2] : make_float4(1.f, 0.f, 1.f, 0.f);
+            const float c0 = cs.x, s0 = cs.y, c1 = cs.z, s1 = cs.w;
+            const int e = 2 * e2;
+            // low half holds a = x_i (partner b = x_{i+D/2}); high half the reverse
+            o[e] = lo ? x[e] * c0 - y[e] * s0 : y[e] * s0 + x[e] * c0;
+            o[e + 1] = lo ? x[e + 1] * c1 - y[e + 1] * s1 : y[e + 1] * s1 + x[e + 1] * c1;
+        }
+        if (valid) {
+            *reinterpret_cast<uint4*>((is_k ? khat : qhat) + r * D + sub * 8) = f32x8_to_f16(o);
+            if (rstd && sub == 0) rstd[(is_k ? rows_per_tensor : 0) + r] = rs;
+        }
+    }
+}
+
+// -------------------------------------------------- backward preprocess ----
+// delta[b][h][t] = <dout_t, out_t> (fp32), lse2[b][h][t] = lse * log2(e),
+// both padded to Tpad columns (delta 0, lse2 +inf beyond T so that padded
+// query rows get probability 0); dq_acc rows are zeroed.  gmax[0] and
+// gmax[1] receive the largest row norms ||dout_t|| and ||out_t|| over the
+// whole tensor (they must be zero on entry); the backward bounds dS with them.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      const float* __restrict__ lse, float* __restrict__ delta,
+                                                      float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                      unsigned int* __restrict__ gmax, int B, int T, int H,
+                                                      int Tpad) {
+    using L = RowLanes<D>;
+    __shared__ float s_max[2][32];
+    const int sub = threadIdx.x % L::LPR;
+    const long long groups = blockDim.x / L::LPR;
+    const long long nrows = static_cast<long long>(B) * T * H;
+    const long long stride = static_cast<long long>(gridDim.x) * groups;
+    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
+    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
+    float mx_do = 0.f, mx_o = 0.f;  // squared norms
+    for (long long base = warp_first, r = first; base < nrows; base += stride, r += stride) {
+        const bool valid = r < nrows;
+        float acc = 0.f, sdo = 0.f, so = 0.f;
+        if (valid) {
+            float a[8], g[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(out + r * D + sub * 8), a);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(dout + r * D + sub * 8), g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc = fmaf(a[e], g[e], acc);
+                sdo = fmaf(g[e], g[e], sdo);
+                so = fmaf(a[e], a[e], so);
+            }
+            float4* z = reinterpret_cast<float4*>(dq_acc + r * D + sub * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        acc = group_sum<L::LPR>(acc);
+        mx_do = fmaxf(mx_do, group_sum<L::LPR>(sdo));
+        mx_o = fmaxf(mx_o, group_sum<L::LPR>(so));
+        if (valid && sub == 0) {
+            const int h = static_cast<int>(r % H);
+            const long long bt = r / H;
+            const int t = static_cast<int>(bt % T);
+            const int b = static_cast<int>(bt / T);
+            const long long o = (static_cast<long long>(b) * H + h) * Tpad + t;
+            delta[o] = acc;
+            lse2[o] = lse[(static_cast<long long>(b) * H + h) * T + t] * 1.4426950408889634f;
+        }
+    }
+    // block maximum of the row norms, one atomic per block (non-negative
+    // floats order like their bit patterns)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx_do = fmaxf(mx_do, __shfl_xor_sync(0xffffffffu, mx_do, o));
+        mx_o = fmaxf(mx_o, __shfl_xor_sync(0xffffffffu, mx_o, o));
+    }
+    const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        s_max[0][wid] = mx_do;
+        s_max[1][wid] = mx_o;
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        float m = 0.f;
+        for (int w = 0; w < nw; ++w) m = fmaxf(m, s_max[threadIdx.x][w]);
+        atomicMax(gmax + threadIdx.x, __float_as_uint(sqrtf(m)));
+    }
+    // padding columns t in [T, Tpad)
+    const int padw = Tpad - T;
+    const long long npad = static_cast<long long>(B) * H * padw;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < npad;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long bh = e / padw;
+        const long long o = bh * Tpad + T + (e % padw);
+        delta[o] = 0.f;
+        lse2[o] = __int_as_float(0x7f800000);  // +inf
+    }
+}
+
+// -------------------------------------------- dQ: RoPE^T + RMSNorm bwd -----
+// dq = (u - y <u, y> / D) / r with u = R(pos)^T g, g = dq_acc row (already
+// scaled by 1/sqrt(D)), y = q / r the normalised query before rotation.
+template <int D>
+__global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ dq_acc,
+                                                          const __nv_bfloat16* __restrict__ q,
+                                                          const float2* __restrict__ tab,
+                                                          __nv_bfloat16* __restrict__ dq, long long nrows, int T,
+                                                          int H, float eps) {
+    using L = RowLanes<D>;
+    const int sub = threadIdx.x % L::LPR;
+    const long long groups = blockDim.x / L::LPR;
+    const long long stride = static_cast<long long>(gridDim.x) * groups;
+    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
+    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
+    for (long long base = warp_first, r = first; base < nrows; base += stride, r += stride) {
+        const bool valid = r < nrows;
+        const long long rr = valid ? r : 0;
+        const int t = static_cast<int>((rr / H) % T);
+        float x[8], g[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(q + rr * D + sub * 8), x);
+        const float4* gp = reinterpret_cast<const float4*>(dq_acc + rr * D + sub * 8);
+        const float4 g0 = gp[0], g1 = gp[1];
+        g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+        g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        ss = group_sum<L::LPR>(ss);
+        const float rs = rsqrtf(ss / D + eps);
+        float pg[8], u[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pg[e] = __shfl_xor_sync(0xffffffffu, g[e], L::HALF);
+        const int i0 = (sub % L::HALF) * 8;
+        const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
+        const bool lo = sub < L::HALF;
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+            const float4 cs = cs4[e2];
+            const float c[2] = {cs.x, cs.z}, s[2] = {cs.y, cs.w};
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = 2 * e2 + k2;
+                // R^T: (a, b) -> (a c + b s, -a s + b c)
+                u[e] = lo ? g[e] * c[k2] + pg[e] * s[k2] : -pg[e] * s[k2] + g[e] * c[k2];
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(u[e], x[e] * rs, dot);
+        dot = group_sum<L::LPR>(dot);
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (u[e] - x[e] * rs * (dot / D)) * rs;
+        if (valid) *reinterpret_cast<uint4*>(dq + r * D + sub * 8) = f32x8_to_bf16(o);
+    }
+}
+
+}  // namespace nc

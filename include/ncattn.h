@@ -1,0 +1,156 @@
+/*
+ * ncattn.h -- C ABI of the B300 (sm_103a) causal attention library with
+ * parameter-free QK RMSNorm and rotary position embeddings.
+ *
+ * The operation.  Per batch b, head h and head dimension D (64 or 128):
+ *   qhat_t = RoPE(q_t / sqrt(mean(q_t^2) + eps), pos_t),  khat_t likewise
+ *   out_i  = sum_{j <= i} softmax_j(qhat_i . khat_j / sqrt(D)) v_j
+ *   lse_i  = ln sum_{j <= i} exp(qhat_i . khat_j / sqrt(D))
+ * RoPE rotates the pair (x_i, x_{i+D/2}) by the angle pos * base^(-2i/D),
+ * i < D/2 (rotate-half pairing).
+ *
+ * Where it comes from.  nanochat's GPT block replaces positional embeddings
+ * with rotary embeddings and normalises queries and keys (QK-norm, RMSNorm
+ * without trainable parameters) before the dot product: ai.flicky.cc,
+ * "nanochat: свой ChatGPT от токенизатора до чата", section
+ * "Модель: что изменилось со времён GPT-2"; adg.csdn.net,
+ * "4小时100美元！...nanochat...", section "1. 极致精简的技术架构".  Attention
+ * runs through FlashAttention-3 with an SDPA fallback and generation uses a
+ * KV cache with prefill/decode (ai.flicky.cc, section "Карта репозитория";
+ * 7minutos.es "Andrej Karpathy lanza nanochat ...", section
+ * "Entrenamiento medio, SFT y uso de herramientas").  The pages give no
+ * formula; the pairing, the angle, eps placement and the per-head norm axis
+ * above are the plainest reading they support.
+ *
+ * Conventions for every entry point.
+ *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
+ *    pointer after the call returns and allocates no memory.  Scratch space
+ *    is the caller's `workspace` of at least nc_attn_workspace_size() bytes,
+ *    256-byte aligned.
+ *  - bf16 tensors are raw bfloat16 bits (nc_bf16), row-major and
+ *    contiguous: token tensors [B][T][H][D], lse [B][H][T] (fp32, natural
+ *    log), decode tensors [B][H][D], caches [B][Tcap][H][D].  Every 16-bit
+ *    tensor must be 16-byte aligned.
+ *  - Normalised, rotated queries and keys (qhat, khat, the decode key cache)
+ *    are IEEE fp16 (nc_f16): RMSNorm bounds each element by sqrt(D), well
+ *    inside fp16's range, and fp16 carries 3 more mantissa bits than bf16
+ *    into the score products.  Everything else is bf16.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising.
+ *  - Return value: NC_OK, or a negative code.  NC_EINVAL: a null pointer
+ *    where one is required, misalignment, D not 64/128, a negative size,
+ *    eps < 0, rope_base <= 0, or a workspace that is too small; nothing is
+ *    launched.  NC_EUNSUPPORTED: the current device is not sm_103.
+ *    NC_ELAUNCH: a CUDA launch failed; nc_last_cuda_error() gives the
+ *    cudaError_t.  A size of zero in B, T or H (Tcap for decode) is an empty
+ *    problem: NC_OK, nothing launched.
+ *  - Kernels never spin unboundedly: a pipeline wait that has not completed
+ *    after 2 s records a device-side status word and the kernel unwinds.
+ *    nc_device_status() reads and clears it.
+ */
+#ifndef NCATTN_H
+#define NCATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t nc_bf16;            /* raw bfloat16 bits */
+typedef uint16_t nc_f16;             /* raw IEEE binary16 bits */
+typedef struct CUstream_st *nc_stream_t; /* == cudaStream_t */
+
+#define NC_OK 0
+#define NC_EINVAL (-1)
+#define NC_EUNSUPPORTED (-2)
+#define NC_ELAUNCH (-3)
+#define NC_EDEVICE (-4)
+
+#define NC_OP_FWD 0
+#define NC_OP_BWD 1
+#define NC_OP_DECODE 2
+#define NC_OP_NORM_ROPE 3
+
+/* Library version, (major << 16) | minor. */
+int nc_version(void);
+
+/* Human-readable name of an NC_* code. */
+const char *nc_strerror(int code);
+
+/* cudaError_t of the last failed launch in this thread (0 if none). */
+int nc_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * the current device.  *status = 0 when no kernel has reported a failure,
+ * else (code << 16) | site with code 1 = a bounded wait timed out,
+ * 2 = a decode length outside [1, Tcap].  Returns NC_OK or NC_ELAUNCH. */
+int nc_device_status(nc_stream_t stream, unsigned int *status);
+
+/* Optional per-kernel timing.  While enabled (on != 0), every kernel the
+ * library launches is bracketed by two CUDA events recorded on the launch
+ * stream.  nc_profile_read() waits for the recorded events, writes up to
+ * max_entries per-kernel sums (launch count, total milliseconds) to `out`,
+ * sets *n_entries to the number of distinct kernels, and clears the
+ * record.  Timing does not change what the kernels compute. */
+typedef struct {
+    char name[48];
+    int launches;
+    double total_ms;
+} nc_kernel_time;
+
+int nc_profile_enable(int on);
+int nc_profile_read(nc_kernel_time *out, int max_entries, int *n_entries);
+
+/* Workspace bytes needed by an operation (op = NC_OP_*).  For
+ * NC_OP_DECODE pass T = Tcap.  The decode workspace holds per-stream
+ * counters that must be zero before the first call; every successful
+ * call leaves them at zero again. */
+size_t nc_attn_workspace_size(int op, int B, int T, int H, int D);
+
+/* QK RMSNorm + RoPE alone (prefill of a KV cache, or a check of the
+ * prologue): xhat = RoPE(x / sqrt(mean(x^2) + eps), pos) for x [B][T][H][D].
+ * xhat is fp16.  pos: [T] int32 positions, or NULL for 0..T-1.  rstd:
+ * optional [B][T][H] fp32 output of 1/sqrt(mean(x^2) + eps).
+ * Workspace: NC_OP_NORM_ROPE. */
+int nc_qk_norm_rope(const nc_bf16 *x, const int32_t *pos, nc_f16 *xhat, float *rstd, void *workspace,
+                    size_t workspace_bytes, int B, int T, int H, int D, float eps, float rope_base,
+                    nc_stream_t stream);
+
+/* Forward.  In: q, k, v [B][T][H][D]; pos [T] or NULL (0..T-1).
+ * Out: out [B][T][H][D]; lse [B][H][T]; qhat, khat [B][T][H][D] (the
+ * normalised, rotated q and k in fp16, kept for the backward); rstd
+ * optional [2][B][T][H] (q then k).  Scale 1/sqrt(D).  Workspace: NC_OP_FWD. */
+int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
+                float *lse, nc_f16 *qhat, nc_f16 *khat, float *rstd, void *workspace, size_t workspace_bytes,
+                int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream);
+
+/* Backward.  In: the forward's inputs q, k, v, pos, its outputs out, lse,
+ * qhat, khat, and the upstream gradient dout [B][T][H][D].  Out: dq, dk, dv
+ * [B][T][H][D] (gradients with respect to the RAW q, k, v: through the
+ * softmax, the RoPE rotation and the RMSNorm).  Workspace: NC_OP_BWD. */
+int nc_attn_bwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
+                const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
+                nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
+                float eps, float rope_base, nc_stream_t stream);
+
+/* Single-token decode over a KV cache.  Stream b holds lens[b] valid cache
+ * slots (1 <= lens[b] <= Tcap) INCLUDING the new token, whose position is
+ * lens[b]-1.  q [B][H][D] is the new token's raw query.  If k_new and v_new
+ * ([B][H][D], raw) are given, the new key is normalised and rotated and
+ * written with v_new into slot lens[b]-1 of kcache / vcache first;
+ * otherwise that slot must already hold them.  kcache (fp16) holds keys
+ * already normalised and rotated at their slot position (as
+ * nc_qk_norm_rope writes them); vcache (bf16) holds raw values.
+ * out [B][H][D] bf16.  Up to 512 / (D/8) heads (32 at D = 128).
+ * Workspace: NC_OP_DECODE with T = Tcap (zeroed once before first use). */
+int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+                   nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
+                   int B, int H, int D, int Tcap, float eps, float rope_base, nc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NCATTN_H */
