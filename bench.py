@@ -110,7 +110,7 @@ def bench_ours(args, ws_n, rank, local):
     import causal_attention_rope_nc_b300 as nc
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workloads.D20
+    w = workloads.ATTN_WORKLOADS[args.workload]
     B, T, H, D = w.B, w.T, w.H, w.D
     eps, base = workloads.EPS, workloads.ROPE_BASE
     # weak scaling: every rank runs its own d20 batch (seed offset by rank)
@@ -167,10 +167,11 @@ def bench_ours(args, ws_n, rank, local):
     value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
 
     # ---- decode (same rank, own timing; L2 flushed between calls) ----
-    dec = bench_decode(nc, dev, args, rank)
-
-    # ---- end to end through the public API with host buffers ----
-    e2e = bench_e2e(nc, dev, args, q, k, v, dout, ws_f, ws_b)
+    dec = e2e = None
+    if not args.no_extras:
+        dec = bench_decode(nc, dev, args, rank)
+        # ---- end to end through the public API with host buffers ----
+        e2e = bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b)
 
     if rank != 0:
         return None
@@ -209,7 +210,7 @@ def bench_ours(args, ws_n, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, d20 shapes)",
-        "config": {"workload": "d20 block attention fwd+bwd: B=32 T=2048 H=10 D=128, causal, "
+        "config": {"workload": f"{w.name} block attention fwd+bwd: B={B} T={T} H={H} D={D}, causal, "
                                "QK RMSNorm eps=1e-6, RoPE base 10000",
                    "B": B, "T": T, "H": H, "D": D, "parallelism": f"replicas x{ws_n} (batch shards)",
                    "l2": "inputs 671 MB > 126 MB L2; no flush between steps"},
@@ -265,10 +266,9 @@ def bench_decode(nc, dev, args, rank):
             "l2": "256 MB buffer written between calls", "tokens_per_s": round(w.B / (ms * 1e-3), 1)}
 
 
-def bench_e2e(nc, dev, args, q, k, v, dout, ws_f, ws_b):
+def bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b):
     """fwd+bwd through the public API with pinned host inputs: H2D of q, k, v,
     dout and D2H of dq, dk, dv inside the timed region."""
-    w = workloads.D20
     hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, dout))
     hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
     stream = torch.cuda.current_stream(dev)
@@ -381,6 +381,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(workloads.ATTN_WORKLOADS), default="d20",
+                    help="fwd+bwd shape (the headline metric is quoted on d20; others for profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the decode and end-to-end legs (short runs under a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

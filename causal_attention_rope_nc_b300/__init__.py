@@ -24,7 +24,8 @@ NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE = 0, 1, 2, 3
 
 EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
             "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
-            "nc_attn_decode", "nc_profile_enable", "nc_profile_read")
+            "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc")
+NC_ETOOLARGE = -5
 
 
 class NcError(RuntimeError):
@@ -65,6 +66,8 @@ def _load():
     L.nc_profile_enable.restype = I
     L.nc_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, ctypes.POINTER(I)]
     L.nc_profile_read.restype = I
+    L.nc_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, F, S]
+    L.nc_attn_decode_noalloc.restype = I
     return L
 
 
@@ -166,6 +169,18 @@ def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, r
     _check(lib.nc_attn_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
                               _ptr(lens), _ptr(out), _ptr(workspace), workspace.numel(), B, H, D, Tcap,
                               eps, rope_base, _stream(stream)), "nc_attn_decode")
+
+
+def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
+    """nc_attn_decode for callers that cannot supply a workspace (the library
+    keeps the scratch in a fixed 8 MiB device array; see include/ncattn.h)."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
+        _bf16(t, n)
+    _f16(kcache, "kcache")
+    B, Tcap, H, D = kcache.shape
+    _check(lib.nc_attn_decode_noalloc(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                                      _ptr(lens), _ptr(out), B, H, D, Tcap, eps, rope_base,
+                                      _stream(stream)), "nc_attn_decode_noalloc")
 
 
 # -------------------------------------------------------- allocating helpers --

@@ -320,6 +320,7 @@ const char* nc_strerror(int code) {
         case NC_EUNSUPPORTED: return "unsupported device (needs sm_103)";
         case NC_ELAUNCH: return "CUDA launch failed";
         case NC_EDEVICE: return "CUDA device unavailable";
+        case NC_ETOOLARGE: return "problem too large for the library's fixed decode scratch";
         default: return "unknown error";
     }
 }
@@ -475,6 +476,81 @@ int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new,
     DecodeWs ws;
     decode_ws_layout(B, H, D, Tcap, &ws, workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode with no device allocation at all.
+//
+// Some callers cannot hand the library a workspace: a serving loop that must
+// not call cudaMalloc between tokens (it synchronises the whole device and
+// stalls every stream), or a host application that owns all device memory
+// and lends none of it to plug-ins.  For them the decode keeps its scratch
+// (per-chunk partial results and per-stream arrival counters) in the fixed
+// array below, which exists once per device for as long as the library is
+// loaded.
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[NC_DECODE_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices];  // device address of g_decode_scratch, per device
+
+// Host code cannot use the array's name as a device address; look the
+// address up once per device, with that device current.
+int scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        t_last_cuda_error = static_cast<int>(e);
+        return NC_EDEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || !p) {
+            t_last_cuda_error = static_cast<int>(e);
+            return NC_EDEVICE;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return NC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_f16* kcache,
+                           nc_bf16* vcache, const int32_t* lens, nc_bf16* out, int B, int H, int D, int Tcap,
+                           float eps, float rope_base, nc_stream_t stream) {
+    if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    if (B == 0 || H == 0 || Tcap == 0) return NC_OK;
+    if (!q || !kcache || !vcache || !lens || !out) return NC_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return NC_EINVAL;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (reinterpret_cast<uintptr_t>(lens) & 3u))
+        return NC_EINVAL;
+    if (nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D) > NC_DECODE_NOALLOC_SCRATCH_BYTES)
+        return NC_ETOOLARGE;
+    const int ks = D == 64 ? nc::dec::Shape<64>::slices(H) : nc::dec::Shape<128>::slices(H);
+    if (ks == 0) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    void* scratch = nullptr;
+    if ((rc = scratch_address(&scratch))) return rc;
+    DecodeWs ws;
+    decode_ws_layout(B, H, D, Tcap, &ws, scratch);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the array keeps whatever the previous call left: the arrival counters
+    // must start from zero
+    if (cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), s) != cudaSuccess)
+        return launch_status();
     return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s)
                    : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s);
 }
