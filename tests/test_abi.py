@@ -19,7 +19,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from causal_attention_rope_nc_b300 import build as b
+    import __graft_entry__
+    b = __graft_entry__._build_module()
     b.build()
     return ctypes.CDLL(b.LIB)
 
