@@ -172,6 +172,24 @@ int rows_grid(long long rows, int D) {
     return static_cast<int>(g);
 }
 
+// One token per D/8-lane group, 256 threads per block: enough blocks for
+// every token, at most 8 resident blocks per SM for a grid-stride walk.
+int tok_grid(long long toks, int D) {
+    const long long groups = 256 / (D / 8);
+    long long g = (toks + groups - 1) / groups;
+    if (g > 148LL * 8) g = 148LL * 8;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+// (b, h) pairs per group of the grouped tile order: about two waves of
+// one-CTA-per-SM tiles.
+int tile_group(int n_t, int nbh) {
+    int g = (2 * 148 + n_t - 1) / n_t;
+    if (g > nbh) g = nbh;
+    return g < 1 ? 1 : g;
+}
+
 int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base, cudaStream_t s) {
     const long long n = static_cast<long long>(T) * (D / 2);
     int grid = static_cast<int>((n + 255) / 256);
@@ -184,11 +202,11 @@ int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base,
 template <int D>
 int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_bf16* qh, nc_bf16* kh, float* rstd,
                      int B, int T, int H, float eps, cudaStream_t s) {
-    const long long rows = static_cast<long long>(B) * T * H;
+    const long long toks = static_cast<long long>(B) * T;
     ProfScope ps("qk_norm_rope", s);
-    nc::qk_norm_rope_kernel<D><<<rows_grid(rows * (k ? 2 : 1), D), 256, 0, s>>>(
+    nc::qk_norm_rope_kernel<D><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
-        reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, rows, T, H, eps);
+        reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, toks, T, H, eps);
     return launch_status();
 }
 
@@ -209,10 +227,12 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     const double scale = 1.0 / std::sqrt(double(D));
     const double log2e = 1.4426950408889634;
     const double mfix = std::sqrt(double(D)) * 1.0079;
-    dim3 grid(n_qt, H, B);
+    const long long nblk = static_cast<long long>(n_qt) * B * H;
+    if (nblk > 0x7fffffffLL) return NC_EINVAL;
     ProfScope ps("attn_fwd", s);
-    nc::fwd::attn_fwd_kernel<D><<<grid, nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
-        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, n_qt, float(scale * log2e),
+    nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
+        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, B, n_qt, tile_group(n_qt, B * H),
+        float(scale * log2e),
         float(mfix * log2e), float(mfix));
     return launch_status();
 }
@@ -247,21 +267,24 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     if (make_tmap(&tq, qhat, B, T, H, D, nc::bwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::bwd::BN, kF16) ||
         make_tmap(&tv, v, B, T, H, D, nc::bwd::BN) || make_tmap(&tdo, dout, B, T, H, D, nc::bwd::BM))
         return NC_EINVAL;
-    const int n_kt = (T + nc::bwd::BN - 1) / nc::bwd::BN;
+    const long long n_kt = (T + nc::bwd::BN - 1) / nc::bwd::BN;
     const double scale = 1.0 / std::sqrt(double(D));
-    dim3 grid(n_kt, H, B);
+    // one CTA per (key tile, b, h), key tile slowest so the longest walks start first
+    const long long nblk = n_kt * B * H;
+    if (nblk > 0x7fffffffLL) return NC_EINVAL;
     {
         ProfScope ps("attn_bwd", s);
-        nc::bwd::attn_bwd_kernel<D><<<grid, nc::bwd::NUM_THREADS, nc::bwd::Smem<D>::ALLOC, s>>>(
+        nc::bwd::attn_bwd_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS, nc::bwd::Smem<D>::ALLOC, s>>>(
             tq, tk, tv, tdo, lse2, delta, dq_acc, gmax, reinterpret_cast<const __nv_bfloat16*>(k), tab,
-            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, Tpad, float(scale),
-            float(scale * 1.4426950408889634), eps);
+            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad,
+            tile_group(static_cast<int>(n_kt), B * H), float(scale), float(scale * 1.4426950408889634), eps);
     }
     if ((rc = launch_status())) return rc;
     {
         ProfScope ps("attn_dq_finalize", s);
-        nc::dq_finalize_kernel<D><<<rows_grid(rows, D), 256, 0, s>>>(
-            dq_acc, reinterpret_cast<const __nv_bfloat16*>(q), tab, reinterpret_cast<__nv_bfloat16*>(dq), rows, T,
+        const long long toks = static_cast<long long>(B) * T;
+        nc::dq_finalize_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
+            dq_acc, reinterpret_cast<const __nv_bfloat16*>(q), tab, reinterpret_cast<__nv_bfloat16*>(dq), toks, T,
             H, eps);
     }
     return launch_status();

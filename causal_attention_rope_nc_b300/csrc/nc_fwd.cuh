@@ -69,16 +69,18 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse, int T, int H, int n_qt, float scale_log2, float mfix_log2,
-                    float mfix) {
+                    float* __restrict__ lse, int T, int H, int B, int n_qt, int group, float scale_log2,
+                    float mfix_log2, float mfix) {
     using S = Smem<D>;
     constexpr int NC = D / 64;  // 64-column (128-byte) swizzle spans per row
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x);  // longest rows first
-    const int h = blockIdx.y, b = blockIdx.z;
+    // grouped (b, h) order, longest rows (the last query tile) first in a group
+    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_qt, group);
+    const int qt = n_qt - 1 - tc.rank;
+    const int b = tc.bh / H, h = tc.bh % H;
     const int n_kv = qt + 1;  // key tiles 0..qt (BM == BN)
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);

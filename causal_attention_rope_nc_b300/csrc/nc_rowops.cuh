@@ -18,36 +18,6 @@ struct RowLanes {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
 };
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = unpack_bf16x2(w[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-
-__device__ __forceinline__ uint4 f32x8_to_bf16(const float (&x)[8]) {
-    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                      pack_bf16x2(x[6], x[7]));
-}
-
-__device__ __forceinline__ uint4 f32x8_to_f16(const float (&x)[8]) {
-    return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                      pack_f16x2(x[6], x[7]));
-}
-
-__device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = unpack_f16x2(w[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-
 // Sum over the LPR lanes of a row group (groups are aligned, so the xor
 // partners never leave the group).
 template <int LPR>
@@ -79,63 +49,79 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // qhat = RoPE(q / sqrt(mean(q^2) + eps)), same for k (k may be null: one
 // tensor only), stored as IEEE fp16: the norm bounds every element by
 // sqrt(D) <= 11.4, well inside fp16's range, and fp16 keeps 3 more mantissa
-// bits than bf16 for the score products.  Rows are enumerated q rows first,
-// then k rows, each in memory order ((b*T + t)*H + h).  rstd (optional)
-// receives 1/r, laid out [2][B][T][H] (q then k).
+// bits than bf16 for the score products.  rstd (optional) receives 1/r,
+// laid out [2][B][T][H] (q then k).
+//
+// One group of D/8 lanes owns one token (b, t) of one tensor: it reads the
+// token's rotation row from the table once and walks the token's H heads,
+// HC heads at a time with every load of a chunk issued before any math, so
+// each lane keeps HC 16-byte loads in flight.  Tokens are enumerated q
+// tokens first, then k tokens.
+constexpr int NORM_HC = 8;
+
 template <int D>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
                                                            const __nv_bfloat16* __restrict__ k,
                                                            const float2* __restrict__ tab,
                                                            __half* __restrict__ qhat,
                                                            __half* __restrict__ khat,
-                                                           float* __restrict__ rstd, long long rows_per_tensor,
+                                                           float* __restrict__ rstd, long long tokens_per_tensor,
                                                            int T, int H, float eps) {
     using L = RowLanes<D>;
     const int sub = threadIdx.x % L::LPR;
     const long long groups = blockDim.x / L::LPR;
-    const long long nrows = (k ? 2 : 1) * rows_per_tensor;
-    // every lane of a warp runs the same number of iterations (shuffles)
+    const long long ntok = (k ? 2 : 1) * tokens_per_tensor;
     const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
     const long long stride = static_cast<long long>(gridDim.x) * groups;
+    // every lane of a warp runs the same number of iterations (shuffles)
     const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
-    for (long long base = warp_first, row = first; base < nrows; base += stride, row += stride) {
-        const bool valid = row < nrows;
-        const bool is_k = valid && row >= rows_per_tensor;
-        const long long r = valid ? (is_k ? row - rows_per_tensor : row) : 0;
-        const int t = static_cast<int>((r / H) % T);
-        float x[8];
-        if (valid) {
-            const __nv_bfloat16* src = (is_k ? k : q) + r * D + sub * 8;
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(src), x);
-        } else {
+    const int i0 = (sub % L::HALF) * 8;
+    const bool lo = sub < L::HALF;
+    for (long long base = warp_first, tok = first; base < ntok; base += stride, tok += stride) {
+        const bool valid = tok < ntok;
+        const bool is_k = valid && tok >= tokens_per_tensor;
+        const long long r = valid ? (is_k ? tok - tokens_per_tensor : tok) : 0;  // b*T + t
+        const int t = static_cast<int>(r % T);
+        float c[8], sn[8];
+        {
+            const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float4 v = valid ? cs4[e2] : make_float4(1.f, 0.f, 1.f, 0.f);
+                c[2 * e2] = v.x, sn[2 * e2] = v.y, c[2 * e2 + 1] = v.z, sn[2 * e2 + 1] = v.w;
+            }
         }
-        float ss = 0.f;
+        const __nv_bfloat16* src = (is_k ? k : q) + r * H * D + sub * 8;
+        __half* dst = (is_k ? khat : qhat) + r * H * D + sub * 8;
+        for (int h0 = 0; h0 < H; h0 += NORM_HC) {
+            uint4 u[NORM_HC];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-        ss = group_sum<L::LPR>(ss);
-        const float rs = rsqrtf(ss / D + eps);
-        float y[8], o[8];
+            for (int j = 0; j < NORM_HC; ++j)
+                u[j] = (valid && h0 + j < H) ? *reinterpret_cast<const uint4*>(src + (h0 + j) * D)
+                                             : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= rs;
+            for (int j = 0; j < NORM_HC; ++j) {
+                if (h0 + j >= H) break;  // uniform: H is the same for every lane
+                float x[8];
+                bf16x8_to_f32(u[j], x);
+                float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], L::HALF);
-        const int i0 = (sub % L::HALF) * 8;
-        const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
-        const bool lo = sub < L::HALF;
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                ss = group_sum<L::LPR>(ss);
+                const float rs = rsqrtf(ss / D + eps);
+                float y[8], o[8];
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-            const float4 cs = valid ? cs4[e2] : make_float4(1.f, 0.f, 1.f, 0.f);
-            const float c0 = cs.x, s0 = cs.y, c1 = cs.z, s1 = cs.w;
-            const int e = 2 * e2;
-            // low half holds a = x_i (partner b = x_{i+D/2}); high half the reverse
-            o[e] = lo ? x[e] * c0 - y[e] * s0 : y[e] * s0 + x[e] * c0;
-            o[e + 1] = lo ? x[e + 1] * c1 - y[e + 1] * s1 : y[e + 1] * s1 + x[e + 1] * c1;
-        }
-        if (valid) {
-            *reinterpret_cast<uint4*>((is_k ? khat : qhat) + r * D + sub * 8) = f32x8_to_f16(o);
-            if (rstd && sub == 0) rstd[(is_k ? rows_per_tensor : 0) + r] = rs;
+                for (int e = 0; e < 8; ++e) x[e] *= rs;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], L::HALF);
+                // low half holds a = x_i (partner b = x_{i+D/2}); high half the reverse
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
+                if (valid) {
+                    *reinterpret_cast<uint4*>(dst + (h0 + j) * D) = f32x8_to_f16(o);
+                    if (rstd && sub == 0) rstd[((is_k ? tokens_per_tensor : 0) + r) * H + h0 + j] = rs;
+                }
+            }
         }
     }
 }
@@ -225,58 +211,76 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 // -------------------------------------------- dQ: RoPE^T + RMSNorm bwd -----
 // dq = (u - y <u, y> / D) / r with u = R(pos)^T g, g = dq_acc row (already
 // scaled by 1/sqrt(D)), y = q / r the normalised query before rotation.
+// Same token-group walk as the prologue: one rotation row per token, the
+// token's heads HC at a time with their loads issued first.
 template <int D>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ dq_acc,
                                                           const __nv_bfloat16* __restrict__ q,
                                                           const float2* __restrict__ tab,
-                                                          __nv_bfloat16* __restrict__ dq, long long nrows, int T,
+                                                          __nv_bfloat16* __restrict__ dq, long long ntok, int T,
                                                           int H, float eps) {
     using L = RowLanes<D>;
+    constexpr int HC = 4;
     const int sub = threadIdx.x % L::LPR;
     const long long groups = blockDim.x / L::LPR;
     const long long stride = static_cast<long long>(gridDim.x) * groups;
     const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
     const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
-    for (long long base = warp_first, r = first; base < nrows; base += stride, r += stride) {
-        const bool valid = r < nrows;
-        const long long rr = valid ? r : 0;
-        const int t = static_cast<int>((rr / H) % T);
-        float x[8], g[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(q + rr * D + sub * 8), x);
-        const float4* gp = reinterpret_cast<const float4*>(dq_acc + rr * D + sub * 8);
-        const float4 g0 = gp[0], g1 = gp[1];
-        g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-        g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-        float ss = 0.f;
+    const int i0 = (sub % L::HALF) * 8;
+    const bool lo = sub < L::HALF;
+    for (long long base = warp_first, tok = first; base < ntok; base += stride, tok += stride) {
+        const bool valid = tok < ntok;
+        const long long r = valid ? tok : 0;  // b*T + t
+        const int t = static_cast<int>(r % T);
+        float c[8], sn[8];
+        {
+            const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-        ss = group_sum<L::LPR>(ss);
-        const float rs = rsqrtf(ss / D + eps);
-        float pg[8], u[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pg[e] = __shfl_xor_sync(0xffffffffu, g[e], L::HALF);
-        const int i0 = (sub % L::HALF) * 8;
-        const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
-        const bool lo = sub < L::HALF;
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-            const float4 cs = cs4[e2];
-            const float c[2] = {cs.x, cs.z}, s[2] = {cs.y, cs.w};
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int e = 2 * e2 + k2;
-                // R^T: (a, b) -> (a c + b s, -a s + b c)
-                u[e] = lo ? g[e] * c[k2] + pg[e] * s[k2] : -pg[e] * s[k2] + g[e] * c[k2];
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float4 v = cs4[e2];
+                c[2 * e2] = v.x, sn[2 * e2] = v.y, c[2 * e2 + 1] = v.z, sn[2 * e2 + 1] = v.w;
             }
         }
-        float dot = 0.f;
+        const long long row0 = r * H * D + sub * 8;
+        for (int h0 = 0; h0 < H; h0 += HC) {
+            uint4 uq[HC];
+            float4 g0[HC], g1[HC];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dot = fmaf(u[e], x[e] * rs, dot);
-        dot = group_sum<L::LPR>(dot);
-        float o[8];
+            for (int j = 0; j < HC; ++j) {
+                const bool in = valid && h0 + j < H;
+                const long long o = row0 + static_cast<long long>(h0 + j) * D;
+                uq[j] = in ? *reinterpret_cast<const uint4*>(q + o) : make_uint4(0, 0, 0, 0);
+                g0[j] = in ? __ldcs(reinterpret_cast<const float4*>(dq_acc + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                g1[j] = in ? __ldcs(reinterpret_cast<const float4*>(dq_acc + o) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (u[e] - x[e] * rs * (dot / D)) * rs;
-        if (valid) *reinterpret_cast<uint4*>(dq + r * D + sub * 8) = f32x8_to_bf16(o);
+            for (int j = 0; j < HC; ++j) {
+                if (h0 + j >= H) break;  // uniform
+                float x[8];
+                bf16x8_to_f32(uq[j], x);
+                const float g[8] = {g0[j].x, g0[j].y, g0[j].z, g0[j].w, g1[j].x, g1[j].y, g1[j].z, g1[j].w};
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                ss = group_sum<L::LPR>(ss);
+                const float rs = rsqrtf(ss / D + eps);
+                float pg[8], u[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pg[e] = __shfl_xor_sync(0xffffffffu, g[e], L::HALF);
+                // R^T: (a, b) -> (a c + b s, -a s + b c)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u[e] = lo ? g[e] * c[e] + pg[e] * sn[e] : -pg[e] * sn[e] + g[e] * c[e];
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dot = fmaf(u[e], x[e] * rs, dot);
+                dot = group_sum<L::LPR>(dot);
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (u[e] - x[e] * rs * (dot / D)) * rs;
+                if (valid)
+                    *reinterpret_cast<uint4*>(dq + row0 + static_cast<long long>(h0 + j) * D) = f32x8_to_bf16(o);
+            }
+        }
     }
 }
 
