@@ -3,9 +3,10 @@
 One step = one pass of the whole hot path over the d20 workload
 (B=32, T=2048, H=10, D=128): nc_attn_fwd (RoPE table, QK RMSNorm+RoPE
 prologue, tcgen05 forward) then nc_attn_bwd (backward preprocess, tcgen05
-backward with the fused dk epilogue, dq finalize).  Inputs are seeded
-synthetic bf16 Gaussians already resident in HBM; q, k, v and dout together
-are 671 MB, more than the 126 MB L2, so no flush is needed between steps.
+key-side kernel with the fused dk epilogue, tcgen05 query-side kernel with
+the fused dq epilogue).  Inputs are seeded synthetic bf16 Gaussians already
+resident in HBM; q, k, v and dout together are 671 MB, more than the 126 MB
+L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  `value` is fwd+bwd TFLOP/s under the
 algorithmic FLOP count (causal half of 2 matmuls forward, 5 backward).
@@ -55,7 +56,10 @@ def dist_env():
 # --------------------------------------------------------------- clocks ----
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms by a reader
+    thread that stamps each line on arrival; summary() keeps the samples that
+    arrived inside the window set by mark_start() / mark_end() (the timed
+    region)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -63,32 +67,50 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.samples = []  # (host time, line)
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.samples.append((time.time(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        # a sample describes the 200 ms before it arrived
+        lo = (self.t0 or 0.0) + 0.2
+        hi = (self.t1 or float("inf")) + 0.2
+        window = [l for t, l in self.samples if lo <= t <= hi]
+        for l in window:
             parts = [p.strip() for p in l.split(",")]
             if len(parts) < 9:
                 continue
@@ -143,14 +165,18 @@ def bench_ours(args, ws_n, rank, local):
     nc.nc_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        time.sleep(0.5)  # let nvidia-smi start sampling
         barrier()
         torch.cuda.synchronize(dev)
+        clk.mark_start()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
         barrier()
+        time.sleep(0.3)  # the sample covering the end of the region
     nc.nc_profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
     kern = nc.nc_profile_read()
@@ -180,7 +206,12 @@ def bench_ours(args, ws_n, rank, local):
     # dominant kernel by total time
     name, (n_l, tot) = max(kern.items(), key=lambda kv: kv[1][1])
     per_launch_ms = tot / max(n_l, 1)
-    alg = {"attn_bwd": 2.5 * w.fwd_flops(), "attn_fwd": w.fwd_flops()}
+    # algorithmic tensor FLOPs per launch (the causal half of each matmul):
+    # forward 2 matmuls; the backward's 5 are split between the key-side kernel
+    # (S^T, dP^T, dV, dK) and the query-side kernel (dQ; its S and dP are
+    # recomputation, not counted)
+    alg = {"attn_fwd": w.fwd_flops(), "attn_bwd_dkdv": 2.0 * w.fwd_flops(),
+           "attn_bwd_dq": 0.5 * w.fwd_flops()}
     timed_s = ms_total * 1e-3
     peak_t = pk["bf16_tflops_sustained"] if timed_s > 2.0 else pk["bf16_tflops"]
     roof = None
@@ -192,7 +223,7 @@ def bench_ours(args, ws_n, rank, local):
     kernels = {k_: {"launches": n_, "avg_us": round(1e3 * t_ / max(n_, 1), 2),
                     "share": round(t_ / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
                for k_, (n_, t_) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
-    for k_ in ("attn_fwd", "attn_bwd"):
+    for k_ in alg:
         if k_ in kern:
             n_, t_ = kern[k_]
             kernels[k_]["tflops"] = round(alg[k_] / (t_ / n_ * 1e-3) / 1e12, 1)
@@ -377,7 +408,7 @@ def bench_reference(args, ws_n, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -9,6 +9,7 @@
 
 #include "ncattn.h"
 #include "nc_bwd.cuh"
+#include "nc_bwd_dq.cuh"
 #include "nc_common.cuh"
 #include "nc_decode.cuh"
 #include "nc_fwd.cuh"
@@ -68,8 +69,10 @@ int device_ready() {
     };
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64>), nc::fwd::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128>), nc::fwd::Smem<128>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_kernel<64>), nc::bwd::Smem<64>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_kernel<128>), nc::bwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<64>), nc::bwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<128>), nc::bwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<64>), nc::bwdq::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<128>), nc::bwdq::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<64>), nc::dec::MAX_SMEM);
     optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<128>), nc::dec::MAX_SMEM);
     if (r != cudaSuccess) {
@@ -162,7 +165,7 @@ bool shape_ok(int B, int T, int H, int D) {
 bool params_ok(float eps, float base) { return std::isfinite(eps) && eps >= 0.f && std::isfinite(base) && base > 0.f; }
 
 size_t tab_bytes(int T, int D) { return up256(static_cast<size_t>(T) * (D / 2) * sizeof(float2)); }
-int tpad_of(int T) { return ((T + nc::bwd::BM - 1) / nc::bwd::BM) * nc::bwd::BM; }
+int tpad_of(int T) { return ((T + 127) / 128) * 128; }  // query blocks of 128
 
 int rows_grid(long long rows, int D) {
     const long long groups = 256 / (D / 8);
@@ -227,11 +230,13 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     const double scale = 1.0 / std::sqrt(double(D));
     const double log2e = 1.4426950408889634;
     const double mfix = std::sqrt(double(D)) * 1.0079;
-    const long long nblk = static_cast<long long>(n_qt) * B * H;
+    // one CTA per pair of query tiles
+    const int n_pairs = (n_qt + 1) / 2;
+    const long long nblk = static_cast<long long>(n_pairs) * B * H;
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
     ProfScope ps("attn_fwd", s);
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
-        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, B, n_qt, tile_group(n_qt, B * H),
+        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
         float(mfix * log2e), float(mfix));
     return launch_status();
@@ -249,43 +254,46 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
     float* lse2 = reinterpret_cast<float*>(w);
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
-    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||out_t||
-    w += 256;
-    float* dq_acc = reinterpret_cast<float*>(w);
+    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||out_t||, max ||v_t||
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    if (cudaMemsetAsync(gmax, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    if (cudaMemsetAsync(gmax, 0, 3 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
     const long long rows = static_cast<long long>(B) * T * H;
     {
         ProfScope ps("attn_bwd_pre", s);
         nc::bwd_pre_kernel<D><<<rows_grid(rows, D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout), lse, delta,
-            lse2, dq_acc, gmax, B, T, H, Tpad);
+            lse2, gmax, B, T, H, Tpad);
     }
     if ((rc = launch_status())) return rc;
     CUtensorMap tq, tk, tv, tdo;
-    if (make_tmap(&tq, qhat, B, T, H, D, nc::bwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::bwd::BN, kF16) ||
-        make_tmap(&tv, v, B, T, H, D, nc::bwd::BN) || make_tmap(&tdo, dout, B, T, H, D, nc::bwd::BM))
+    if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, H, D, 128, kF16) ||
+        make_tmap(&tv, v, B, T, H, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128))
         return NC_EINVAL;
-    const long long n_kt = (T + nc::bwd::BN - 1) / nc::bwd::BN;
-    const double scale = 1.0 / std::sqrt(double(D));
-    // one CTA per (key tile, b, h), key tile slowest so the longest walks start first
-    const long long nblk = n_kt * B * H;
+    const long long n_t = (T + 127) / 128;
+    const long long nblk = n_t * B * H;
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
+    const double scale = 1.0 / std::sqrt(double(D));
+    const int group = tile_group(static_cast<int>(n_t), B * H);
     {
-        ProfScope ps("attn_bwd", s);
-        nc::bwd::attn_bwd_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS, nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, lse2, delta, dq_acc, gmax, reinterpret_cast<const __nv_bfloat16*>(k), tab,
-            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad,
-            tile_group(static_cast<int>(n_kt), B * H), float(scale), float(scale * 1.4426950408889634), eps);
+        // key side: dk, dv (one CTA per key tile, longest walks first)
+        ProfScope ps("attn_bwd_dkdv", s);
+        nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS,
+                                           nc::bwd::Smem<D>::ALLOC, s>>>(
+            tq, tk, tv, tdo, lse2, delta, gmax, reinterpret_cast<const __nv_bfloat16*>(k), tab,
+            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad, group,
+            float(scale), float(scale * 1.4426950408889634), eps);
     }
     if ((rc = launch_status())) return rc;
     {
-        ProfScope ps("attn_dq_finalize", s);
-        const long long toks = static_cast<long long>(B) * T;
-        nc::dq_finalize_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
-            dq_acc, reinterpret_cast<const __nv_bfloat16*>(q), tab, reinterpret_cast<__nv_bfloat16*>(dq), toks, T,
-            H, eps);
+        // query side: dq (one CTA per query tile), after the key side has
+        // published max ||v_t|| for the dS bound
+        ProfScope ps("attn_bwd_dq", s);
+        nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
+                                          nc::bwdq::Smem<D>::ALLOC, s>>>(
+            tq, tk, tv, tdo, lse2, delta, gmax, reinterpret_cast<const __nv_bfloat16*>(q), tab,
+            reinterpret_cast<__nv_bfloat16*>(dq), T, H, B, Tpad, group, float(scale),
+            float(scale * 1.4426950408889634), eps);
     }
     return launch_status();
 }
@@ -418,8 +426,7 @@ size_t nc_attn_workspace_size(int op, int B, int T, int H, int D) {
         case NC_OP_FWD: return tab_bytes(T, D);
         case NC_OP_BWD: {
             const int Tpad = tpad_of(T);
-            return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256 +
-                   up256(static_cast<size_t>(B) * T * H * D * 4);
+            return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256;
         }
         case NC_OP_DECODE: return decode_ws_layout(B, H, D, T, nullptr, nullptr);
         default: return 0;

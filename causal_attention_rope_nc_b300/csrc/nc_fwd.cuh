@@ -1,12 +1,23 @@
 // Causal attention forward on sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
-// One CTA computes one 128-row query tile of one (batch, head):
-//   warp 4      TMA producer: Q once, then K_j / V_j tiles into 2-stage rings
-//   warp 5      MMA issuer (one thread): S_j = Q K_j^T into a TMEM ping-pong,
-//               O += P_j V_j into a TMEM accumulator
-//   warps 0-3   softmax: thread r owns query row r (TMEM lane r); reads S_j
-//               from TMEM, writes P_j = exp(S_j - m) in bf16 to shared
-//               memory; at the end scales O by 1/l and writes out and lse.
+// One CTA computes two consecutive 128-row query tiles (2p and 2p+1) of one
+// (batch, head); both share every K/V tile it streams:
+//   warp 8      TMA producer: both Q tiles once, then K_j / V_j in 2-stage rings
+//   warp 9      MMA issuer (one thread)
+//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: thread r owns
+//               query row r (TMEM lane r) of its tile
+// Tensor memory: S_t (128 fp32 columns) per tile, overwritten in place by the
+// bf16 probabilities P_t that the PV product reads as its A operand, and an
+// output accumulator O_t (D columns) per tile: 2 x 128 + 2 x D <= 512.
+//
+// Issue order (the tensor pipe executes one thread's MMAs in issue order):
+//   S_0(0) S_1(0) | PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) | ...
+// so each softmax warpgroup has the other tile's two products (about 1000
+// cycles) to turn S_t(j) into P_t(j), and the two groups alternate.
+//
+// Exponentials: a quarter of them are computed on the FMA pipe
+// (exp2_poly), the rest by ex2.approx, so that neither unit limits the
+// tensor pipe.
 //
 // Operand types: qhat and khat arrive in fp16 (their elements are bounded by
 // sqrt(D), so fp16's range suffices and its finer mantissa keeps the scores
@@ -23,13 +34,16 @@
 #pragma once
 
 #include "nc_common.cuh"
+#include "nc_exp2.cuh"
 
 namespace nc {
 namespace fwd {
 
-constexpr int BM = 128;  // query rows per CTA (one TMEM lane each)
+constexpr int BM = 128;  // query rows per tile (one TMEM lane each)
 constexpr int BN = 128;  // keys per tile
-constexpr int NUM_THREADS = 192;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int NUM_THREADS = 10 * 32;
 
 enum Bar {
     Q_FULL = 0,
@@ -37,33 +51,32 @@ enum Bar {
     K_EMPTY = 3,   // +stage
     V_FULL = 5,    // +stage
     V_EMPTY = 7,   // +stage
-    S_FULL = 9,    // +buffer
-    S_FREE = 11,   // +buffer
-    P_FULL = 13,   // +buffer
-    P_FREE = 15,   // +buffer
-    O_FULL = 17,
-    MMA_DONE = 18,
-    NUM_BARS = 19
+    S_FULL = 9,    // +tile
+    P_FULL = 11,   // +tile
+    O_FULL = 13,   // +tile
+    MMA_DONE = 15,
+    NUM_BARS = 16
 };
 
 template <int D>
 struct Smem {
     static constexpr int QBYTES = BM * D * 2;
     static constexpr int KBYTES = BN * D * 2;
-    static constexpr int PBYTES = BM * BN * 2;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + QBYTES;
-    static constexpr int OFF_V = OFF_K + 2 * KBYTES;
-    static constexpr int OFF_P = OFF_V + 2 * KBYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
+    static constexpr int OFF_Q = 0;                       // 2 tiles
+    static constexpr int OFF_K = OFF_Q + 2 * QBYTES;      // 2 stages
+    static constexpr int OFF_V = OFF_K + 2 * KBYTES;      // 2 stages
+    static constexpr int OFF_BAR = OFF_V + 2 * KBYTES;
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_TSLOT + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;    // two 128-column score buffers
-constexpr uint32_t TM_O = 256;  // D-column output accumulator
+__host__ __device__ constexpr uint32_t tm_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+template <int D>
+__host__ __device__ constexpr uint32_t tm_o(int t) {
+    return 256u + static_cast<uint32_t>(t) * D;
+}
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -74,14 +87,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using S = Smem<D>;
     constexpr int NC = D / 64;  // 64-column (128-byte) swizzle spans per row
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_align1024(smem_raw, S::BYTES, S::ALLOC);
+    if (smem == nullptr) {  // uniform over the CTA: nothing has started yet
+        if (threadIdx.x == 0) flag_error(3, 0x0f0);
+        return;
+    }
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grouped (b, h) order, longest rows (the last query tile) first in a group
-    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_qt, group);
-    const int qt = n_qt - 1 - tc.rank;
+    // grouped (b, h) order, longest rows (the last pair of query tiles) first in a group
+    const int n_pairs = (n_qt + 1) / 2;
+    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_pairs, group);
+    const int qt0 = 2 * (n_pairs - 1 - tc.rank);
     const int b = tc.bh / H, h = tc.bh % H;
-    const int n_kv = qt + 1;  // key tiles 0..qt (BM == BN)
+    const bool has1 = qt0 + 1 < n_qt;
+    const int n0 = qt0 + 1;             // key tiles of query tile qt0
+    const int n1 = has1 ? qt0 + 2 : 0;  // key tiles of query tile qt0 + 1
+    const int n_kv = has1 ? n1 : n0;
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
 
@@ -93,11 +114,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(V_FULL + s), 1);
             mbar_init(bar(V_EMPTY + s), 1);
             mbar_init(bar(S_FULL + s), 1);
-            mbar_init(bar(S_FREE + s), 128);
             mbar_init(bar(P_FULL + s), 128);
-            mbar_init(bar(P_FREE + s), 1);
+            mbar_init(bar(O_FULL + s), 1);
         }
-        mbar_init(bar(O_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
         fence_mbar_init();
     }
@@ -110,13 +129,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
+    if (warp == WARP_TMA) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
             int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
-            mbar_expect_tx(bar(Q_FULL), S::QBYTES);
-            for (int c = 0; c < NC; ++c)
-                tma_load_4d(sb + S::OFF_Q + c * (BM * 128), &tm_q, c * 64, h, qt * BM, b, bar(Q_FULL));
+            mbar_expect_tx(bar(Q_FULL), (has1 ? 2 : 1) * S::QBYTES);
+            for (int t = 0; t < (has1 ? 2 : 1); ++t)
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_Q + t * S::QBYTES + c * (BM * 128), &tm_q, c * 64, h, (qt0 + t) * BM, b,
+                                bar(Q_FULL));
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j & 1, use = j >> 1;
                 if (j >= 2 && !mbar_wait(bar(K_EMPTY + st), (use - 1) & 1, 0x101)) break;
@@ -140,100 +161,124 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == WARP_MMA) {
         // ------------------------------------------------- MMA issuer -----
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);   // qhat (K-major) x khat (K-major), fp16
-            constexpr uint32_t IDESC_O = idesc_bf16(BM, D, 0, 1);   // P (K-major) x V (MN-major)
-            bool ok = mbar_wait(bar(Q_FULL), 0, 0x201);
-            for (int j = 0; ok && j <= n_kv; ++j) {
-                if (j < n_kv) {
-                    const int st = j & 1, use = j >> 1;
-                    if (!mbar_wait(bar(K_FULL + st), use & 1, 0x202)) { ok = false; break; }
-                    if (j >= 2 && !mbar_wait(bar(S_FREE + st), (use - 1) & 1, 0x203)) { ok = false; break; }
-                    tc_fence_after();
+            constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);  // qhat (K-major) x khat (K-major), fp16
+            constexpr uint32_t IDESC_O = idesc_bf16(BM, D, 0, 1);  // P (TMEM) x V (MN-major)
+            auto issue_s = [&](int t, int st) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                        const uint64_t a = sdesc_sw128(sb + S::OFF_Q + koff, 16, 1024);
-                        const uint64_t bd =
-                            sdesc_sw128(sb + S::OFF_K + st * S::KBYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16,
-                                        1024);
-                        mma_bf16(tmem + TM_S + st * BN, a, bd, IDESC_S, kk > 0);
-                    }
-                    mma_commit(bar(S_FULL + st));
-                    mma_commit(bar(K_EMPTY + st));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qa = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+                    const uint32_t ka = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                    mma_bf16(tmem + tm_s(t), sdesc_sw128(sb + S::OFF_Q + t * S::QBYTES + qa, 16, 1024),
+                             sdesc_sw128(sb + S::OFF_K + st * S::KBYTES + ka, 16, 1024), IDESC_S, kk > 0);
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, st = jj & 1, use = jj >> 1;
-                    if (!mbar_wait(bar(P_FULL + st), use & 1, 0x204)) { ok = false; break; }
-                    if (!mbar_wait(bar(V_FULL + st), use & 1, 0x205)) { ok = false; break; }
-                    tc_fence_after();
+                mma_commit(bar(S_FULL + t));
+            };
+            auto issue_pv = [&](int t, int st, bool first) {
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(
-                            sb + S::OFF_P + st * S::PBYTES + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            sdesc_sw128(sb + S::OFF_V + st * S::KBYTES + kk * (16 * 128), BN * 128, 1024);
-                        mma_bf16(tmem + TM_O, a, bd, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar(P_FREE + st));
-                    mma_commit(bar(V_EMPTY + st));
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + tm_o<D>(t), tmem + tm_s(t) + kk * 8,
+                           sdesc_sw128(sb + S::OFF_V + st * S::KBYTES + kk * (16 * 128), BN * 128, 1024), IDESC_O,
+                           (!first || kk > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bar(Q_FULL), 0, 0x201) && mbar_wait(bar(K_FULL + 0), 0, 0x202);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                if (has1) issue_s(1, 0);
+                mma_commit(bar(K_EMPTY + 0));
             }
-            if (ok) mma_commit(bar(O_FULL));
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int st = j & 1;
+                const bool nxt = j + 1 < n_kv;
+                if (!mbar_wait(bar(V_FULL + st), (j >> 1) & 1, 0x203)) { ok = false; break; }
+                bool k_ready = false;  // K_{j+1} waited for
+                if (j < n0) {
+                    if (!mbar_wait(bar(P_FULL + 0), j & 1, 0x204)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(0, st, j == 0);
+                    if (j == n0 - 1) mma_commit(bar(O_FULL + 0));
+                    if (j + 1 < n0) {
+                        if (!mbar_wait(bar(K_FULL + (st ^ 1)), ((j + 1) >> 1) & 1, 0x205)) { ok = false; break; }
+                        k_ready = true;
+                        tc_fence_after();
+                        issue_s(0, st ^ 1);
+                    }
+                }
+                if (has1) {
+                    if (!mbar_wait(bar(P_FULL + 1), j & 1, 0x206)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(1, st, j == 0);
+                    if (j == n1 - 1) mma_commit(bar(O_FULL + 1));
+                }
+                mma_commit(bar(V_EMPTY + st));
+                if (has1 && nxt) {
+                    if (!k_ready && !mbar_wait(bar(K_FULL + (st ^ 1)), ((j + 1) >> 1) & 1, 0x207)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(1, st ^ 1);
+                }
+                if (nxt) mma_commit(bar(K_EMPTY + (st ^ 1)));
+            }
             // all MMAs issued by this thread complete before teardown
             mma_commit(bar(MMA_DONE));
-            mbar_wait(bar(MMA_DONE), 0, 0x206);
+            mbar_wait(bar(MMA_DONE), 0, 0x208);
         }
         __syncwarp();
     } else {
         // ----------------------------------------- softmax + epilogue -----
-        const int row = warp * 32 + lane;
+        const int t = warp >> 2;        // query tile of this warpgroup
+        const int quarter = warp & 3;   // TMEM lane quarter
+        const int row = quarter * 32 + lane;
+        const int qt = qt0 + t;
         const int q_idx = qt * BM + row;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int n_t = t ? n1 : n0;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t ts = tmem + lane_base + tm_s(t);
         float l_sum = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int st = j & 1, use = j >> 1;
-            if (!mbar_wait(bar(S_FULL + st), use & 1, 0x301)) { ok = false; break; }
+        for (int j = 0; j < n_t; ++j) {
+            if (!mbar_wait(bar(S_FULL + t), j & 1, 0x301)) { ok = false; break; }
             tc_fence_after();
-            if (j >= 2 && !mbar_wait(bar(P_FREE + st), (use - 1) & 1, 0x302)) { ok = false; break; }
             const bool diag = (j == qt);
-            const uint32_t pb = sb + S::OFF_P + st * S::PBYTES;
+            uint32_t r[2][32];
+            tmem_ld32(ts, r[0]);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + TM_S + st * BN + c * 32, r);
-                tmem_wait_ld();
-                float p[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = fmaf(__uint_as_float(r[e]), scale_log2, -mfix_log2);
-                    p[e] = (diag && (c * 32 + e) > row) ? 0.f : ex2(x);
-                }
-                // The normaliser sums the bf16-ROUNDED probabilities that the
-                // PV product consumes, so each row's weights sum to exactly 1.
+                // the load of chunk c+1 overlaps the exponentials of chunk c
+                if (c + 1 < BN / 32) tmem_ld32(ts + (c + 1) * 32, r[(c + 1) & 1]);
+                const uint32_t* rc = r[c & 1];
                 uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-#pragma unroll
-                for (int i = 0; i < 16; i += 2)
-                    l_sum += (__uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xffff0000u)) +
-                             (__uint_as_float(w[i + 1] << 16) + __uint_as_float(w[i + 1] & 0xffff0000u));
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int chunk = c * 4 + g;  // 16-byte chunk 0..15 of the 256-byte P row
-                    const uint32_t addr = pb + (chunk >> 3) * (BM * 128) + sw128_offset(row, chunk & 7);
-                    st_shared_v4(addr, w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+                for (int e = 0; e < 32; e += 2) {
+                    const float x0 = fmaf(__uint_as_float(rc[e]), scale_log2, -mfix_log2);
+                    const float x1 = fmaf(__uint_as_float(rc[e + 1]), scale_log2, -mfix_log2);
+                    float p0 = ex2(x0);
+                    float p1 = (e & 2) ? exp2_poly(x1) : ex2(x1);  // one in four on the FMA pipe
+                    if (diag) {
+                        if (c * 32 + e > row) p0 = 0.f;
+                        if (c * 32 + e + 1 > row) p1 = 0.f;
+                    }
+                    // the normaliser sums the bf16-ROUNDED probabilities that the
+                    // PV product consumes, so each row's weights sum to exactly 1
+                    const uint32_t wv = pack_bf16x2(p0, p1);
+                    l_sum += __uint_as_float(wv << 16) + __uint_as_float(wv & 0xffff0000u);
+                    w[e / 2] = wv;
                 }
+                // chunk c lands in packed columns [16c, 16c+16): already read
+                tmem_st16(ts + c * 16, w);
+                if (c + 1 < BN / 32) tmem_wait_ld();
             }
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(S_FREE + st));
-            fence_proxy_async_smem();
-            mbar_arrive(bar(P_FULL + st));
+            mbar_arrive(bar(P_FULL + t));
         }
-        if (ok && mbar_wait(bar(O_FULL), 0, 0x303)) {
+        if (n_t > 0 && ok && mbar_wait(bar(O_FULL + t), 0, 0x303)) {
             tc_fence_after();
             const float inv_l = 1.f / l_sum;
             const bool valid = q_idx < T;
@@ -241,18 +286,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __nv_bfloat16* orow = out + ((static_cast<long long>(b) * T + q_idx) * H + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + TM_O + c * 32, r);
+                uint32_t ro[32];
+                tmem_ld32(tmem + lane_base + tm_o<D>(t) + c * 32, ro);
                 tmem_wait_ld();
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
-                        const float* f = reinterpret_cast<const float*>(r) + 8 * g;
-                        dst[g] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
-                                            pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                                            pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
-                                            pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(ro[8 * g + i]) * inv_l;
+                        dst[g] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                            pack_bf16x2(f[6], f[7]));
                     }
                 }
             }

@@ -129,15 +129,15 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
 // -------------------------------------------------- backward preprocess ----
 // delta[b][h][t] = <dout_t, out_t> (fp32), lse2[b][h][t] = lse * log2(e),
 // both padded to Tpad columns (delta 0, lse2 +inf beyond T so that padded
-// query rows get probability 0); dq_acc rows are zeroed.  gmax[0] and
+// query rows get probability 0).  gmax[0] and
 // gmax[1] receive the largest row norms ||dout_t|| and ||out_t|| over the
 // whole tensor (they must be zero on entry); the backward bounds dS with them.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ delta,
-                                                      float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                      unsigned int* __restrict__ gmax, int B, int T, int H,
+                                                      float* __restrict__ lse2, unsigned int* __restrict__ gmax,
+                                                      int B, int T, int H,
                                                       int Tpad) {
     using L = RowLanes<D>;
     __shared__ float s_max[2][32];
@@ -161,9 +161,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                 sdo = fmaf(g[e], g[e], sdo);
                 so = fmaf(a[e], a[e], so);
             }
-            float4* z = reinterpret_cast<float4*>(dq_acc + r * D + sub * 8);
-            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         acc = group_sum<L::LPR>(acc);
         mx_do = fmaxf(mx_do, group_sum<L::LPR>(sdo));
@@ -205,82 +202,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
         const long long o = bh * Tpad + T + (e % padw);
         delta[o] = 0.f;
         lse2[o] = __int_as_float(0x7f800000);  // +inf
-    }
-}
-
-// -------------------------------------------- dQ: RoPE^T + RMSNorm bwd -----
-// dq = (u - y <u, y> / D) / r with u = R(pos)^T g, g = dq_acc row (already
-// scaled by 1/sqrt(D)), y = q / r the normalised query before rotation.
-// Same token-group walk as the prologue: one rotation row per token, the
-// token's heads HC at a time with their loads issued first.
-template <int D>
-__global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ dq_acc,
-                                                          const __nv_bfloat16* __restrict__ q,
-                                                          const float2* __restrict__ tab,
-                                                          __nv_bfloat16* __restrict__ dq, long long ntok, int T,
-                                                          int H, float eps) {
-    using L = RowLanes<D>;
-    constexpr int HC = 4;
-    const int sub = threadIdx.x % L::LPR;
-    const long long groups = blockDim.x / L::LPR;
-    const long long stride = static_cast<long long>(gridDim.x) * groups;
-    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
-    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
-    const int i0 = (sub % L::HALF) * 8;
-    const bool lo = sub < L::HALF;
-    for (long long base = warp_first, tok = first; base < ntok; base += stride, tok += stride) {
-        const bool valid = tok < ntok;
-        const long long r = valid ? tok : 0;  // b*T + t
-        const int t = static_cast<int>(r % T);
-        float c[8], sn[8];
-        {
-            const float4* cs4 = reinterpret_cast<const float4*>(tab + static_cast<long long>(t) * (D / 2) + i0);
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const float4 v = cs4[e2];
-                c[2 * e2] = v.x, sn[2 * e2] = v.y, c[2 * e2 + 1] = v.z, sn[2 * e2 + 1] = v.w;
-            }
-        }
-        const long long row0 = r * H * D + sub * 8;
-        for (int h0 = 0; h0 < H; h0 += HC) {
-            uint4 uq[HC];
-            float4 g0[HC], g1[HC];
-#pragma unroll
-            for (int j = 0; j < HC; ++j) {
-                const bool in = valid && h0 + j < H;
-                const long long o = row0 + static_cast<long long>(h0 + j) * D;
-                uq[j] = in ? *reinterpret_cast<const uint4*>(q + o) : make_uint4(0, 0, 0, 0);
-                g0[j] = in ? __ldcs(reinterpret_cast<const float4*>(dq_acc + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                g1[j] = in ? __ldcs(reinterpret_cast<const float4*>(dq_acc + o) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < HC; ++j) {
-                if (h0 + j >= H) break;  // uniform
-                float x[8];
-                bf16x8_to_f32(uq[j], x);
-                const float g[8] = {g0[j].x, g0[j].y, g0[j].z, g0[j].w, g1[j].x, g1[j].y, g1[j].z, g1[j].w};
-                float ss = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-                ss = group_sum<L::LPR>(ss);
-                const float rs = rsqrtf(ss / D + eps);
-                float pg[8], u[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) pg[e] = __shfl_xor_sync(0xffffffffu, g[e], L::HALF);
-                // R^T: (a, b) -> (a c + b s, -a s + b c)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) u[e] = lo ? g[e] * c[e] + pg[e] * sn[e] : -pg[e] * sn[e] + g[e] * c[e];
-                float dot = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dot = fmaf(u[e], x[e] * rs, dot);
-                dot = group_sum<L::LPR>(dot);
-                float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (u[e] - x[e] * rs * (dot / D)) * rs;
-                if (valid)
-                    *reinterpret_cast<uint4*>(dq + row0 + static_cast<long long>(h0 + j) * D) = f32x8_to_bf16(o);
-            }
-        }
     }
 }
 

@@ -129,7 +129,11 @@ int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int3
 /* Backward.  In: the forward's inputs q, k, v, pos, its outputs out, lse,
  * qhat, khat, and the upstream gradient dout [B][T][H][D].  Out: dq, dk, dv
  * [B][T][H][D] (gradients with respect to the RAW q, k, v: through the
- * softmax, the RoPE rotation and the RMSNorm).  Workspace: NC_OP_BWD. */
+ * softmax, the RoPE rotation and the RMSNorm).  Every output element is
+ * computed by one CTA (a key-side kernel writes dk and dv, a query-side
+ * kernel dq): no atomics, bit-identical results on repeated calls.
+ * Workspace: NC_OP_BWD (RoPE table, per-row delta and lse, three norm
+ * maxima; overwritten by every call). */
 int nc_attn_bwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
                 const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
                 nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,

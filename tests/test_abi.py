@@ -48,7 +48,7 @@ def test_workspace_sizes(lib):
     B, T, H, D = 32, 2048, 10, 128
     tab = T * (D // 2) * 8
     assert f(0, B, T, H, D) == tab
-    assert f(1, B, T, H, D) == tab + 2 * B * H * T * 4 + 256 + B * T * H * D * 4
+    assert f(1, B, T, H, D) == tab + 2 * B * H * T * 4 + 256
     assert f(2, B, T, H, D) > 0
     assert f(0, B, T, H, 96) == 0  # unsupported head dim
 
