@@ -173,7 +173,7 @@ def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, r
 
 def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
     """nc_attn_decode for callers that cannot supply a workspace (the library
-    keeps the scratch in a fixed 8 MiB device array; see include/ncattn.h)."""
+    keeps the scratch in a fixed 16 MiB device array; see include/ncattn.h)."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
         _bf16(t, n)
     _f16(kcache, "kcache")

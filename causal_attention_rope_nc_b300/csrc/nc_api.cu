@@ -157,6 +157,19 @@ int make_tmap(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D, int 
     return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
 }
 
+// The RoPE table [T][D/2] (cos, sin) viewed as an fp32 [T][D] tensor: boxes
+// of 32 values x 128 rows, 128-byte swizzled.  Rows past T read as zero.
+int make_tab_tmap(CUtensorMap* tm, const float2* tab, int T, int D) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode_fn()(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float2*>(tab), dims, strides, box,
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
 bool shape_ok(int B, int T, int H, int D) {
     return B >= 0 && T >= 0 && H >= 0 && (D == 64 || D == 128) && B <= 65535 && H <= 65535 &&
            T <= (1 << 24);
@@ -266,9 +279,10 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
             lse2, gmax, B, T, H, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, H, D, 128, kF16) ||
-        make_tmap(&tv, v, B, T, H, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128))
+        make_tmap(&tv, v, B, T, H, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
+        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, H, D, 128) || make_tab_tmap(&ttab, tab, T, D))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -280,8 +294,8 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         ProfScope ps("attn_bwd_dkdv", s);
         nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS,
                                            nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, lse2, delta, gmax, reinterpret_cast<const __nv_bfloat16*>(k), tab,
-            reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad, group,
+            tq, tk, tv, tdo, tkr, ttab, lse2, delta, gmax, reinterpret_cast<__nv_bfloat16*>(dk),
+            reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad, group,
             float(scale), float(scale * 1.4426950408889634), eps);
     }
     if ((rc = launch_status())) return rc;
@@ -291,8 +305,8 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         ProfScope ps("attn_bwd_dq", s);
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
                                           nc::bwdq::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, lse2, delta, gmax, reinterpret_cast<const __nv_bfloat16*>(q), tab,
-            reinterpret_cast<__nv_bfloat16*>(dq), T, H, B, Tpad, group, float(scale),
+            tq, tk, tv, tdo, tqr, ttab, lse2, delta, gmax, reinterpret_cast<__nv_bfloat16*>(dq), T, H, B, Tpad,
+            group, float(scale),
             float(scale * 1.4426950408889634), eps);
     }
     return launch_status();
@@ -305,9 +319,9 @@ struct DecodeWs {
 };
 
 size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base) {
-    const int nch = (Tcap + nc::dec::CHUNK - 1) / nc::dec::CHUNK;
-    const size_t o_bytes = up256(static_cast<size_t>(B) * nch * H * D * 4);
-    const size_t ml_bytes = up256(static_cast<size_t>(B) * nch * H * 2 * 4);
+    const int nit = (Tcap + nc::dec::ITEM - 1) / nc::dec::ITEM;  // partial results per stream, at most
+    const size_t o_bytes = up256(static_cast<size_t>(B) * nit * H * D * 4);
+    const size_t ml_bytes = up256(static_cast<size_t>(B) * nit * H * 2 * 4);
     const size_t c_bytes = up256(static_cast<size_t>(B) * 4);
     if (out) {
         uint8_t* w = reinterpret_cast<uint8_t*>(base);
@@ -318,23 +332,33 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
     return c_bytes + ml_bytes + o_bytes;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess)
+        return 148;
+    return n > 0 ? n : 148;
+}
+
 template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
                 cudaStream_t s) {
-    const int nch = (Tcap + nc::dec::CHUNK - 1) / nc::dec::CHUNK;
-    const int xt = nc::dec::Shape<D>::xthreads(H);
-    const int ks = nc::dec::Shape<D>::slices(H);
-    dim3 block(xt, ks);
-    dim3 grid(nch, B);
-    const size_t smem = static_cast<size_t>(H) * D * 4 + (D / 2) * 8 + static_cast<size_t>(ks) * xt * 10 * 4;
+    using Sh = nc::dec::Shape<D>;
+    const int nit = (Tcap + nc::dec::ITEM - 1) / nc::dec::ITEM;
+    const int xt = Sh::xthreads(H), ks = Sh::slices(H);
+    const int sps = Sh::sps(H) < ks * nc::dec::MAX_SPT ? Sh::sps(H) : ks * nc::dec::MAX_SPT;
+    const nc::dec::Layout ly = nc::dec::layout(H, D, sps, xt, ks);
+    if (ly.bytes > nc::dec::MAX_SMEM) return NC_EINVAL;
+    // persistent: one CTA per SM, each with an equal share of the items
+    const int grid = sm_count();
     const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
     ProfScope ps("attn_decode", s);
-    nc::dec::attn_decode_kernel<D><<<grid, block, smem, s>>>(
+    nc::dec::attn_decode_kernel<D><<<grid, xt * ks + 32, ly.bytes, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, H, Tcap, nch, eps, std::log2(double(base)), float(scale_log2));
+        ws.part_ml, ws.counters, B, H, Tcap, nit, sps, eps, std::log2(double(base)), float(scale_log2));
     return launch_status();
 }
 

@@ -28,7 +28,8 @@
 // Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 key rows,
 // query half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end warps 0-3
 // write dv and warps 4-7 dk (through the RoPE transpose and the RMSNorm
-// backward).
+// backward, from the raw k rows and RoPE table rows that the producer stages
+// in shared memory once the last product is done).
 //
 // Operand types: the score side (qhat, khat, dS) is IEEE fp16, the value
 // side (P, v, dout) bf16; tcgen05 wants A and B of one product in one type.
@@ -42,6 +43,7 @@
 #pragma once
 
 #include "nc_common.cuh"
+#include "nc_exp2.cuh"
 #include "nc_normrope_bwd.cuh"
 
 namespace nc {
@@ -64,7 +66,8 @@ enum Bar {
     DS_FULL = 8,  // softmax wrote dS^T over dP^T
     DKV_FULL = 9,
     MMA_DONE = 10,
-    NUM_BARS = 11
+    EPI_FULL = 11,  // raw k tile and RoPE table tile staged for the dk epilogue
+    NUM_BARS = 12
 };
 
 template <int D>
@@ -82,11 +85,12 @@ struct Smem {
     static constexpr int OFF_MISC = OFF_TSLOT + 16;  // 4 warp maxima of ||v_j||^2
     static constexpr int BYTES = OFF_MISC + 32;
     static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
-    // dk epilogue: u = RoPE^T(dKhat) rows staged over the (then idle) qhat and
-    // dout stages, 16 bytes of padding per row against bank conflicts
-    static constexpr int U_STRIDE = D * 4 + 16;
+    // dk epilogue, once every MMA is done: the raw k tile over the dout
+    // stages, the RoPE table tile (fp32 [128][D]) over the qhat stages
+    static constexpr int XBYTES = BN * D * 2;
+    static constexpr int CBYTES = BN * D * 4;
     static_assert(BYTES <= SMEM_LIMIT, "backward tiles exceed shared memory");
-    static_assert(BN * U_STRIDE <= 4 * QBYTES, "dk staging exceeds the qhat/dout stages");
+    static_assert(XBYTES <= 2 * QBYTES && CBYTES <= 2 * QBYTES, "epilogue tiles exceed the stages");
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -104,9 +108,9 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_kraw, const __grid_constant__ CUtensorMap tm_tab,
                          const float* __restrict__ lse2, const float* __restrict__ delta,
-                         unsigned int* __restrict__ gmax, const __nv_bfloat16* __restrict__ k_raw,
-                         const float2* __restrict__ tab, __nv_bfloat16* __restrict__ dk,
+                         unsigned int* __restrict__ gmax, __nv_bfloat16* __restrict__ dk,
                          __nv_bfloat16* __restrict__ dv, int T, int H, int B, int Tpad, int group, float scale,
                          float scale_log2, float eps) {
     using S = Smem<D>;
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(bar(DS_FULL), 256);
         mbar_init(bar(DKV_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
+        mbar_init(bar(EPI_FULL), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -183,6 +188,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_wait(bar(KV_FULL), 0, 0x112);
             for (int s = 0; s < 2; ++s)
                 if (issued[s]) mbar_wait(bar(QF + s), (issued[s] - 1) & 1, 0x113);
+            // once every MMA is done the stages are free: stage the dk
+            // epilogue's raw k rows and RoPE table rows
+            if (mbar_wait(bar(DKV_FULL), 0, 0x114)) {
+                mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_DO + c * (BN * 128), &tm_kraw, c * 64, h, kt * BN, b, bar(EPI_FULL));
+                for (int c = 0; c < D / 32; ++c)
+                    tma_load_2d(sb + S::OFF_Q + c * (BN * 128), &tm_tab, c * 32, kt * BN, bar(EPI_FULL));
+                mbar_wait(bar(EPI_FULL), 0, 0x115);
+            }
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -318,7 +333,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int i = 0; i < 4; ++i) {
                             const int qi = c * 32 + e4 * 4 + i;
                             const float x = fmaf(__uint_as_float(r[c][e4 * 4 + i]), scale_log2, -lv[i]);
-                            p[i] = (diag && q0 + qi < key) ? 0.f : ex2(x);
+                            // one in four on the FMA pipe, the rest on the SFU
+                            p[i] = (diag && q0 + qi < key) ? 0.f : (i == 3 ? exp2_poly(x) : ex2(x));
                         }
                         pk[c * 16 + e4 * 2] = pack_bf16x2(p[0], p[1]);
                         pk[c * 16 + e4 * 2 + 1] = pack_bf16x2(p[2], p[3]);
@@ -385,16 +401,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
                     }
                 }
-            } else {
-                // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha)); every MMA and
-                // tile load has completed, so the stages stage u
+            } else if (mbar_wait(bar(EPI_FULL), 0, 0x316)) {
+                // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha)) from the staged tiles
                 const bool valid = key < T;
-                const int kr = valid ? key : T - 1;  // clamp reads of invalid rows
-                norm_rope_bwd_row<D>(tmem + lane_base + TM_DK, scale / alpha,
-                                     k_raw + ((static_cast<long long>(b) * T + kr) * H + h) * D,
-                                     tab + static_cast<long long>(kr) * (D / 2), eps,
-                                     reinterpret_cast<float*>(smem + S::OFF_Q + row * S::U_STRIDE),
-                                     valid ? dk + ((static_cast<long long>(b) * T + key) * H + h) * D : nullptr);
+                norm_rope_bwd_tile_row<D>(tmem + lane_base + TM_DK, scale / alpha, smem + S::OFF_DO, smem + S::OFF_Q,
+                                          row, eps,
+                                          valid ? dk + ((static_cast<long long>(b) * T + key) * H + h) * D : nullptr);
             }
         }
     }

@@ -24,7 +24,8 @@
 //
 // Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 query rows,
 // key half w/4 = 64 columns), warp 8 TMA, warp 9 MMA; at the end warps 0-3
-// write dq.
+// write dq from the raw q rows and RoPE table rows that the producer stages
+// in shared memory once the last product is done.
 //
 // dS is stored as alpha * dS in fp16 with a per-CTA power of two alpha from
 // the bound |dS_ij| <= P_ij |dP_ij - delta_i| <= ||dout_i|| max_j ||v_j|| +
@@ -33,6 +34,7 @@
 #pragma once
 
 #include "nc_common.cuh"
+#include "nc_exp2.cuh"
 #include "nc_normrope_bwd.cuh"
 
 namespace nc {
@@ -57,7 +59,8 @@ enum Bar {
     DS_FULL = 14,  // softmax read dP_j and wrote dS_j
     DQ_FULL = 15,
     MMA_DONE = 16,
-    NUM_BARS = 17
+    EPI_FULL = 17,  // raw q tile and RoPE table tile staged for the dq epilogue
+    NUM_BARS = 18
 };
 
 template <int D>
@@ -72,10 +75,11 @@ struct Smem {
     static constexpr int OFF_MISC = OFF_TSLOT + 16;  // 4 warp maxima of the dS bound
     static constexpr int BYTES = OFF_MISC + 32;
     static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
-    // epilogue: u = RoPE^T(dQhat) rows staged over the (then idle) K ring
-    static constexpr int U_STRIDE = D * 4 + 16;
+    // dq epilogue, once every MMA is done: the raw q tile over the V ring,
+    // the RoPE table tile (fp32 [128][D]) over the K ring
+    static constexpr int CBYTES = BM * D * 4;
     static_assert(BYTES <= SMEM_LIMIT, "dQ tiles exceed shared memory");
-    static_assert(BM * U_STRIDE <= KSTAGES * TBYTES, "dq staging exceeds the K ring");
+    static_assert(CBYTES <= KSTAGES * TBYTES && TBYTES <= 2 * TBYTES, "epilogue tiles exceed the rings");
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -91,9 +95,9 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
                        const float* __restrict__ lse2, const float* __restrict__ delta,
-                       const unsigned int* __restrict__ gmax, const __nv_bfloat16* __restrict__ q_raw,
-                       const float2* __restrict__ tab, __nv_bfloat16* __restrict__ dq, int T, int H, int B,
+                       const unsigned int* __restrict__ gmax, __nv_bfloat16* __restrict__ dq, int T, int H, int B,
                        int Tpad, int group, float scale, float scale_log2, float eps) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
@@ -131,6 +135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(bar(DS_FULL), 256);
         mbar_init(bar(DQ_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
+        mbar_init(bar(EPI_FULL), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -172,6 +177,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (issued_k[s]) mbar_wait(bar(K_FULL + s), (issued_k[s] - 1) & 1, 0x124);
             for (int s = 0; s < 2; ++s)
                 if (issued_v[s]) mbar_wait(bar(V_FULL + s), (issued_v[s] - 1) & 1, 0x125);
+            // once every MMA is done the rings are free: stage the dq
+            // epilogue's raw q rows and RoPE table rows
+            if (mbar_wait(bar(DQ_FULL), 0, 0x126)) {
+                mbar_expect_tx(bar(EPI_FULL), S::TBYTES + S::CBYTES);
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_V + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM, b, bar(EPI_FULL));
+                for (int c = 0; c < D / 32; ++c)
+                    tma_load_2d(sb + S::OFF_K + c * (BM * 128), &tm_tab, c * 32, qt * BM, bar(EPI_FULL));
+                mbar_wait(bar(EPI_FULL), 0, 0x127);
+            }
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -302,7 +317,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int e = 0; e < 32; e += 2) {
                         const int kc = k0 + c * 32 + e;
                         float p0 = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2_row));
-                        float p1 = ex2(fmaf(__uint_as_float(r[c][e + 1]), scale_log2, -lse2_row));
+                        const float x1 = fmaf(__uint_as_float(r[c][e + 1]), scale_log2, -lse2_row);
+                        float p1 = (e & 2) ? exp2_poly(x1) : ex2(x1);  // one in four on the FMA pipe
                         if (diag) {
                             if (kc > row) p0 = 0.f;
                             if (kc + 1 > row) p1 = 0.f;
@@ -336,17 +352,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(DS_FULL));
         }
-        if (half == 0 && ok && mbar_wait(bar(DQ_FULL), 0, 0x323)) {
+        if (half == 0 && ok && mbar_wait(bar(DQ_FULL), 0, 0x323) && mbar_wait(bar(EPI_FULL), 0, 0x324)) {
             tc_fence_after();
-            // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)); every MMA and tile
-            // load has completed, so the K ring stages u
+            // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)) from the staged tiles
             const bool valid = q < T;
-            const int qr = valid ? q : T - 1;  // clamp reads of invalid rows
-            norm_rope_bwd_row<D>(tmem + lane_base + TM_DQ, scale / alpha,
-                                 q_raw + ((static_cast<long long>(b) * T + qr) * H + h) * D,
-                                 tab + static_cast<long long>(qr) * (D / 2), eps,
-                                 reinterpret_cast<float*>(smem + S::OFF_K + row * S::U_STRIDE),
-                                 valid ? dq + ((static_cast<long long>(b) * T + q) * H + h) * D : nullptr);
+            norm_rope_bwd_tile_row<D>(tmem + lane_base + TM_DQ, scale / alpha, smem + S::OFF_V, smem + S::OFF_K, row,
+                                      eps, valid ? dq + ((static_cast<long long>(b) * T + q) * H + h) * D : nullptr);
         }
     }
     tc_fence_before();

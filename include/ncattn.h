@@ -160,11 +160,11 @@ int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new,
  * memory and lends none to the library.  It computes exactly what
  * nc_attn_decode computes, with the same arguments minus the workspace.
  *  - Scratch lives in one fixed array of NC_DECODE_NOALLOC_SCRATCH_BYTES
- *    (8 MiB) inside the library, present on every device that loads the
+ *    (16 MiB) inside the library, present on every device that loads the
  *    library until the process exits.  Problems whose decode workspace
  *    (nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D)) exceeds it are
  *    rejected with NC_ETOOLARGE; nothing is launched.  (The 32-stream,
- *    10-head, D = 128, capacity 2048 case needs about 5.3 MB.)
+ *    10-head, D = 128, capacity 2048 case needs about 10.6 MB.)
  *  - The first call on a device looks up the array's device address; make
  *    that first call before any stream capture.
  *  - Every call on a device shares the one array.  Calls that may overlap on
@@ -173,7 +173,7 @@ int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new,
  *    workspaces.  Each call clears the counters it needs at its start.
  *  - No cudaMalloc, cudaFree or allocating library routine is called. */
 #define NC_ETOOLARGE (-5)
-#define NC_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define NC_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 int nc_attn_decode_noalloc(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
                            nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, int B, int H, int D, int Tcap,
