@@ -143,9 +143,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(QE + s), 1);
         }
         mbar_init(bar(S_FULL), 1);
-        mbar_init(bar(P_FULL), 256);
+        mbar_init(bar(P_FULL), 8);   // one arrival per softmax warp
         mbar_init(bar(DP_FULL), 1);
-        mbar_init(bar(DS_FULL), 256);
+        mbar_init(bar(DS_FULL), 8);
         mbar_init(bar(DKV_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int key = kt * BN + row;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int cbase = half * 64;  // this warp's query columns
-        bool ok = mbar_wait(bar(KV_FULL), 0, 0x310);
+        bool ok = mbar_wait_warp(bar(KV_FULL), 0, 0x310);
         // dS scale alpha (see the header comment): max ||v_j|| over this tile
         // from shared memory, the global row-norm maxima from the preprocess.
         if (half == 0) {
@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int it = 0; ok && it < n_it; ++it) {
             const int st = it & 1, use = it >> 1;
             const int q0 = (qb0 + it) * BM + cbase;
-            if (!mbar_wait(bar(QF + st), use & 1, 0x311)) { ok = false; break; }
-            if (!mbar_wait(bar(S_FULL), it & 1, 0x312)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(QF + st), use & 1, 0x311)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(S_FULL), it & 1, 0x312)) { ok = false; break; }
             tc_fence_after();
             const float4* l2 = reinterpret_cast<const float4*>(smem + S::OFF_L + st * BM * 4 + cbase * 4);
             const float4* dl = reinterpret_cast<const float4*>(smem + S::OFF_DL + st * BM * 4 + cbase * 4);
@@ -345,9 +345,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_st16(ts + cbase + 16, pk + 16);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(P_FULL));
+            mbar_arrive_warp(bar(P_FULL));
             // dS^T = P^T o (dP^T - delta) * alpha as fp16 pairs over this half's dP^T columns
-            if (!mbar_wait(bar(DP_FULL), it & 1, 0x313)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(DP_FULL), it & 1, 0x313)) { ok = false; break; }
             tc_fence_after();
             {
                 uint32_t r[2][32];
@@ -377,9 +377,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(DS_FULL));
+            mbar_arrive_warp(bar(DS_FULL));
         }
-        if (ok && mbar_wait(bar(DKV_FULL), 0, 0x315)) {
+        if (ok && mbar_wait_warp(bar(DKV_FULL), 0, 0x315)) {
             tc_fence_after();
             if (half == 0) {
                 // dv: one key row per thread
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
                     }
                 }
-            } else if (mbar_wait(bar(EPI_FULL), 0, 0x316)) {
+            } else if (mbar_wait_warp(bar(EPI_FULL), 0, 0x316)) {
                 // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha)) from the staged tiles
                 const bool valid = key < T;
                 norm_rope_bwd_tile_row<D>(tmem + lane_base + TM_DK, scale / alpha, smem + S::OFF_DO, smem + S::OFF_Q,

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(S_FULL + s), 1);
         }
         mbar_init(bar(DP_FULL), 1);
-        mbar_init(bar(DS_FULL), 256);
+        mbar_init(bar(DS_FULL), 8);   // one arrival per softmax warp
         mbar_init(bar(DQ_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int cbase = half * 64;  // this warp's key columns
         const float lse2_row = lse2[bh * Tpad + q];  // +inf on padded rows: P = 0
         const float delta_row = delta[bh * Tpad + q];
-        bool ok = mbar_wait(bar(QD_FULL), 0, 0x320);
+        bool ok = mbar_wait_warp(bar(QD_FULL), 0, 0x320);
         // dS scale: the largest per-row bound over the tile
         if (half == 0) {
             float dn = 0.f;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         named_bar_sync(1, 256);
         const float alpha = ds_scale_for(fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3])) * 1.0625f);
         for (int j = 0; ok && j < n_kv; ++j) {
-            if (!mbar_wait(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ts = tmem + lane_base + tm_s(j & 1) + cbase;
             const bool diag = (j == qt);  // only the diagonal tile has masked entries
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                     }
             }
-            if (!mbar_wait(bar(DP_FULL), j & 1, 0x322)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(DP_FULL), j & 1, 0x322)) { ok = false; break; }
             tc_fence_after();
             {
                 uint32_t r[2][32];
@@ -350,9 +350,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(DS_FULL));
+            mbar_arrive_warp(bar(DS_FULL));
         }
-        if (half == 0 && ok && mbar_wait(bar(DQ_FULL), 0, 0x323) && mbar_wait(bar(EPI_FULL), 0, 0x324)) {
+        if (half == 0 && ok && mbar_wait_warp(bar(DQ_FULL), 0, 0x323) && mbar_wait_warp(bar(EPI_FULL), 0, 0x324)) {
             tc_fence_after();
             // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)) from the staged tiles
             const bool valid = q < T;

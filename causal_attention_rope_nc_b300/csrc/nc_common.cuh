@@ -130,6 +130,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One arrival for the whole warp: the lanes' prior writes are ordered before
+// the leader's (releasing) arrive by the warp barrier.  Barriers that count
+// warps instead of threads avoid one shared-memory atomic per thread.  Only
+// the active lanes synchronise, so a warp that (on an error path) is not
+// converged cannot deadlock here.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+    const unsigned m = __activemask();
+    __syncwarp(m);
+    if ((threadIdx.x & 31) == __ffs(m) - 1) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -157,6 +168,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
             return false;
         }
     }
+}
+
+// mbar_wait for warp-collective code: every lane waits, then the lanes agree
+// on the outcome, so a timeout near the deadline cannot split the warp
+// between the success and the error path (the warp-synchronous tcgen05 and
+// shuffle instructions that follow need the whole warp).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned int site) {
+    const bool ok = mbar_wait(bar, parity, site);
+    return __all_sync(__activemask(), ok);
 }
 
 // ---------------------------------------------------------------------- TMA --

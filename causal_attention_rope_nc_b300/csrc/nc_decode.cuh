@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(MAX_CONSUMERS + 32) attn_decode_kernel(
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), NCONS);
+            mbar_init(empty_bar(s), NCONS / 32);  // one arrival per consumer warp
         }
         fence_mbar_init();
     }
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(MAX_CONSUMERS + 32) attn_decode_kernel(
         for (int j = s0; j < s1; j += sps) {
             const int n = min(sps, s1 - j);
             const int st = consumed % STAGES;
-            if (ok && !mbar_wait(full_bar(st), (consumed / STAGES) & 1, 0x521)) ok = false;
+            if (ok && !mbar_wait_warp(full_bar(st), (consumed / STAGES) & 1, 0x521)) ok = false;
             const uint8_t* kst = dsm + LY.ring + st * stage_bytes;
             const uint8_t* vst = kst + stage_bytes / 2;
             // scores of this thread's slots first (independent chains), then one
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(MAX_CONSUMERS + 32) attn_decode_kernel(
                     for (int e = 0; e < 8; ++e) acc[e] = fmaf(pe, vf[e], acc[e]);
                 }
             }
-            mbar_arrive(empty_bar(st));
+            mbar_arrive_warp(empty_bar(st));
             ++consumed;
         }
 

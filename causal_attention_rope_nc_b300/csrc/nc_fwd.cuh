@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(V_FULL + s), 1);
             mbar_init(bar(V_EMPTY + s), 1);
             mbar_init(bar(S_FULL + s), 1);
-            mbar_init(bar(P_FULL + s), 128);
+            mbar_init(bar(P_FULL + s), 4);  // one arrival per softmax warp of the tile
             mbar_init(bar(O_FULL + s), 1);
         }
         mbar_init(bar(MMA_DONE), 1);
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_t; ++j) {
-            if (!mbar_wait(bar(S_FULL + t), j & 1, 0x301)) { ok = false; break; }
+            if (!mbar_wait_warp(bar(S_FULL + t), j & 1, 0x301)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (j == qt);
             uint32_t r[2][32];
@@ -276,9 +276,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(P_FULL + t));
+            mbar_arrive_warp(bar(P_FULL + t));
         }
-        if (n_t > 0 && ok && mbar_wait(bar(O_FULL + t), 0, 0x303)) {
+        if (n_t > 0 && ok && mbar_wait_warp(bar(O_FULL + t), 0, 0x303)) {
             tc_fence_after();
             const float inv_l = 1.f / l_sum;
             const bool valid = q_idx < T;
