@@ -279,10 +279,12 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
             lse2, gmax, B, T, H, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab;
+    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, H, D, 128, kF16) ||
         make_tmap(&tv, v, B, T, H, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
-        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, H, D, 128) || make_tab_tmap(&ttab, tab, T, D))
+        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, H, D, 128) || make_tab_tmap(&ttab, tab, T, D) ||
+        make_tmap(&tdq, dq, B, T, H, D, 128) || make_tmap(&tdk, dk, B, T, H, D, 128) ||
+        make_tmap(&tdv, dv, B, T, H, D, 128))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -294,8 +296,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         ProfScope ps("attn_bwd_dkdv", s);
         nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS,
                                            nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tkr, ttab, lse2, delta, gmax, reinterpret_cast<__nv_bfloat16*>(dk),
-            reinterpret_cast<__nv_bfloat16*>(dv), T, H, B, Tpad, group,
+            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, T, H, B, Tpad, group,
             float(scale), float(scale * 1.4426950408889634), eps);
     }
     if ((rc = launch_status())) return rc;
@@ -305,8 +306,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         ProfScope ps("attn_bwd_dq", s);
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
                                           nc::bwdq::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tqr, ttab, lse2, delta, gmax, reinterpret_cast<__nv_bfloat16*>(dq), T, H, B, Tpad,
-            group, float(scale),
+            tq, tk, tv, tdo, tqr, ttab, tdq, lse2, delta, gmax, T, H, B, Tpad, group, float(scale),
             float(scale * 1.4426950408889634), eps);
     }
     return launch_status();

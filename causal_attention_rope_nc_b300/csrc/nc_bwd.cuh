@@ -26,10 +26,13 @@
 // so each softmax phase overlaps two products.
 //
 // Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 key rows,
-// query half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end warps 0-3
-// write dv and warps 4-7 dk (through the RoPE transpose and the RMSNorm
-// backward, from the raw k rows and RoPE table rows that the producer stages
-// in shared memory once the last product is done).
+// query half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end the same
+// eight warps stage dv and then dk (through the RoPE transpose and the RMSNorm
+// backward, two threads per key row) in shared memory, and both tiles leave
+// through TMA stores.  The raw k rows and RoPE table rows that dk needs are
+// prefetched during the last query block: the table over the query stage the
+// last block does not use, the raw rows over the khat tile once the last
+// product that reads khat and v is done.
 //
 // Operand types: the score side (qhat, khat, dS) is IEEE fp16, the value
 // side (P, v, dout) bf16; tcgen05 wants A and B of one product in one type.
@@ -67,7 +70,8 @@ enum Bar {
     DKV_FULL = 9,
     MMA_DONE = 10,
     EPI_FULL = 11,  // raw k tile and RoPE table tile staged for the dk epilogue
-    NUM_BARS = 12
+    KV_FREE = 12,   // the last products reading khat and v are done
+    NUM_BARS = 13
 };
 
 template <int D>
@@ -85,12 +89,14 @@ struct Smem {
     static constexpr int OFF_MISC = OFF_TSLOT + 16;  // 4 warp maxima of ||v_j||^2
     static constexpr int BYTES = OFF_MISC + 32;
     static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
-    // dk epilogue, once every MMA is done: the raw k tile over the dout
-    // stages, the RoPE table tile (fp32 [128][D]) over the qhat stages
+    // epilogue: the raw k tile over the khat tile, the RoPE table tile (fp32
+    // [128][D]) over the qhat and dout halves of the stage the last block
+    // does not use; dv staged over the v tile, dk over the last block's qhat
+    // stage, the row-half exchange over its dout stage
     static constexpr int XBYTES = BN * D * 2;
     static constexpr int CBYTES = BN * D * 4;
     static_assert(BYTES <= SMEM_LIMIT, "backward tiles exceed shared memory");
-    static_assert(XBYTES <= 2 * QBYTES && CBYTES <= 2 * QBYTES, "epilogue tiles exceed the stages");
+    static_assert(XBYTES <= KBYTES && CBYTES == 2 * QBYTES && 2 * BN * 8 <= QBYTES, "epilogue tiles exceed the stages");
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -109,9 +115,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_kraw, const __grid_constant__ CUtensorMap tm_tab,
+                         const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                          const float* __restrict__ lse2, const float* __restrict__ delta,
-                         unsigned int* __restrict__ gmax, __nv_bfloat16* __restrict__ dk,
-                         __nv_bfloat16* __restrict__ dv, int T, int H, int B, int Tpad, int group, float scale,
+                         unsigned int* __restrict__ gmax, int T, int H, int B, int Tpad, int group, float scale,
                          float scale_log2, float eps) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
@@ -135,6 +141,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
     const long long bh = static_cast<long long>(b) * H + h;
+    const int sp = n_it & 1;             // query stage the last block does not use
+    const int st_last = (n_it - 1) & 1;  // the last block's query stage
 
     if (threadIdx.x == 0) {
         mbar_init(bar(KV_FULL), 1);
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(bar(DKV_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
+        mbar_init(bar(KV_FREE), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -184,20 +193,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bulk_load(sb + S::OFF_DL + st * BM * 4, delta + bh * Tpad + q0, BM * 4, bar(QF + st));
                 ++issued[st];
             }
+            // dk epilogue tiles, each as soon as its space is free: the RoPE
+            // table rows over stage sp (free once block n_it-2 is done), the
+            // raw k rows over the khat tile
+            mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
+            bool epi = n_it < 2 || mbar_wait(bar(QE + sp), ((n_it - 2) >> 1) & 1, 0x117);
+            if (epi) {
+                for (int c = 0; c < D / 32; ++c) {
+                    const uint32_t dst = c < NC ? S::OFF_Q + sp * S::QBYTES + c * (BN * 128)
+                                                : S::OFF_DO + sp * S::QBYTES + (c - NC) * (BN * 128);
+                    tma_load_2d(sb + dst, &tm_tab, c * 32, kt * BN, bar(EPI_FULL));
+                }
+            }
+            epi = epi && mbar_wait(bar(KV_FREE), 0, 0x118);
+            if (epi) {
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_K + c * (BN * 128), &tm_kraw, c * 64, h, kt * BN, b, bar(EPI_FULL));
+            }
             // never leave the CTA with a bulk copy still in flight
             mbar_wait(bar(KV_FULL), 0, 0x112);
             for (int s = 0; s < 2; ++s)
                 if (issued[s]) mbar_wait(bar(QF + s), (issued[s] - 1) & 1, 0x113);
-            // once every MMA is done the stages are free: stage the dk
-            // epilogue's raw k rows and RoPE table rows
-            if (mbar_wait(bar(DKV_FULL), 0, 0x114)) {
-                mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
-                for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_DO + c * (BN * 128), &tm_kraw, c * 64, h, kt * BN, b, bar(EPI_FULL));
-                for (int c = 0; c < D / 32; ++c)
-                    tma_load_2d(sb + S::OFF_Q + c * (BN * 128), &tm_tab, c * 32, kt * BN, bar(EPI_FULL));
-                mbar_wait(bar(EPI_FULL), 0, 0x115);
-            }
+            if (epi) mbar_wait(bar(EPI_FULL), 0, 0x115);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -234,6 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 issue_s(0);
                 issue_dp(0);
+                if (n_it == 1) mma_commit(bar(KV_FREE));
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it & 1;
@@ -266,7 +284,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                (it > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(bar(QE + st));
                 }
-                if (more) issue_dp(st ^ 1);
+                if (more) {
+                    issue_dp(st ^ 1);
+                    if (it + 2 == n_it) mma_commit(bar(KV_FREE));  // that was the last dP
+                }
             }
             if (ok) mma_commit(bar(DKV_FULL));
             // all MMAs issued by this thread complete before teardown
@@ -379,35 +400,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive_warp(bar(DS_FULL));
         }
-        if (ok && mbar_wait_warp(bar(DKV_FULL), 0, 0x315)) {
+        // ------------------------------------------------------ epilogue ----
+        // Every barrier below is reached by all 256 threads; the AND-barriers
+        // keep their branches uniform even if a wait timed out somewhere.
+        const bool epi = named_bar_and(1, 256, ok && mbar_wait_warp(bar(DKV_FULL), 0, 0x315));
+        uint8_t* dv_stage = smem + S::OFF_V;
+        uint8_t* dk_stage = smem + S::OFF_Q + st_last * S::QBYTES;
+        float2* xch = reinterpret_cast<float2*>(smem + S::OFF_DO + st_last * S::QBYTES);
+        if (epi) {
             tc_fence_after();
-            if (half == 0) {
-                // dv: one key row per thread
-                const bool valid = key < T;
-                __nv_bfloat16* vrow = dv + ((static_cast<long long>(b) * T + key) * H + h) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + TM_DV + c * 32, r);
-                    tmem_wait_ld();
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(vrow + c * 32);
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            dst[g] = make_uint4(
-                                pack_bf16x2(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1])),
-                                pack_bf16x2(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3])),
-                                pack_bf16x2(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5])),
-                                pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
-                    }
-                }
-            } else if (mbar_wait_warp(bar(EPI_FULL), 0, 0x316)) {
-                // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha)) from the staged tiles
-                const bool valid = key < T;
-                norm_rope_bwd_tile_row<D>(tmem + lane_base + TM_DK, scale / alpha, smem + S::OFF_DO, smem + S::OFF_Q,
-                                          row, eps,
-                                          valid ? dk + ((static_cast<long long>(b) * T + key) * H + h) * D : nullptr);
+            stage_acc_bf16<D / 2>(tmem + lane_base + TM_DV, 1.f, dv_stage, row, half * (D / 2));
+            fence_proxy_async_smem();
+        }
+        const bool epi_dk = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), 0, 0x316));
+        if (epi && threadIdx.x == 0) {
+            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dv, sb + S::OFF_V + c * (BN * 128), c * 64, h, kt * BN, b);
+            bulk_commit();
+        }
+        // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha))
+        norm_rope_bwd_stage<D>(epi_dk, tmem + lane_base + TM_DK, scale / alpha, smem + S::OFF_K,
+                               smem + S::OFF_Q + sp * S::QBYTES, smem + S::OFF_DO + sp * S::QBYTES, row, half, eps,
+                               xch, dk_stage, 1, 256);
+        if (epi_dk) fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+        if (threadIdx.x == 0) {
+            if (epi_dk) {
+                for (int c = 0; c < NC; ++c)
+                    tma_store_4d(&tm_dk, smem_u32(dk_stage) + c * (BN * 128), c * 64, h, kt * BN, b);
+                bulk_commit();
             }
+            bulk_wait_read_all();  // the staged tiles stay valid until the stores have read them
         }
     }
     tc_fence_before();

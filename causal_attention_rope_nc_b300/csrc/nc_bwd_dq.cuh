@@ -23,9 +23,11 @@
 // V tiles in a 2-stage ring.
 //
 // Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 query rows,
-// key half w/4 = 64 columns), warp 8 TMA, warp 9 MMA; at the end warps 0-3
-// write dq from the raw q rows and RoPE table rows that the producer stages
-// in shared memory once the last product is done.
+// key half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end the same
+// eight warps (two threads per query row) stage dq in shared memory and it
+// leaves through TMA stores.  The raw q rows and RoPE table rows it needs
+// are prefetched while the last key tiles are processed, into the v stage
+// and the two k stages the last key tile does not use, as they free up.
 //
 // dS is stored as alpha * dS in fp16 with a per-CTA power of two alpha from
 // the bound |dS_ij| <= P_ij |dP_ij - delta_i| <= ||dout_i|| max_j ||v_j|| +
@@ -75,11 +77,12 @@ struct Smem {
     static constexpr int OFF_MISC = OFF_TSLOT + 16;  // 4 warp maxima of the dS bound
     static constexpr int BYTES = OFF_MISC + 32;
     static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
-    // dq epilogue, once every MMA is done: the raw q tile over the V ring,
-    // the RoPE table tile (fp32 [128][D]) over the K ring
+    // epilogue: the raw q tile over a v stage, the RoPE table tile (fp32
+    // [128][D]) over two k stages, dq staged over the qhat tile and the
+    // row-half exchange over the dout tile
     static constexpr int CBYTES = BM * D * 4;
     static_assert(BYTES <= SMEM_LIMIT, "dQ tiles exceed shared memory");
-    static_assert(CBYTES <= KSTAGES * TBYTES && TBYTES <= 2 * TBYTES, "epilogue tiles exceed the rings");
+    static_assert(CBYTES == 2 * TBYTES && 2 * BM * 8 <= TBYTES, "epilogue tiles exceed the rings");
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -96,8 +99,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
-                       const float* __restrict__ lse2, const float* __restrict__ delta,
-                       const unsigned int* __restrict__ gmax, __nv_bfloat16* __restrict__ dq, int T, int H, int B,
+                       const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
+                       const float* __restrict__ delta, const unsigned int* __restrict__ gmax, int T, int H, int B,
                        int Tpad, int group, float scale, float scale_log2, float eps) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
@@ -119,6 +122,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
     const long long bh = static_cast<long long>(b) * H + h;
+    // epilogue space: the v stage of key tile n_kv-2 and the k stages of
+    // tiles n_kv-3 and n_kv-2 (never used when those tiles do not exist)
+    const int vs_epi = n_kv & 1, ks_a = n_kv % KSTAGES, ks_b = (n_kv + 1) % KSTAGES;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(QD_FULL), 1);
@@ -171,22 +177,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 bar(V_FULL + vs));
                 ++issued_v[vs];
             }
+            // dq epilogue tiles, each as soon as its stage is released
+            mbar_expect_tx(bar(EPI_FULL), S::TBYTES + S::CBYTES);
+            bool epi = n_kv < 2 || mbar_wait(bar(V_EMPTY + vs_epi), ((n_kv - 2) >> 1) & 1, 0x128);
+            if (epi) {
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_V + vs_epi * S::TBYTES + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM,
+                                b, bar(EPI_FULL));
+            }
+            epi = epi && (n_kv < 3 || mbar_wait(bar(K_EMPTY + ks_a), ((n_kv - 3) / KSTAGES) & 1, 0x129));
+            if (epi) {
+                for (int c = 0; c < NC; ++c)
+                    tma_load_2d(sb + S::OFF_K + ks_a * S::TBYTES + c * (BM * 128), &tm_tab, c * 32, qt * BM,
+                                bar(EPI_FULL));
+            }
+            epi = epi && (n_kv < 2 || mbar_wait(bar(K_EMPTY + ks_b), ((n_kv - 2) / KSTAGES) & 1, 0x12a));
+            if (epi) {
+                for (int c = 0; c < NC; ++c)
+                    tma_load_2d(sb + S::OFF_K + ks_b * S::TBYTES + c * (BM * 128), &tm_tab, (NC + c) * 32,
+                                qt * BM, bar(EPI_FULL));
+            }
             // never leave the CTA with a bulk copy still in flight
             mbar_wait(bar(QD_FULL), 0, 0x123);
             for (int s = 0; s < KSTAGES; ++s)
                 if (issued_k[s]) mbar_wait(bar(K_FULL + s), (issued_k[s] - 1) & 1, 0x124);
             for (int s = 0; s < 2; ++s)
                 if (issued_v[s]) mbar_wait(bar(V_FULL + s), (issued_v[s] - 1) & 1, 0x125);
-            // once every MMA is done the rings are free: stage the dq
-            // epilogue's raw q rows and RoPE table rows
-            if (mbar_wait(bar(DQ_FULL), 0, 0x126)) {
-                mbar_expect_tx(bar(EPI_FULL), S::TBYTES + S::CBYTES);
-                for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM, b, bar(EPI_FULL));
-                for (int c = 0; c < D / 32; ++c)
-                    tma_load_2d(sb + S::OFF_K + c * (BM * 128), &tm_tab, c * 32, qt * BM, bar(EPI_FULL));
-                mbar_wait(bar(EPI_FULL), 0, 0x127);
-            }
+            if (epi) mbar_wait(bar(EPI_FULL), 0, 0x127);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -352,12 +369,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive_warp(bar(DS_FULL));
         }
-        if (half == 0 && ok && mbar_wait_warp(bar(DQ_FULL), 0, 0x323) && mbar_wait_warp(bar(EPI_FULL), 0, 0x324)) {
-            tc_fence_after();
-            // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)) from the staged tiles
-            const bool valid = q < T;
-            norm_rope_bwd_tile_row<D>(tmem + lane_base + TM_DQ, scale / alpha, smem + S::OFF_V, smem + S::OFF_K, row,
-                                      eps, valid ? dq + ((static_cast<long long>(b) * T + q) * H + h) * D : nullptr);
+        // ------------------------------------------------------ epilogue ----
+        // Every barrier below is reached by all 256 threads; the AND-barriers
+        // keep their branches uniform even if a wait timed out somewhere.
+        bool epi = named_bar_and(1, 256, ok && mbar_wait_warp(bar(DQ_FULL), 0, 0x323));
+        epi = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), 0, 0x324));
+        if (epi) tc_fence_after();
+        // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha))
+        norm_rope_bwd_stage<D>(epi, tmem + lane_base + TM_DQ, scale / alpha, smem + S::OFF_V + vs_epi * S::TBYTES,
+                               smem + S::OFF_K + ks_a * S::TBYTES, smem + S::OFF_K + ks_b * S::TBYTES, row, half,
+                               eps, reinterpret_cast<float2*>(smem + S::OFF_DO), smem + S::OFF_Q, 1, 256);
+        if (epi) fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+        if (epi && threadIdx.x == 0) {
+            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dq, sb + S::OFF_Q + c * (BM * 128), c * 64, h, qt * BM, b);
+            bulk_commit();
+            bulk_wait_read_all();  // the staged tile stays valid until the stores have read it
         }
     }
     tc_fence_before();

@@ -1,5 +1,5 @@
 // Backward of the QK RMSNorm + RoPE prologue for one head vector, fused into
-// the epilogues of the backward kernels (thread = one token's head vector).
+// the epilogues of the backward kernels (two threads per token's head vector).
 //
 // Given the gradient g with respect to xhat = RoPE(x / r, p) (r =
 // sqrt(mean(x^2) + eps)), the gradient with respect to the raw x is
@@ -11,74 +11,119 @@
 
 namespace nc {
 
-// dx for row `row` of a 128-row tile whose raw x rows (bf16, D/64 spans)
-// and RoPE table rows (fp32 (cos, sin) pairs, D/32 spans) were staged in
-// shared memory by TMA with 128-byte swizzling, g = out_scale * (the D fp32
-// columns of this thread's TMEM lane at `tm`), read twice (once for <u, y>,
-// once for the output).  dx == nullptr: no store (rows past the sequence end
-// still take part, tcgen05.ld being warp-collective).
-template <int D>
-__device__ __forceinline__ void norm_rope_bwd_tile_row(uint32_t tm, float out_scale, const uint8_t* xt,
-                                                       const uint8_t* ct, int row, float eps,
-                                                       __nv_bfloat16* __restrict__ dx) {
-    constexpr int HALF = D / 2;
-    // 8 bf16 of x starting at element e (e % 8 == 0); 4 fp32 of the table at f (f % 4 == 0)
-    auto xchunk = [&](int e) -> uint4 {
-        return *reinterpret_cast<const uint4*>(xt + (e >> 6) * (128 * 128) + sw128_offset(row, (e & 63) >> 3));
-    };
-    auto cchunk = [&](int f) -> float4 {
-        return *reinterpret_cast<const float4*>(ct + (f >> 5) * (128 * 128) + sw128_offset(row, (f & 31) >> 2));
-    };
-    float ss = 0.f;
+// Byte offset of the 8 16-bit values at columns [col, col + 8) of row `row`
+// in a [128][D] tile kept as D/64 boxes of 128 rows x 128 bytes with 128-byte
+// swizzling: the shared-memory layout of a TMA box of 64 values x 128 rows.
+__device__ __forceinline__ uint32_t tile16_off(int row, int col) {
+    return static_cast<uint32_t>((col >> 6) * (128 * 128)) + sw128_offset(row, (col & 63) >> 3);
+}
+
+// N consecutive TMEM columns of this warp's 32 lanes (thread i: lane base + i).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t tm, uint32_t (&r)[N]) {
+    static_assert(N % 16 == 0, "column count");
+    if constexpr (N % 32 == 0) {
 #pragma unroll
-    for (int g = 0; g < D / 8; ++g) {
-        float y[8];
-        bf16x8_to_f32(xchunk(g * 8), y);
+        for (int i = 0; i < N / 32; ++i) tmem_ld32(tm + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * i));
+    } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(y[i], y[i], ss);
+        for (int i = 0; i < N / 16; ++i) tmem_ld16(tm + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
     }
-    const float rsd = rsqrtf(ss / D + eps);
-    float dot = 0.f;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        const float m = dot / D;
-#pragma unroll 2
-        for (int ch = 0; ch < HALF / 8; ++ch) {
-            uint32_t glo[8], ghi[8];
-            tmem_ld8(tm + ch * 8, glo);
-            tmem_ld8(tm + HALF + ch * 8, ghi);
-            float ylo[8], yhi[8];
-            bf16x8_to_f32(xchunk(ch * 8), ylo);
-            bf16x8_to_f32(xchunk(HALF + ch * 8), yhi);
-            float4 c4[4];
+}
+
+// bf16(s * acc) for row `row`, columns [c0, c0 + NCOL) of a TMEM fp32
+// accumulator (tm = the accumulator's first column, this warp's lanes), into
+// a staging tile in the layout of tile16_off.
+template <int NCOL>
+__device__ __forceinline__ void stage_acc_bf16(uint32_t tm, float s, uint8_t* stage, int row, int c0) {
+    uint32_t r[NCOL];
+    tmem_ld_cols<NCOL>(tm + c0, r);
+    tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c4[i] = cchunk(16 * ch + 4 * i);
-            tmem_wait_ld();
-            float olo[8], ohi[8];
+    for (int g = 0; g < NCOL / 8; ++g) {
+        const uint32_t* v = r + 8 * g;
+        *reinterpret_cast<uint4*>(stage + tile16_off(row, c0 + 8 * g)) = make_uint4(
+            pack_bf16x2(__uint_as_float(v[0]) * s, __uint_as_float(v[1]) * s),
+            pack_bf16x2(__uint_as_float(v[2]) * s, __uint_as_float(v[3]) * s),
+            pack_bf16x2(__uint_as_float(v[4]) * s, __uint_as_float(v[5]) * s),
+            pack_bf16x2(__uint_as_float(v[6]) * s, __uint_as_float(v[7]) * s));
+    }
+}
+
+// dx for one 128-row tile, two threads per row: thread `half` takes the
+// rotation pairs (f, f + D/2) for f in [half D/4, (half + 1) D/4).
+//   g   = out_scale * (the D fp32 columns of TMEM lane `row` at `tm`)
+//   u   = R(p)^T g
+//   dx  = u rsd - x rsd^3 <u, x> / D,   rsd = 1 / sqrt(mean(x^2) + eps)
+// (the same as (u - y <u, y> / D) rsd with y = x rsd).  The raw x rows (bf16,
+// layout of tile16_off) and the RoPE table rows (fp32 (cos, sin) pairs as
+// D/32 boxes of 32 values x 128 rows, 128-byte swizzled; boxes [0, D/64) at
+// ct0, the rest at ct1) were staged by TMA.  The two halves of a row swap
+// their partial sums of x^2 and <u, x> through xch (2 x 128 float2) across
+// named barrier `bar_id` over `nthreads` threads, which every participating
+// thread reaches exactly once whether or not it is `active`.  The bf16 dx
+// goes into `stage` (layout of tile16_off).
+template <int D>
+__device__ __forceinline__ void norm_rope_bwd_stage(bool active, uint32_t tm, float out_scale, const uint8_t* xt,
+                                                    const uint8_t* ct0, const uint8_t* ct1, int row, int half,
+                                                    float eps, float2* xch, uint8_t* stage, int bar_id,
+                                                    int nthreads) {
+    constexpr int HALF = D / 2, NF = D / 4;
+    const int f0 = half * NF;
+    const uint8_t* ct = half ? ct1 : ct0;  // this half's table floats [2 f0, 2 f0 + 2 NF)
+    uint32_t u[2][NF];                     // g, then u, for the lo and hi columns
+    float ss = 0.f, dot = 0.f;
+    if (active) {
+        tmem_ld_cols<NF>(tm + f0, u[0]);
+        tmem_ld_cols<NF>(tm + HALF + f0, u[1]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float c = (e & 1) ? c4[e >> 1].z : c4[e >> 1].x;
-                const float sn = (e & 1) ? c4[e >> 1].w : c4[e >> 1].y;
-                const float a = __uint_as_float(glo[e]) * out_scale;
-                const float bb = __uint_as_float(ghi[e]) * out_scale;
-                // R^T: (a, b) -> (a c + b s, -a s + b c)
-                const float ulo = a * c + bb * sn;
-                const float uhi = -a * sn + bb * c;
-                const float yl = ylo[e] * rsd, yh = yhi[e] * rsd;
-                if (pass == 0) {
-                    dot = fmaf(ulo, yl, fmaf(uhi, yh, dot));
-                } else {
-                    olo[e] = (ulo - yl * m) * rsd;
-                    ohi[e] = (uhi - yh * m) * rsd;
+        for (int ch = 0; ch < NF / 8; ++ch) {
+            const int e0 = f0 + ch * 8;
+            float xl[8], xh[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(xt + tile16_off(row, e0)), xl);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(xt + tile16_off(row, HALF + e0)), xh);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = 16 * ch + 4 * i;  // table float index relative to this half
+                const float4 cs =
+                    *reinterpret_cast<const float4*>(ct + (f >> 5) * (128 * 128) + sw128_offset(row, (f & 31) >> 2));
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = ch * 8 + 2 * i + k;
+                    const float c = k ? cs.z : cs.x, sn = k ? cs.w : cs.y;
+                    const float a = __uint_as_float(u[0][e]) * out_scale;
+                    const float bb = __uint_as_float(u[1][e]) * out_scale;
+                    // R^T: (a, b) -> (a c + b s, b c - a s)
+                    const float ul = fmaf(a, c, bb * sn), uh = fmaf(bb, c, -a * sn);
+                    u[0][e] = __float_as_uint(ul);
+                    u[1][e] = __float_as_uint(uh);
+                    const float x0 = xl[2 * i + k], x1 = xh[2 * i + k];
+                    ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+                    dot = fmaf(ul, x0, fmaf(uh, x1, dot));
                 }
             }
-            if (pass == 1 && dx != nullptr) {
-                *reinterpret_cast<uint4*>(dx + ch * 8) =
-                    make_uint4(pack_bf16x2(olo[0], olo[1]), pack_bf16x2(olo[2], olo[3]), pack_bf16x2(olo[4], olo[5]),
-                               pack_bf16x2(olo[6], olo[7]));
-                *reinterpret_cast<uint4*>(dx + HALF + ch * 8) =
-                    make_uint4(pack_bf16x2(ohi[0], ohi[1]), pack_bf16x2(ohi[2], ohi[3]), pack_bf16x2(ohi[4], ohi[5]),
-                               pack_bf16x2(ohi[6], ohi[7]));
+        }
+        xch[half * 128 + row] = make_float2(ss, dot);
+    }
+    named_bar_sync(bar_id, nthreads);
+    if (active) {
+        const float2 o = xch[(half ^ 1) * 128 + row];
+        ss += o.x;
+        dot += o.y;
+        const float rsd = rsqrtf(ss / D + eps);
+        const float kx = rsd * rsd * rsd * dot / D;
+#pragma unroll
+        for (int ch = 0; ch < NF / 8; ++ch) {
+            const int e0 = f0 + ch * 8;
+#pragma unroll
+            for (int side = 0; side < 2; ++side) {
+                const uint32_t off = tile16_off(row, side * HALF + e0);
+                float x[8], o8[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(xt + off), x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = fmaf(__uint_as_float(u[side][ch * 8 + e]), rsd, -x[e] * kx);
+                *reinterpret_cast<uint4*>(stage + off) = f32x8_to_bf16(o8);
             }
         }
     }
