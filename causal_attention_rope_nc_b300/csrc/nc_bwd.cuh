@@ -46,7 +46,7 @@
 #pragma once
 
 #include "nc_common.cuh"
-#include "nc_exp2.cuh"
+#include <type_traits>
 #include "nc_normrope_bwd.cuh"
 
 namespace nc {
@@ -299,7 +299,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------- P, dS ----
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;  // key row within the tile = TMEM lane
-        const int key = kt * BN + row;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int cbase = half * 64;  // this warp's query columns
         bool ok = mbar_wait_warp(bar(KV_FULL), 0, 0x310);
@@ -329,38 +328,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t ts = tmem + lane_base + TM_S, tdp = tmem + lane_base + TM_DP;
         for (int it = 0; ok && it < n_it; ++it) {
             const int st = it & 1, use = it >> 1;
-            const int q0 = (qb0 + it) * BM + cbase;
             if (!mbar_wait_warp(bar(QF + st), use & 1, 0x311)) { ok = false; break; }
             if (!mbar_wait_warp(bar(S_FULL), it & 1, 0x312)) { ok = false; break; }
             tc_fence_after();
             const float4* l2 = reinterpret_cast<const float4*>(smem + S::OFF_L + st * BM * 4 + cbase * 4);
             const float4* dl = reinterpret_cast<const float4*>(smem + S::OFF_DL + st * BM * 4 + cbase * 4);
-            const bool diag = (it == 0);  // only the diagonal block has masked entries
-            // P^T = exp2(S^T scale log2e - lse2) as bf16 pairs over this half's S^T columns
+            // P^T = exp2(S^T scale log2e - lse2) as bf16 pairs over this half's S^T
+            // columns.  Only the diagonal block (it == 0) has masked entries
+            // (query < key); it takes its own copy of the loop, so the other
+            // blocks pay nothing for the mask.
             uint32_t pk[32];
             {
                 uint32_t r[2][32];
                 tmem_ld32(ts + cbase, r[0]);
                 tmem_ld32(ts + cbase + 32, r[1]);
                 tmem_wait_ld();
+                auto exp_block = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 l4 = l2[c * 8 + e4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        float p[4];
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 l4 = l2[c * 8 + e4];
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            float p[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int qi = c * 32 + e4 * 4 + i;
-                            const float x = fmaf(__uint_as_float(r[c][e4 * 4 + i]), scale_log2, -lv[i]);
-                            // one in four on the FMA pipe, the rest on the SFU
-                            p[i] = (diag && q0 + qi < key) ? 0.f : (i == 3 ? exp2_poly(x) : ex2(x));
+                            for (int i = 0; i < 4; ++i) {
+                                p[i] = ex2(fmaf(__uint_as_float(r[c][e4 * 4 + i]), scale_log2, -lv[i]));
+                                if constexpr (decltype(masked)::value) {
+                                    if (cbase + c * 32 + e4 * 4 + i < row) p[i] = 0.f;
+                                }
+                            }
+                            pk[c * 16 + e4 * 2] = pack_bf16x2(p[0], p[1]);
+                            pk[c * 16 + e4 * 2 + 1] = pack_bf16x2(p[2], p[3]);
                         }
-                        pk[c * 16 + e4 * 2] = pack_bf16x2(p[0], p[1]);
-                        pk[c * 16 + e4 * 2 + 1] = pack_bf16x2(p[2], p[3]);
                     }
-                }
+                };
+                if (it == 0)
+                    exp_block(std::true_type{});
+                else
+                    exp_block(std::false_type{});
             }
             tmem_st16(ts + cbase, pk);
             tmem_st16(ts + cbase + 16, pk + 16);

@@ -36,7 +36,7 @@
 #pragma once
 
 #include "nc_common.cuh"
-#include "nc_exp2.cuh"
+#include <type_traits>
 #include "nc_normrope_bwd.cuh"
 
 namespace nc {
@@ -320,28 +320,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait_warp(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ts = tmem + lane_base + tm_s(j & 1) + cbase;
-            const bool diag = (j == qt);  // only the diagonal tile has masked entries
-            const int k0 = cbase;        // key column offset inside the tile
+            // P = exp2(S scale log2e - lse2) as bf16 pairs.  Only the diagonal
+            // tile (j == qt) has masked entries (key > query); it takes its own
+            // copy of the loop, so the other tiles pay nothing for the mask.
             uint32_t pk[32];
             {
                 uint32_t r[2][32];
                 tmem_ld32(ts, r[0]);
                 tmem_ld32(ts + 32, r[1]);
                 tmem_wait_ld();
+                auto exp_tile = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int kc = k0 + c * 32 + e;
-                        float p0 = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2_row));
-                        const float x1 = fmaf(__uint_as_float(r[c][e + 1]), scale_log2, -lse2_row);
-                        float p1 = (e & 2) ? exp2_poly(x1) : ex2(x1);  // one in four on the FMA pipe
-                        if (diag) {
-                            if (kc > row) p0 = 0.f;
-                            if (kc + 1 > row) p1 = 0.f;
+                        for (int e = 0; e < 32; e += 2) {
+                            float p0 = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2_row));
+                            float p1 = ex2(fmaf(__uint_as_float(r[c][e + 1]), scale_log2, -lse2_row));
+                            if constexpr (decltype(masked)::value) {
+                                const int kc = cbase + c * 32 + e;  // key column inside the tile
+                                if (kc > row) p0 = 0.f;
+                                if (kc + 1 > row) p1 = 0.f;
+                            }
+                            pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                         }
-                        pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
-                    }
+                };
+                if (j == qt)
+                    exp_tile(std::true_type{});
+                else
+                    exp_tile(std::false_type{});
             }
             if (!mbar_wait_warp(bar(DP_FULL), j & 1, 0x322)) { ok = false; break; }
             tc_fence_after();
