@@ -73,8 +73,6 @@ int device_ready() {
     optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<128>), nc::bwd::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<64>), nc::bwdq::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<128>), nc::bwdq::Smem<128>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<64>), nc::dec::MAX_SMEM);
-    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_kernel<128>), nc::dec::MAX_SMEM);
     if (r != cudaSuccess) {
         t_last_cuda_error = static_cast<int>(r);
         state[dev] = NC_ELAUNCH;
@@ -319,7 +317,7 @@ struct DecodeWs {
 };
 
 size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base) {
-    const int nit = (Tcap + nc::dec::ITEM - 1) / nc::dec::ITEM;  // partial results per stream, at most
+    const int nit = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;  // partial results per stream, at most
     const size_t o_bytes = up256(static_cast<size_t>(B) * nit * H * D * 4);
     const size_t ml_bytes = up256(static_cast<size_t>(B) * nit * H * 2 * 4);
     const size_t c_bytes = up256(static_cast<size_t>(B) * 4);
@@ -344,21 +342,16 @@ template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
                 cudaStream_t s) {
-    using Sh = nc::dec::Shape<D>;
-    const int nit = (Tcap + nc::dec::ITEM - 1) / nc::dec::ITEM;
-    const int xt = Sh::xthreads(H), ks = Sh::slices(H);
-    const int sps = Sh::sps(H) < ks * nc::dec::MAX_SPT ? Sh::sps(H) : ks * nc::dec::MAX_SPT;
-    const nc::dec::Layout ly = nc::dec::layout(H, D, sps, xt, ks);
-    if (ly.bytes > nc::dec::MAX_SMEM) return NC_EINVAL;
-    // persistent: one CTA per SM, each with an equal share of the items
-    const int grid = sm_count();
+    const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
+    const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
+    const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
     const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
     ProfScope ps("attn_decode", s);
-    nc::dec::attn_decode_kernel<D><<<grid, xt * ks + 32, ly.bytes, s>>>(
+    nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, B, H, Tcap, nit, sps, eps, std::log2(double(base)), float(scale_log2));
+        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, std::log2(double(base)), float(scale_log2));
     return launch_status();
 }
 
@@ -523,8 +516,7 @@ int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new,
         (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (reinterpret_cast<uintptr_t>(lens) & 3u))
         return NC_EINVAL;
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D)) return NC_EINVAL;
-    const int ks = D == 64 ? nc::dec::Shape<64>::slices(H) : nc::dec::Shape<128>::slices(H);
-    if (ks == 0) return NC_EINVAL;  // H*D/8 > 512: too many heads for one CTA per chunk
+    if (H * (D / 8) > 512) return NC_EINVAL;  // at most 512 / (D/8) heads
     int rc = device_ready();
     if (rc) return rc;
     DecodeWs ws;
@@ -592,8 +584,7 @@ int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16
         return NC_EINVAL;
     if (nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D) > NC_DECODE_NOALLOC_SCRATCH_BYTES)
         return NC_ETOOLARGE;
-    const int ks = D == 64 ? nc::dec::Shape<64>::slices(H) : nc::dec::Shape<128>::slices(H);
-    if (ks == 0) return NC_EINVAL;
+    if (H * (D / 8) > 512) return NC_EINVAL;  // at most 512 / (D/8) heads
     int rc = device_ready();
     if (rc) return rc;
     void* scratch = nullptr;
