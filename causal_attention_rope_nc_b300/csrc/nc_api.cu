@@ -330,14 +330,6 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
     return c_bytes + ml_bytes + o_bytes;
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                   cudaSuccess)
-        return 148;
-    return n > 0 ? n : 148;
-}
-
 template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
@@ -346,12 +338,14 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
     const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
     const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
     const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
+    nc::dec::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
+    for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
     ProfScope ps("attn_decode", s);
     nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, std::log2(double(base)), float(scale_log2));
+        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2));
     return launch_status();
 }
 

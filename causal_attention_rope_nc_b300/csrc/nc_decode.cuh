@@ -13,8 +13,9 @@
 // Inside a CTA warp w takes heads w, w + NW, ...  For one head it walks the
 // chunk's slots BATCH at a time: a group of D/8 lanes reads one slot's key
 // row (fp16) and value row (bf16) as 16-byte pieces, 32/(D/8) slots per warp
-// load, every load of a batch issued before any arithmetic (streaming
-// loads, evict-first), so each lane keeps 2 * BATCH / (32/(D/8)) loads in
+// load (streaming loads, evict-first).  The batches are software-pipelined
+// over two register buffers: every load of batch n+1 is issued before the
+// arithmetic of batch n, so each lane keeps 2 * BATCH / (32/(D/8)) loads in
 // flight and the rows come straight from HBM into registers.  Scores are
 // formed in log2 units (qhat carries scale * log2 e); each lane group keeps
 // its part of an online softmax state (m shared by the warp, l and o per
@@ -37,7 +38,7 @@
 namespace nc {
 namespace dec {
 
-constexpr int CH = 64;          // cache slots per CTA (one partial result)
+constexpr int CH = 128;         // cache slots per CTA (one partial result)
 constexpr int PART_SLOTS = 32;  // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / CH) partials
 constexpr int MAX_WARPS = 16;   // warps per CTA (heads beyond this many loop)
 constexpr int BATCH = 8;        // slots per warp batch
@@ -51,6 +52,12 @@ struct Lanes {
     static_assert(NLD >= 1 && BATCH % SPW == 0, "batch shape");
 };
 
+// RoPE frequencies theta_i = base^(-2i/D), i < D/2, formed on the host in
+// double precision and passed by value.
+struct Theta {
+    double t[64];
+};
+
 // 16-byte streaming load (read once: evict first).  A regular coherent global
 // load, so a slot written earlier by the same warp is seen after __syncwarp.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
@@ -58,12 +65,12 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) { return __ldcs(rein
 // Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
 // counters [B] u32 (zero between calls).
 template <int D>
-__global__ void __launch_bounds__(MAX_WARPS * 32, 2) attn_decode_kernel(
+__global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
-    unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps, double log2_base,
-    float scale_log2) {
+    unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
+    const __grid_constant__ Theta theta, float scale_log2) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
     __shared__ float2 s_cs[D / 2];  // rotation at the new token's position
@@ -81,13 +88,13 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 2) attn_decode_kernel(
     const int p_new = L - 1;
     const bool own_new = (k_new != nullptr) && (c == nch - 1);
     const int s0 = c * CH, s1 = min(L, s0 + CH);
-    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, rope_theta(i, D, log2_base));
-    __syncthreads();
-
     const int g = lane / LPS;    // slot of this lane group within a warp load
     const int sub = lane % LPS;  // 16-byte piece of the row
     const int e0 = sub * 8;      // first head-dim element of this lane
     const long long slot_elems = static_cast<long long>(H) * D;
+    auto head_base = [&](int h) -> long long {
+        return static_cast<long long>(b) * Tcap * slot_elems + static_cast<long long>(h) * D + e0;
+    };
 
     // RoPE(RMSNorm(x)) of row x (D bf16) at the new token's position: the 8
     // elements [e0, e0 + 8) of this lane (every lane group computes the row).
@@ -113,13 +120,35 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 2) attn_decode_kernel(
         }
     };
 
+    auto load_batch = [&](long long base, int j, uint4 (&kr)[NLD], uint4 (&vr)[NLD]) {
+#pragma unroll
+        for (int u = 0; u < NLD; ++u) {
+            const int s = j + g + SPW * u;
+            if (s < s1) {
+                const long long at = base + static_cast<long long>(s) * slot_elems;
+                kr[u] = ld_stream16(kcache + at);
+                vr[u] = ld_stream16(vcache + at);
+            } else {
+                kr[u] = make_uint4(0u, 0u, 0u, 0u);
+                vr[u] = kr[u];
+            }
+        }
+    };
+    // The first batch of this warp's first head goes out before anything
+    // else: its loads do not depend on qhat.  (When k_new is given, the
+    // chunk that holds the new slot waits for the slot's store below.)
+    uint4 ka[NLD], va[NLD], kb[NLD], vb[NLD];
+    if (!own_new && warp < H) load_batch(head_base(warp), s0, ka, va);
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
+    __syncthreads();
+
     for (int h = warp; h < H; h += NW) {
         const long long row_bh = (static_cast<long long>(b) * H + h) * D;
         float qv[8];
         norm_rope8(q + row_bh, qv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale_log2;
-        const long long base = static_cast<long long>(b) * Tcap * slot_elems + static_cast<long long>(h) * D + e0;
+        const long long base = head_base(h);
         if (own_new) {
             float kv[8];
             norm_rope8(k_new + row_bh, kv);
@@ -130,23 +159,11 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 2) attn_decode_kernel(
             }
             __syncwarp();  // orders the slot's stores before the warp's loads below
         }
+        if (own_new || h != warp) load_batch(base, s0, ka, va);
         float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int j = s0; j < s1; j += BATCH) {
-            uint4 kr[NLD], vr[NLD];
-#pragma unroll
-            for (int u = 0; u < NLD; ++u) {
-                const int s = j + g + SPW * u;
-                if (s < s1) {
-                    const long long at = base + static_cast<long long>(s) * slot_elems;
-                    kr[u] = ld_stream16(kcache + at);
-                    vr[u] = ld_stream16(vcache + at);
-                } else {
-                    kr[u] = make_uint4(0u, 0u, 0u, 0u);
-                    vr[u] = kr[u];
-                }
-            }
+        auto math_batch = [&](int j, const uint4 (&kr)[NLD], const uint4 (&vr)[NLD]) {
             float sc[NLD];
 #pragma unroll
             for (int u = 0; u < NLD; ++u) {
@@ -185,6 +202,15 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 2) attn_decode_kernel(
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[e] = fmaf(pe, vf[e], acc[e]);
             }
+        };
+        // software pipeline over two register buffers: the loads of the next
+        // batch are in flight while the current one is reduced
+        for (int j = s0; j < s1; j += 2 * BATCH) {
+            if (j + BATCH < s1) load_batch(base, j + BATCH, kb, vb);
+            math_batch(j, ka, va);
+            if (j + BATCH >= s1) break;
+            if (j + 2 * BATCH < s1) load_batch(base, j + 2 * BATCH, ka, va);
+            math_batch(j + BATCH, kb, vb);
         }
         // add the lane groups' parts (same m)
 #pragma unroll
