@@ -17,8 +17,10 @@
 // dP (128 columns) and the dQ accumulator (D columns).
 //
 // Issue order (one thread's MMAs execute in issue order):
-//   S_0, S_1, dP_0 | [dS_j in TMEM] dQ(j), dP_{j+1}, S_{j+2} | ...
-// so the softmax warps compute P_{j+1} while dQ(j) and dP_{j+1} run.  K tiles
+//   S_0, S_1, dP_0 | [dP_j in registers] dP_{j+1} | [dS_j in TMEM] dQ(j), S_{j+2} | ...
+// dS_j is written over S_j, not over dP_j, so the next dP may start as soon
+// as the softmax warps have loaded dP_j: it runs while they form dS_j, and
+// dQ(j) and S_{j+2} run while they form P_{j+1}.  K tiles
 // sit in a 3-stage ring (tile j is read by S_j and by dQ(j) two steps later),
 // V tiles in a 2-stage ring.
 //
@@ -62,7 +64,8 @@ enum Bar {
     DQ_FULL = 15,
     MMA_DONE = 16,
     EPI_FULL = 17,  // raw q tile and RoPE table tile staged for the dq epilogue
-    NUM_BARS = 18
+    DP_READ = 18,   // the softmax warps hold dP_j in registers: dP_{j+1} may start
+    NUM_BARS = 19
 };
 
 template <int D>
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(bar(DP_FULL), 1);
         mbar_init(bar(DS_FULL), 8);   // one arrival per softmax warp
+        mbar_init(bar(DP_READ), 8);
         mbar_init(bar(DQ_FULL), 1);
         mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
@@ -255,6 +259,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             for (int j = 0; ok && j < n_kv; ++j) {
+                // dP_{j+1} as soon as the softmax warps hold dP_j
+                if (j + 1 < n_kv) {
+                    if (!mbar_wait(bar(DP_READ), j & 1, 0x225) || !wait_v(j + 1)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_dp(j + 1);
+                }
                 // dQ += dS_j khat_j, dS_j from TMEM
                 if (!mbar_wait(bar(DS_FULL), j & 1, 0x223)) { ok = false; break; }
                 tc_fence_after();
@@ -266,11 +276,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                sdesc_sw128(k_s + kk * (16 * 128), BN * 128, 1024), IDESC_DQ,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(bar(K_EMPTY + j % KSTAGES));
-                }
-                if (j + 1 < n_kv) {
-                    if (!wait_v(j + 1)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_dp(j + 1);
                 }
                 if (j + 2 < n_kv) {
                     if (!wait_k(j + 2)) { ok = false; break; }
@@ -316,14 +321,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         named_bar_sync(1, 256);
         const float alpha = ds_scale_for(fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3])) * 1.0625f);
+        // P feeds only dS here (no product reads it), so it stays in fp32
+        // registers, and alpha (a power of two) rides in the exponent:
+        // alpha P = exp2(S scale log2e - (lse2 - log2 alpha)).
+        const float lse2a = lse2_row - static_cast<float>(ilogbf(alpha));
         for (int j = 0; ok && j < n_kv; ++j) {
             if (!mbar_wait_warp(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ts = tmem + lane_base + tm_s(j & 1) + cbase;
-            // P = exp2(S scale log2e - lse2) as bf16 pairs.  Only the diagonal
-            // tile (j == qt) has masked entries (key > query); it takes its own
-            // copy of the loop, so the other tiles pay nothing for the mask.
-            uint32_t pk[32];
+            // alpha P over this half's 64 keys.  Only the diagonal tile (j == qt)
+            // has masked entries (key > query); it takes its own copy of the
+            // loop, so the other tiles pay nothing for the mask.
+            float pa[64];
             {
                 uint32_t r[2][32];
                 tmem_ld32(ts, r[0]);
@@ -333,15 +342,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float p0 = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2_row));
-                            float p1 = ex2(fmaf(__uint_as_float(r[c][e + 1]), scale_log2, -lse2_row));
+                        for (int e = 0; e < 32; ++e) {
+                            float p = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2a));
                             if constexpr (decltype(masked)::value) {
-                                const int kc = cbase + c * 32 + e;  // key column inside the tile
-                                if (kc > row) p0 = 0.f;
-                                if (kc + 1 > row) p1 = 0.f;
+                                if (cbase + c * 32 + e > row) p = 0.f;  // key column inside the tile
                             }
-                            pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+                            pa[c * 32 + e] = p;
                         }
                 };
                 if (j == qt)
@@ -356,15 +362,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld32(tmem + lane_base + TM_DP + cbase, r[0]);
                 tmem_ld32(tmem + lane_base + TM_DP + cbase + 32, r[1]);
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive_warp(bar(DP_READ));  // dP_j is in registers: the next dP may overwrite it
+                // alpha dS = (alpha P) o (dP - delta) as fp16 pairs
                 uint32_t w[32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const uint32_t pw = pk[c * 16 + e / 2];
-                        const float d0 = alpha * __uint_as_float(pw << 16) * (__uint_as_float(r[c][e]) - delta_row);
-                        const float d1 =
-                            alpha * __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(r[c][e + 1]) - delta_row);
+                        const float d0 = pa[c * 32 + e] * (__uint_as_float(r[c][e]) - delta_row);
+                        const float d1 = pa[c * 32 + e + 1] * (__uint_as_float(r[c][e + 1]) - delta_row);
                         w[c * 16 + e / 2] = pack_f16x2(d0, d1);
                     }
                 // dS over this half's own S columns (already read)
