@@ -233,9 +233,9 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     if (rc) return rc;
     rc = launch_norm_rope<D>(q, k, tab, qhat, khat, rstd, B, T, H, eps, s);
     if (rc) return rc;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::fwd::BN, kF16) ||
-        make_tmap(&tv, v, B, T, H, D, nc::fwd::BN))
+        make_tmap(&tv, v, B, T, H, D, nc::fwd::BN) || make_tmap(&to, out, B, T, H, D, nc::fwd::BM))
         return NC_EINVAL;
     const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
     const double scale = 1.0 / std::sqrt(double(D));
@@ -247,7 +247,7 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
     ProfScope ps("attn_fwd", s);
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
-        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
+        tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
         float(mfix * log2e), float(mfix));
     return launch_status();

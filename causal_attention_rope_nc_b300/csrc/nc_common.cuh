@@ -361,6 +361,45 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Byte offset of the 8 16-bit values at columns [col, col + 8) of row `row`
+// in a [128][D] tile kept as D/64 boxes of 128 rows x 128 bytes with 128-byte
+// swizzling: the shared-memory layout of a TMA box of 64 values x 128 rows.
+__device__ __forceinline__ uint32_t tile16_off(int row, int col) {
+    return static_cast<uint32_t>((col >> 6) * (128 * 128)) + sw128_offset(row, (col & 63) >> 3);
+}
+
+// N consecutive TMEM columns of this warp's 32 lanes (thread i: lane base + i).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t tm, uint32_t (&r)[N]) {
+    static_assert(N % 16 == 0, "column count");
+    if constexpr (N % 32 == 0) {
+#pragma unroll
+        for (int i = 0; i < N / 32; ++i) tmem_ld32(tm + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * i));
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 16; ++i) tmem_ld16(tm + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
+    }
+}
+
+// bf16(s * acc) for row `row`, columns [c0, c0 + NCOL) of a TMEM fp32
+// accumulator (tm = the accumulator's first column, this warp's lanes), into
+// a staging tile in the layout of tile16_off.
+template <int NCOL>
+__device__ __forceinline__ void stage_acc_bf16(uint32_t tm, float s, uint8_t* stage, int row, int c0) {
+    uint32_t r[NCOL];
+    tmem_ld_cols<NCOL>(tm + c0, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int g = 0; g < NCOL / 8; ++g) {
+        const uint32_t* v = r + 8 * g;
+        *reinterpret_cast<uint4*>(stage + tile16_off(row, c0 + 8 * g)) = make_uint4(
+            pack_bf16x2(__uint_as_float(v[0]) * s, __uint_as_float(v[1]) * s),
+            pack_bf16x2(__uint_as_float(v[2]) * s, __uint_as_float(v[3]) * s),
+            pack_bf16x2(__uint_as_float(v[4]) * s, __uint_as_float(v[5]) * s),
+            pack_bf16x2(__uint_as_float(v[6]) * s, __uint_as_float(v[7]) * s));
+    }
+}
+
 // Dynamic shared memory rounded up to a 1024-byte boundary (128-byte swizzled
 // tiles need it).  Returns nullptr when the rounding would leave fewer than
 // `need` of the `alloc` bytes the launch provided.

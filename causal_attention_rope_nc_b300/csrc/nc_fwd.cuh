@@ -81,7 +81,7 @@ __host__ __device__ constexpr uint32_t tm_o(int t) {
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
                     float* __restrict__ lse, int T, int H, int B, int n_qt, int group, float scale_log2,
                     float mfix_log2, float mfix) {
     using S = Smem<D>;
@@ -282,30 +282,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive_warp(bar(P_FULL + t));
         }
-        if (n_t > 0 && ok && mbar_wait_warp(bar(O_FULL + t), 0, 0x303)) {
+        // ---- epilogue: O / l into the tile's qhat buffer (free: every product
+        // of the tile is done), then TMA stores (rows past T are clipped).
+        // Both barriers are reached by the group's four warps whatever
+        // happened; the AND keeps their branch uniform.
+        const bool epi = named_bar_and(2 + t, 128, n_t > 0 && ok && mbar_wait_warp(bar(O_FULL + t), 0, 0x303));
+        uint8_t* stage = smem + S::OFF_Q + t * S::QBYTES;
+        if (epi) {
             tc_fence_after();
             const float l_sum = l_lo + l_hi;
             const float inv_l = 1.f / l_sum;
-            const bool valid = q_idx < T;
-            if (valid) lse[(static_cast<long long>(b) * H + h) * T + q_idx] = mfix + logf(l_sum);
-            __nv_bfloat16* orow = out + ((static_cast<long long>(b) * T + q_idx) * H + h) * D;
+            if (q_idx < T) lse[(static_cast<long long>(b) * H + h) * T + q_idx] = mfix + logf(l_sum);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ro[32];
-                tmem_ld32(tmem + lane_base + tm_o<D>(t) + c * 32, ro);
-                tmem_wait_ld();
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float f[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(ro[8 * g + i]) * inv_l;
-                        dst[g] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                            pack_bf16x2(f[6], f[7]));
-                    }
-                }
-            }
+            for (int c = 0; c < D / 32; ++c) stage_acc_bf16<32>(tmem + lane_base + tm_o<D>(t), inv_l, stage, row, c * 32);
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(2 + t, 128);
+        if (epi && quarter == 0 && lane == 0) {
+            for (int c = 0; c < NC; ++c)
+                tma_store_4d(&tm_out, smem_u32(stage) + c * (BM * 128), c * 64, h, qt * BM, b);
+            bulk_commit();
+            bulk_wait_read_all();  // the staged tile stays valid until the stores have read it
         }
     }
     tc_fence_before();
