@@ -272,7 +272,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     const long long rows = static_cast<long long>(B) * T * H;
     {
         ProfScope ps("attn_bwd_pre", s);
-        nc::bwd_pre_kernel<D><<<rows_grid(rows, D), 256, 0, s>>>(
+        nc::bwd_pre_kernel<D><<<rows_grid(rows / 4 + 1, D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout), lse, delta,
             lse2, gmax, B, T, H, Tpad);
     }

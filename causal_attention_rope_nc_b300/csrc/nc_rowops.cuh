@@ -140,39 +140,73 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       int B, int T, int H,
                                                       int Tpad) {
     using L = RowLanes<D>;
+    constexpr int RB = 4;  // consecutive positions of one (b, h) per group and iteration
     __shared__ float s_max[2][32];
     const int sub = threadIdx.x % L::LPR;
     const long long groups = blockDim.x / L::LPR;
-    const long long nrows = static_cast<long long>(B) * T * H;
+    const int tb = (T + RB - 1) / RB;  // position blocks per (b, h)
+    const long long nblk = static_cast<long long>(B) * H * tb;
     const long long stride = static_cast<long long>(gridDim.x) * groups;
     const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
     const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
     float mx_do = 0.f, mx_o = 0.f;  // squared norms
-    for (long long base = warp_first, r = first; base < nrows; base += stride, r += stride) {
-        const bool valid = r < nrows;
-        float acc = 0.f, sdo = 0.f, so = 0.f;
-        if (valid) {
+    // every lane of a warp runs the same iterations (the group sums shuffle)
+    for (long long base = warp_first, k = first; base < nblk; base += stride, k += stride) {
+        const bool valid = k < nblk;
+        const long long bh = valid ? k / tb : 0;
+        const int t0 = valid ? static_cast<int>(k % tb) * RB : 0;
+        const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+        // every load of the block first
+        uint4 ua[RB], ug[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            if (valid && t0 + i < T) {
+                const long long r = (static_cast<long long>(b) * T + t0 + i) * H + h;
+                ua[i] = *reinterpret_cast<const uint4*>(out + r * D + sub * 8);
+                ug[i] = *reinterpret_cast<const uint4*>(dout + r * D + sub * 8);
+            } else {
+                ua[i] = make_uint4(0u, 0u, 0u, 0u);
+                ug[i] = ua[i];
+            }
+        }
+        float acc[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
             float a[8], g[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(out + r * D + sub * 8), a);
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(dout + r * D + sub * 8), g);
+            bf16x8_to_f32(ua[i], a);
+            bf16x8_to_f32(ug[i], g);
+            float d = 0.f, sdo = 0.f, so = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                acc = fmaf(a[e], g[e], acc);
+                d = fmaf(a[e], g[e], d);
                 sdo = fmaf(g[e], g[e], sdo);
                 so = fmaf(a[e], a[e], so);
             }
+            acc[i] = group_sum<L::LPR>(d);
+            mx_do = fmaxf(mx_do, group_sum<L::LPR>(sdo));
+            mx_o = fmaxf(mx_o, group_sum<L::LPR>(so));
         }
-        acc = group_sum<L::LPR>(acc);
-        mx_do = fmaxf(mx_do, group_sum<L::LPR>(sdo));
-        mx_o = fmaxf(mx_o, group_sum<L::LPR>(so));
         if (valid && sub == 0) {
-            const int h = static_cast<int>(r % H);
-            const long long bt = r / H;
-            const int t = static_cast<int>(bt % T);
-            const int b = static_cast<int>(bt / T);
-            const long long o = (static_cast<long long>(b) * H + h) * Tpad + t;
-            delta[o] = acc;
-            lse2[o] = lse[(static_cast<long long>(b) * H + h) * T + t] * 1.4426950408889634f;
+            // delta and lse2 live in the workspace: o = bh * Tpad + t0 is a
+            // multiple of 4 (Tpad a multiple of 128), so 16-byte stores are
+            // aligned; lse is the caller's (4-byte aligned only): scalar loads
+            const long long o = bh * Tpad + t0;
+            float l2[RB];
+#pragma unroll
+            for (int i = 0; i < RB; ++i)
+                l2[i] = t0 + i < T ? lse[bh * T + t0 + i] * 1.4426950408889634f : 0.f;
+            if (t0 + RB <= T) {
+                *reinterpret_cast<float4*>(delta + o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(lse2 + o) = make_float4(l2[0], l2[1], l2[2], l2[3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < RB; ++i) {
+                    if (t0 + i < T) {
+                        delta[o + i] = acc[i];
+                        lse2[o + i] = l2[i];
+                    }
+                }
+            }
         }
     }
     // block maximum of the row norms, one atomic per block (non-negative
