@@ -24,6 +24,11 @@
  *  - Decode: generation with a KV cache (ai.flicky.cc, section
  *    "Карта репозитория", engine.py row; 7minutos.es "Andrej Karpathy lanza
  *    nanochat ...", section "Entrenamiento medio, SFT y uso de herramientas").
+ *  - Sliding windows: most layers attend through a short window of a quarter
+ *    of the context (ai.flicky.cc, section "Модель: что изменилось со времён
+ *    GPT-2", window-pattern bullet).  Read here as: with window W > 0, query
+ *    i sees key j exactly when 0 <= i - j < W (W keys, itself included);
+ *    W <= 0 means the plain causal mask.
  *
  * Layout: q, k, v, o, dout, dq, dk, dv are [B, T, H, D] row-major; lse is
  * [B, H, T]; rms factors are [B, T, H].  pos is [T] (NULL means 0..T-1).
@@ -36,6 +41,9 @@
 
 #define ORC_NORM 1
 #define ORC_ROPE 2
+
+/* Is key j visible from query i?  Causal, and inside the window when W > 0. */
+static int visible(int i, int j, int W) { return j <= i && (W <= 0 || i - j < W); }
 
 static size_t at4(int b, int t, int h, int d, int T, int H, int D)
 {
@@ -96,10 +104,10 @@ static double dot(const double *a, const double *b, int n)
     return s;
 }
 
-/* Step 3 for one (b, h): probabilities P[i][j] (j <= i, zero above the
- * diagonal), outputs o and log-sum-exp.  P is T*T, row-major. */
+/* Step 3 for one (b, h): probabilities P[i][j] (zero where j is not
+ * visible from i), outputs o and log-sum-exp.  P is T*T, row-major. */
 static void attend_head(const double *qh, const double *kh, const double *v,
-                        int b, int h, int T, int H, int D, double *P,
+                        int b, int h, int T, int H, int D, int W, double *P,
                         double *o, double *lse)
 {
     double scale = 1.0 / sqrt((double)D);
@@ -107,30 +115,35 @@ static void attend_head(const double *qh, const double *kh, const double *v,
         double *row = P + (size_t)i * T;
         const double *qi = qh + at4(b, i, h, 0, T, H, D);
         double m = -INFINITY;
-        for (int j = 0; j <= i; ++j) {
+        for (int j = 0; j < T; ++j) {
+            if (!visible(i, j, W)) continue;
             row[j] = dot(qi, kh + at4(b, j, h, 0, T, H, D), D) * scale;
             if (row[j] > m) m = row[j];
         }
         double l = 0.0;
-        for (int j = 0; j <= i; ++j) {
+        for (int j = 0; j < T; ++j) {
+            if (!visible(i, j, W)) {
+                row[j] = 0.0;
+                continue;
+            }
             row[j] = exp(row[j] - m);
             l += row[j];
         }
-        for (int j = 0; j <= i; ++j) row[j] /= l;
-        for (int j = i + 1; j < T; ++j) row[j] = 0.0;
+        for (int j = 0; j < T; ++j) row[j] /= l;
         double *oi = o + at4(b, i, h, 0, T, H, D);
         for (int d = 0; d < D; ++d) {
             double acc = 0.0;
-            for (int j = 0; j <= i; ++j) acc += row[j] * v[at4(b, j, h, d, T, H, D)];
+            for (int j = 0; j < T; ++j) acc += row[j] * v[at4(b, j, h, d, T, H, D)];
             oi[d] = acc;
         }
         if (lse) lse[((size_t)b * H + h) * T + i] = m + log(l);
     }
 }
 
-/* Forward: o = softmax(qhat khat^T / sqrt(D) + causal mask) v; lse [B,H,T]. */
+/* Forward: o = softmax(qhat khat^T / sqrt(D) + mask) v; lse [B,H,T].  The
+ * mask is causal, banded to the last W keys when W > 0. */
 int orc_attn_fwd(const double *q, const double *k, const double *v, const int *pos,
-                 int B, int T, int H, int D, double eps, double base, int flags,
+                 int B, int T, int H, int D, double eps, double base, int flags, int W,
                  double *o, double *lse)
 {
     size_t n = (size_t)B * T * H * D;
@@ -144,7 +157,7 @@ int orc_attn_fwd(const double *q, const double *k, const double *v, const int *p
         for (int h = 0; h < H; ++h) {
             double *P = malloc((size_t)T * T * sizeof(double));
             if (!P) { err = -1; continue; }
-            attend_head(qh, kh, v, b, h, T, H, D, P, o, lse);
+            attend_head(qh, kh, v, b, h, T, H, D, W, P, o, lse);
             free(P);
         }
     free(qh);
@@ -172,15 +185,15 @@ static void norm_rope_backward(const double *x, const double *g, int p, int D,
     free(u);
 }
 
-/* Step 4, by hand (no autograd):
- *   dv_j  = sum_{i>=j} P_ij do_i
+/* Step 4, by hand (no autograd), with P zero where j is not visible from i:
+ *   dv_j  = sum_i P_ij do_i
  *   dP_ij = <do_i, v_j>,  Delta_i = <do_i, o_i>
  *   dS_ij = P_ij (dP_ij - Delta_i)
  *   dqhat_i = sum_j dS_ij khat_j / sqrt(D),  dkhat_j = sum_i dS_ij qhat_i / sqrt(D)
  * then back through RoPE and RMSNorm to dq, dk. */
 int orc_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
                  const int *pos, int B, int T, int H, int D, double eps, double base,
-                 int flags, double *dq, double *dk, double *dv)
+                 int flags, int W, double *dq, double *dk, double *dv)
 {
     size_t n = (size_t)B * T * H * D;
     double *qh = malloc(n * sizeof(double)), *kh = malloc(n * sizeof(double));
@@ -200,13 +213,13 @@ int orc_attn_bwd(const double *q, const double *k, const double *v, const double
             double *P = malloc((size_t)T * T * sizeof(double));
             double *dS = malloc((size_t)T * T * sizeof(double));
             if (!P || !dS) { free(P); free(dS); err = -1; continue; }
-            attend_head(qh, kh, v, b, h, T, H, D, P, o, NULL);
+            attend_head(qh, kh, v, b, h, T, H, D, W, P, o, NULL);
             for (int i = 0; i < T; ++i) {
                 const double *doi = dout + at4(b, i, h, 0, T, H, D);
                 double delta = dot(doi, o + at4(b, i, h, 0, T, H, D), D);
                 for (int j = 0; j < T; ++j) {
                     double pij = P[(size_t)i * T + j];
-                    double dpij = (j <= i) ? dot(doi, v + at4(b, j, h, 0, T, H, D), D) : 0.0;
+                    double dpij = visible(i, j, W) ? dot(doi, v + at4(b, j, h, 0, T, H, D), D) : 0.0;
                     dS[(size_t)i * T + j] = pij * (dpij - delta);
                 }
             }
@@ -244,12 +257,13 @@ int orc_attn_bwd(const double *q, const double *k, const double *v, const double
 }
 
 /* Step 5, decode: one new query per stream b at position p = lens[b] - 1,
- * attending over cache slots 0 .. lens[b]-1.  Keys are given RAW: slot j is
+ * attending over the cache slots j <= p visible from p (all of them, or the
+ * last W when W > 0).  Keys are given RAW: slot j is
  * normalised and rotated at position j here, exactly as a prefill over the
  * same raw keys would have stored it; the new token's raw key sits at slot p.
  * q [B,H,D]; k_raw, v [B,Tcap,H,D]; out [B,H,D]. */
 int orc_attn_decode(const double *q, const double *k_raw, const double *v, const int *lens,
-                    int B, int H, int D, int Tcap, double eps, double base, int flags,
+                    int B, int H, int D, int Tcap, double eps, double base, int flags, int W,
                     double *out)
 {
     double scale = 1.0 / sqrt((double)D);
@@ -268,6 +282,8 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
             if (flags & ORC_ROPE) rotate(qh, L - 1, D, base, +1);
             double m = -INFINITY;
             for (int j = 0; j < L; ++j) {
+                s[j] = -INFINITY;
+                if (!visible(L - 1, j, W)) continue;
                 const double *kj = k_raw + at4(b, j, h, 0, Tcap, H, D);
                 double rk = (flags & ORC_NORM) ? rms_of(kj, D, eps) : 1.0;
                 for (int d = 0; d < D; ++d) kh[d] = kj[d] / rk;
@@ -277,7 +293,7 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
             }
             double l = 0.0;
             for (int j = 0; j < L; ++j) {
-                s[j] = exp(s[j] - m);
+                s[j] = exp(s[j] - m);  /* exp(-inf) = 0 for the slots outside the window */
                 l += s[j];
             }
             double *oi = out + ((size_t)b * H + h) * D;
