@@ -24,7 +24,8 @@ NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE = 0, 1, 2, 3
 
 EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
             "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
-            "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc")
+            "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc",
+            "nc_attn_fwd_sw", "nc_attn_bwd_sw", "nc_attn_decode_sw")
 NC_ETOOLARGE = -5
 
 
@@ -68,6 +69,12 @@ def _load():
     L.nc_profile_read.restype = I
     L.nc_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, F, S]
     L.nc_attn_decode_noalloc.restype = I
+    L.nc_attn_fwd_sw.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
+    L.nc_attn_fwd_sw.restype = I
+    L.nc_attn_bwd_sw.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
+    L.nc_attn_bwd_sw.restype = I
+    L.nc_attn_decode_sw.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
+    L.nc_attn_decode_sw.restype = I
     return L
 
 
@@ -138,37 +145,65 @@ def nc_qk_norm_rope(x, pos, xhat, rstd, workspace, eps, rope_base, stream=None):
            "nc_qk_norm_rope")
 
 
-def nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, stream=None):
+def _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace):
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         _bf16(t, n)
     _f16(qhat, "qhat"), _f16(khat, "khat")
     B, T, H, D = q.shape
-    _check(lib.nc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat),
-                           _ptr(khat), _ptr(rstd), _ptr(workspace), workspace.numel(), B, T, H, D,
-                           eps, rope_base, _stream(stream)), "nc_attn_fwd")
+    return (_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat), _ptr(khat), _ptr(rstd),
+            _ptr(workspace), workspace.numel(), B, T, H, D)
 
 
-def nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base,
-                stream=None):
+def nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, stream=None):
+    args = _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace)
+    _check(lib.nc_attn_fwd(*args, eps, rope_base, _stream(stream)), "nc_attn_fwd")
+
+
+def nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, window, stream=None):
+    args = _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace)
+    _check(lib.nc_attn_fwd_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_fwd_sw")
+
+
+def _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace):
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout), ("dq", dq), ("dk", dk),
                  ("dv", dv)):
         _bf16(t, n)
     _f16(qhat, "qhat"), _f16(khat, "khat")
     B, T, H, D = q.shape
-    _check(lib.nc_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat),
-                           _ptr(khat), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                           workspace.numel(), B, T, H, D, eps, rope_base, _stream(stream)),
-           "nc_attn_bwd")
+    return (_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat), _ptr(khat), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, T, H, D)
 
 
-def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, stream=None):
+def nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base,
+                stream=None):
+    args = _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace)
+    _check(lib.nc_attn_bwd(*args, eps, rope_base, _stream(stream)), "nc_attn_bwd")
+
+
+def nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base, window,
+                   stream=None):
+    args = _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace)
+    _check(lib.nc_attn_bwd_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_bwd_sw")
+
+
+def _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace):
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
         _bf16(t, n)
     _f16(kcache, "kcache")
     B, Tcap, H, D = kcache.shape
-    _check(lib.nc_attn_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
-                              _ptr(lens), _ptr(out), _ptr(workspace), workspace.numel(), B, H, D, Tcap,
-                              eps, rope_base, _stream(stream)), "nc_attn_decode")
+    return (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(lens), _ptr(out),
+            _ptr(workspace), workspace.numel(), B, H, D, Tcap)
+
+
+def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, stream=None):
+    args = _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace)
+    _check(lib.nc_attn_decode(*args, eps, rope_base, _stream(stream)), "nc_attn_decode")
+
+
+def nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, window,
+                      stream=None):
+    args = _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace)
+    _check(lib.nc_attn_decode_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_decode_sw")
 
 
 def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
@@ -185,25 +220,31 @@ def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope
 
 # -------------------------------------------------------- allocating helpers --
 
-def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, stream=None):
-    """Returns (out, lse, qhat, khat)."""
+def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, stream=None, window=0):
+    """Returns (out, lse, qhat, khat).  window > 0: sliding-window mask."""
     B, T, H, D = q.shape
     out = torch.empty_like(q)
     qhat = torch.empty_like(q, dtype=torch.float16)
     khat = torch.empty_like(k, dtype=torch.float16)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     ws = workspace if workspace is not None else new_workspace(NC_OP_FWD, B, T, H, D, q.device)
-    nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, stream)
+    if window:
+        nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, window, stream)
+    else:
+        nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, stream)
     return out, lse, qhat, khat
 
 
 def attn_bwd(q, k, v, out, lse, qhat, khat, dout, pos=None, eps=1e-6, rope_base=10000.0,
-             workspace=None, stream=None):
-    """Returns (dq, dk, dv)."""
+             workspace=None, stream=None, window=0):
+    """Returns (dq, dk, dv).  window: as passed to attn_fwd."""
     B, T, H, D = q.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace if workspace is not None else new_workspace(NC_OP_BWD, B, T, H, D, q.device)
-    nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, stream)
+    if window:
+        nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, window, stream)
+    else:
+        nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, stream)
     return dq, dk, dv
 
 
@@ -216,9 +257,12 @@ def qk_norm_rope(x, pos=None, eps=1e-6, rope_base=10000.0, stream=None):
 
 
 def attn_decode(q, kcache, vcache, lens, k_new=None, v_new=None, eps=1e-6, rope_base=10000.0,
-                workspace=None, stream=None):
+                workspace=None, stream=None, window=0):
     B, Tcap, H, D = kcache.shape
     out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
     ws = workspace if workspace is not None else new_workspace(NC_OP_DECODE, B, Tcap, H, D, q.device)
-    nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, stream)
+    if window:
+        nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, window, stream)
+    else:
+        nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, stream)
     return out

@@ -224,9 +224,13 @@ int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_b
     return launch_status();
 }
 
+// Sliding window as the kernels take it: a value no distance reaches when
+// there is none (window <= 0, or at least the sequence length).
+int window_eff(int window, int T) { return (window <= 0 || window >= T) ? (1 << 30) : window; }
+
 template <int D>
 int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
-             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, float eps, float base,
+             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, float eps, float base, int W,
              cudaStream_t s) {
     float2* tab = reinterpret_cast<float2*>(ws);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
@@ -249,14 +253,14 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
-        float(mfix * log2e), float(mfix));
+        float(mfix * log2e), float(mfix), W);
     return launch_status();
 }
 
 template <int D>
 int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
              const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
-             nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, float eps, float base, cudaStream_t s) {
+             nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, float eps, float base, int W, cudaStream_t s) {
     const int Tpad = tpad_of(T);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
     float2* tab = reinterpret_cast<float2*>(w);
@@ -295,7 +299,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS,
                                            nc::bwd::Smem<D>::ALLOC, s>>>(
             tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, T, H, B, Tpad, group,
-            float(scale), float(scale * 1.4426950408889634), eps);
+            float(scale), float(scale * 1.4426950408889634), eps, W);
     }
     if ((rc = launch_status())) return rc;
     {
@@ -305,7 +309,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
                                           nc::bwdq::Smem<D>::ALLOC, s>>>(
             tq, tk, tv, tdo, tqr, ttab, tdq, lse2, delta, gmax, T, H, B, Tpad, group, float(scale),
-            float(scale * 1.4426950408889634), eps);
+            float(scale * 1.4426950408889634), eps, W);
     }
     return launch_status();
 }
@@ -333,7 +337,7 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
 template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
-                cudaStream_t s) {
+                int W, cudaStream_t s) {
     const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
     const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
     const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
@@ -345,7 +349,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2));
+        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2), W);
     return launch_status();
 }
 
@@ -463,7 +467,14 @@ int nc_qk_norm_rope(const nc_bf16* x, const int32_t* pos, nc_bf16* xhat, float* 
 int nc_attn_fwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
                 float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
                 int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream) {
-    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    return nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, workspace_bytes, B, T, H, D, eps,
+                          rope_base, 0, stream);
+}
+
+int nc_attn_fwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
+                   float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
+                   int B, int T, int H, int D, float eps, float rope_base, int window, nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
     if (B == 0 || T == 0 || H == 0) return NC_OK;
     if (!q || !k || !v || !out || !lse || !qhat || !khat || !workspace) return NC_EINVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(qhat) || !aligned16(khat) ||
@@ -473,15 +484,24 @@ int nc_attn_fwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int3
     int rc = device_ready();
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return D == 64 ? fwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, s)
-                   : fwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, s);
+    const int W = window_eff(window, T);
+    return D == 64 ? fwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, W, s)
+                   : fwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, W, s);
 }
 
 int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
                 const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
                 nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
                 float eps, float rope_base, nc_stream_t stream) {
-    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    return nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, workspace_bytes, B, T, H,
+                          D, eps, rope_base, 0, stream);
+}
+
+int nc_attn_bwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
+                   const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+                   nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
+                   float eps, float rope_base, int window, nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
     if (B == 0 || T == 0 || H == 0) return NC_OK;
     if (!q || !k || !v || !out || !lse || !qhat || !khat || !dout || !dq || !dk || !dv || !workspace)
         return NC_EINVAL;
@@ -493,16 +513,24 @@ int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int3
     int rc = device_ready();
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int W = window_eff(window, T);
     return D == 64 ? bwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
-                                  rope_base, s)
+                                  rope_base, W, s)
                    : bwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
-                                   rope_base, s);
+                                   rope_base, W, s);
 }
 
 int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                    const int32_t* lens, nc_bf16* out, void* workspace, size_t workspace_bytes, int B, int H, int D,
                    int Tcap, float eps, float rope_base, nc_stream_t stream) {
-    if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
+    return nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, workspace, workspace_bytes, B, H, D, Tcap,
+                             eps, rope_base, 0, stream);
+}
+
+int nc_attn_decode_sw(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache,
+                      nc_bf16* vcache, const int32_t* lens, nc_bf16* out, void* workspace, size_t workspace_bytes,
+                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream) {
+    if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
     if (B == 0 || H == 0 || Tcap == 0) return NC_OK;
     if (!q || !kcache || !vcache || !lens || !out || !workspace) return NC_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr)) return NC_EINVAL;
@@ -516,8 +544,10 @@ int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new,
     DecodeWs ws;
     decode_ws_layout(B, H, D, Tcap, &ws, workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s)
-                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s);
+    const int W = window_eff(window, Tcap);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W, s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W,
+                                      s);
 }
 
 }  // extern "C"
@@ -590,8 +620,10 @@ int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16
     // must start from zero
     if (cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), s) != cudaSuccess)
         return launch_status();
-    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s)
-                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, s);
+    const int W = window_eff(0, Tcap);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W, s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W,
+                                      s);
 }
 
 }  // extern "C"

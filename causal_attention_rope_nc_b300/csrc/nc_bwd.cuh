@@ -4,7 +4,9 @@
 // atomics: each output element is owned by exactly one CTA.
 //
 // One CTA owns one 128-key tile j of one (batch, head) and walks the
-// 128-query blocks i >= j.  Everything is computed transposed (keys on the
+// 128-query blocks i >= j that can see it (all of them, or with a sliding
+// window W -- query q sees key k when 0 <= q - k < W -- those up to the block
+// of the last query within W of the tile's last key).  Everything is computed transposed (keys on the
 // TMEM lanes):
 //   S^T   = khat_j qhat_i^T                 (M=128 keys, N=128 queries, K=D)
 //   P^T   = exp2(S^T * scale*log2e - lse2_i)  recomputed from the forward's
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                          const float* __restrict__ lse2, const float* __restrict__ delta,
                          unsigned int* __restrict__ gmax, int T, int H, int B, int Tpad, int group, float scale,
-                         float scale_log2, float eps) {
+                         float scale_log2, float eps, int W) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
     constexpr uint32_t TM_DK = TM_DV + D;
@@ -136,7 +138,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int kt = tc.rank;
     const int b = tc.bh / H, h = tc.bh % H;
     const int qb0 = kt;  // BM == BN: the diagonal query block
-    const int n_it = nqb - qb0;
+    const int qb_last = min(nqb - 1, (kt * BN + BN - 1 + W - 1) / BM);  // W >= 2^30 means no window
+    const int n_it = qb_last - qb0 + 1;
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
@@ -334,9 +337,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float4* l2 = reinterpret_cast<const float4*>(smem + S::OFF_L + st * BM * 4 + cbase * 4);
             const float4* dl = reinterpret_cast<const float4*>(smem + S::OFF_DL + st * BM * 4 + cbase * 4);
             // P^T = exp2(S^T scale log2e - lse2) as bf16 pairs over this half's S^T
-            // columns.  Only the diagonal block (it == 0) has masked entries
-            // (query < key); it takes its own copy of the loop, so the other
-            // blocks pay nothing for the mask.
+            // columns.  Blocks with masked entries (the diagonal one: query <
+            // key; at the far end of a window: query - key >= W) take their
+            // own copy of the loop, so the other blocks pay nothing for the mask.
+            const int qb = qb0 + it;
+            const int d0 = (qb - kt) * BM + cbase - row;  // query - key at this thread's first column
             uint32_t pk[32];
             {
                 uint32_t r[2][32];
@@ -355,7 +360,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             for (int i = 0; i < 4; ++i) {
                                 p[i] = ex2(fmaf(__uint_as_float(r[c][e4 * 4 + i]), scale_log2, -lv[i]));
                                 if constexpr (decltype(masked)::value) {
-                                    if (cbase + c * 32 + e4 * 4 + i < row) p[i] = 0.f;
+                                    const int dd = d0 + c * 32 + e4 * 4 + i;  // visible: 0 <= dd < W
+                                    if (dd < 0 || dd >= W) p[i] = 0.f;
                                 }
                             }
                             pk[c * 16 + e4 * 2] = pack_bf16x2(p[0], p[1]);
@@ -363,10 +369,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 };
-                if (it == 0)
-                    exp_block(std::true_type{});
-                else
+                if (qb > kt && (qb - kt) * BM + BM - 1 < W)
                     exp_block(std::false_type{});
+                else
+                    exp_block(std::true_type{});
             }
             tmem_st16(ts + cbase, pk);
             tmem_st16(ts + cbase + 16, pk + 16);

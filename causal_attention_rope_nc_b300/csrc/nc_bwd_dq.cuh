@@ -3,7 +3,10 @@
 // fused into the epilogue, so dq leaves the kernel finished (bf16).
 //
 // One CTA owns one 128-query tile i of one (batch, head) and walks the key
-// tiles j <= i, recomputing what it needs from the forward's lse:
+// tiles j <= i that it can see (all of them, or with a sliding window W --
+// query q sees key k when 0 <= q - k < W -- those from the tile of the first
+// query's oldest visible key), recomputing what it needs from the forward's
+// lse:
 //   S_j   = qhat_i khat_j^T                 (M=128 queries, N=128 keys, K=D)
 //   P_j   = exp2(S_j * scale*log2e - lse2_i)
 //   dP_j  = dout_i v_j^T                    (M=128 queries, N=128 keys, K=D)
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
                        const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
                        const float* __restrict__ delta, const unsigned int* __restrict__ gmax, int T, int H, int B,
-                       int Tpad, int group, float scale, float scale_log2, float eps) {
+                       int Tpad, int group, float scale, float scale_log2, float eps, int W) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
     extern __shared__ uint8_t smem_raw[];
@@ -120,7 +123,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_qt, group);
     const int qt = n_qt - 1 - tc.rank;
     const int b = tc.bh / H, h = tc.bh % H;
-    const int n_kv = qt + 1;  // BM == BN: key tiles 0..qt
+    const int kt_lo = max(0, qt * BM - W + 1) / BN;  // first visible key tile (W >= 2^30: none cut)
+    const int n_kv = qt - kt_lo + 1;                  // BM == BN: key tiles kt_lo..qt
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
@@ -171,13 +175,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (j >= KSTAGES && !mbar_wait(bar(K_EMPTY + ks), (j / KSTAGES - 1) & 1, 0x121)) break;
                 mbar_expect_tx(bar(K_FULL + ks), S::TBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + ks * S::TBYTES + c * (BN * 128), &tm_k, c * 64, h, j * BN, b,
+                    tma_load_4d(sb + S::OFF_K + ks * S::TBYTES + c * (BN * 128), &tm_k, c * 64, h, (kt_lo + j) * BN, b,
                                 bar(K_FULL + ks));
                 ++issued_k[ks];
                 if (j >= 2 && !mbar_wait(bar(V_EMPTY + vs), ((j >> 1) - 1) & 1, 0x122)) break;
                 mbar_expect_tx(bar(V_FULL + vs), S::TBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + vs * S::TBYTES + c * (BN * 128), &tm_v, c * 64, h, j * BN, b,
+                    tma_load_4d(sb + S::OFF_V + vs * S::TBYTES + c * (BN * 128), &tm_v, c * 64, h, (kt_lo + j) * BN, b,
                                 bar(V_FULL + vs));
                 ++issued_v[vs];
             }
@@ -329,15 +333,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait_warp(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ts = tmem + lane_base + tm_s(j & 1) + cbase;
-            // alpha P over this half's 64 keys.  Only the diagonal tile (j == qt)
-            // has masked entries (key > query); it takes its own copy of the
-            // loop, so the other tiles pay nothing for the mask.
+            // alpha P over this half's 64 keys.  Tiles with masked entries (the
+            // diagonal one: key > query; at the far end of a window: query - key
+            // >= W) take their own copy of the loop, so the other tiles pay
+            // nothing for the mask.
             float pa[64];
             {
                 uint32_t r[2][32];
                 tmem_ld32(ts, r[0]);
                 tmem_ld32(ts + 32, r[1]);
                 tmem_wait_ld();
+                const int kt = kt_lo + j;                     // key tile
+                const int d0 = (qt - kt) * BN + row - cbase;  // query - key at this thread's first column
                 auto exp_tile = [&](auto masked) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
@@ -345,15 +352,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int e = 0; e < 32; ++e) {
                             float p = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2a));
                             if constexpr (decltype(masked)::value) {
-                                if (cbase + c * 32 + e > row) p = 0.f;  // key column inside the tile
+                                const int dd = d0 - (c * 32 + e);  // visible: 0 <= dd < W
+                                if (dd < 0 || dd >= W) p = 0.f;
                             }
                             pa[c * 32 + e] = p;
                         }
                 };
-                if (j == qt)
-                    exp_tile(std::true_type{});
-                else
+                if (kt < qt && (qt - kt) * BM + BM - 1 < W)
                     exp_tile(std::false_type{});
+                else
+                    exp_tile(std::true_type{});
             }
             if (!mbar_wait_warp(bar(DP_FULL), j & 1, 0x322)) { ok = false; break; }
             tc_fence_after();

@@ -26,6 +26,10 @@
 // to finish (per-stream arrival counter) merges the chunks in chunk order
 // (deterministic) and resets the counter for the next call.
 //
+// With a sliding window W only the last W slots are attended (slot j is
+// visible when 0 <= p - j < W); chunks wholly before them exit at once and
+// take no part in the merge.
+//
 // The new token (position p = lens[b] - 1): the CTA that owns the last chunk
 // normalises and rotates k_new, writes it (fp16) and v_new into slot p, and
 // reads them back through the cache like every other slot, so the score at p
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
     unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
-    const __grid_constant__ Theta theta, float scale_log2) {
+    const __grid_constant__ Theta theta, float scale_log2, int W) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
     __shared__ float2 s_cs[D / 2];  // rotation at the new token's position
@@ -82,12 +86,15 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         return;
     }
     const int nch = (L + CH - 1) / CH;
-    if (c >= nch) return;  // uniform over the CTA
+    const int s_vis = max(0, L - W);  // first visible slot (W >= 2^30: slot 0)
+    const int c_lo = s_vis / CH;      // first chunk holding a visible slot
+    if (c >= nch || c < c_lo) return;  // uniform over the CTA
+    const int n_parts = nch - c_lo;    // chunks that produce a partial
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NW = static_cast<int>(blockDim.x >> 5);
     const int p_new = L - 1;
     const bool own_new = (k_new != nullptr) && (c == nch - 1);
-    const int s0 = c * CH, s1 = min(L, s0 + CH);
+    const int s0 = max(c * CH, s_vis), s1 = min(L, c * CH + CH);
     const int g = lane / LPS;    // slot of this lane group within a warp load
     const int sub = lane % LPS;  // 16-byte piece of the row
     const int e0 = sub * 8;      // first head-dim element of this lane
@@ -220,7 +227,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
         }
         if (g == 0) {
-            if (nch == 1) {
+            if (n_parts == 1) {
                 float o[8];
                 const float inv = 1.f / l;
 #pragma unroll
@@ -235,12 +242,12 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             }
         }
     }
-    if (nch == 1) return;  // uniform
+    if (n_parts == 1) return;  // uniform
 
     // ---- the last chunk of the stream to finish merges every chunk ----
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&counters[b], 1u) == static_cast<unsigned>(nch - 1);
+    if (threadIdx.x == 0) s_last = atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
     __syncthreads();
     if (!s_last) return;  // uniform
     __threadfence();
@@ -250,11 +257,11 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         const float* pmb = part_ml + (static_cast<long long>(b) * max_parts * H + h) * 2;
         const float* pob = part_o + (static_cast<long long>(b) * max_parts * H + h) * D + lane * EPL;
         float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pmb + static_cast<long long>(cc) * H * 2));
+        for (int cc = c_lo; cc < nch; ++cc) M = fmaxf(M, __ldcg(pmb + static_cast<long long>(cc) * H * 2));
         float Ls = 0.f, o[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
+        for (int cc = c_lo; cc < nch; ++cc) {
             const float2 ml = __ldcg(reinterpret_cast<const float2*>(pmb + static_cast<long long>(cc) * H * 2));
             const float w = ex2(ml.x - M);
             Ls = fmaf(ml.y, w, Ls);

@@ -1,7 +1,10 @@
 // Causal attention forward on sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // One CTA computes two consecutive 128-row query tiles (2p and 2p+1) of one
-// (batch, head); both share every K/V tile it streams:
+// (batch, head); both share every K/V tile it streams.  With a sliding window
+// W (query i sees key j when 0 <= i - j < W) the stream starts at the first
+// key tile either query tile can see, and tile 2p+1 may start one K/V tile
+// later than tile 2p:
 //   warp 8      TMA producer: both Q tiles once, then K_j / V_j in 2-stage rings
 //   warp 9      MMA issuer (one thread)
 //   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: thread r owns
@@ -83,7 +86,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
                     float* __restrict__ lse, int T, int H, int B, int n_qt, int group, float scale_log2,
-                    float mfix_log2, float mfix) {
+                    float mfix_log2, float mfix, int W) {
     using S = Smem<D>;
     constexpr int NC = D / 64;  // 64-column (128-byte) swizzle spans per row
     extern __shared__ uint8_t smem_raw[];
@@ -100,9 +103,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int qt0 = 2 * (n_pairs - 1 - tc.rank);
     const int b = tc.bh / H, h = tc.bh % H;
     const bool has1 = qt0 + 1 < n_qt;
-    const int n0 = qt0 + 1;             // key tiles of query tile qt0
-    const int n1 = has1 ? qt0 + 2 : 0;  // key tiles of query tile qt0 + 1
-    const int n_kv = has1 ? n1 : n0;
+    // first key tile a query tile sees (W >= 2^30 means no window)
+    auto first_kt = [&](int qt) { return max(0, qt * BM - W + 1) / BN; };
+    const int lo0 = first_kt(qt0), lo1 = has1 ? first_kt(qt0 + 1) : lo0;
+    const int f1 = lo1 - lo0;                 // stream index of tile qt0+1's first key tile (0 or 1)
+    const int n0 = qt0 - lo0 + 1;             // key tiles of query tile qt0
+    const int n1 = has1 ? qt0 + 2 - lo1 : 0;  // key tiles of query tile qt0 + 1
+    const int n_kv = has1 ? qt0 + 2 - lo0 : n0;
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
 
@@ -143,13 +150,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (j >= 2 && !mbar_wait(bar(K_EMPTY + st), (use - 1) & 1, 0x101)) break;
                 mbar_expect_tx(bar(K_FULL + st), S::KBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + st * S::KBYTES + c * (BN * 128), &tm_k, c * 64, h, j * BN, b,
+                    tma_load_4d(sb + S::OFF_K + st * S::KBYTES + c * (BN * 128), &tm_k, c * 64, h, (lo0 + j) * BN, b,
                                 bar(K_FULL + st));
                 ++issued_k[st];
                 if (j >= 2 && !mbar_wait(bar(V_EMPTY + st), (use - 1) & 1, 0x102)) break;
                 mbar_expect_tx(bar(V_FULL + st), S::KBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + st * S::KBYTES + c * (BN * 128), &tm_v, c * 64, h, j * BN, b,
+                    tma_load_4d(sb + S::OFF_V + st * S::KBYTES + c * (BN * 128), &tm_v, c * 64, h, (lo0 + j) * BN, b,
                                 bar(V_FULL + st));
                 ++issued_v[st];
             }
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
-                if (has1) issue_s(1, 0);
+                if (has1 && f1 == 0) issue_s(1, 0);
                 mma_commit(bar(K_EMPTY + 0));
             }
             for (int j = 0; ok && j < n_kv; ++j) {
@@ -207,11 +214,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         issue_s(0, st ^ 1);
                     }
                 }
-                if (has1) {
-                    if (!mbar_wait(bar(P_FULL + 1), j & 1, 0x206)) { ok = false; break; }
+                if (has1 && j >= f1) {
+                    if (!mbar_wait(bar(P_FULL + 1), (j - f1) & 1, 0x206)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(1, st, j == 0);
-                    if (j == n1 - 1) mma_commit(bar(O_FULL + 1));
+                    issue_pv(1, st, j == f1);
+                    if (j == n_kv - 1) mma_commit(bar(O_FULL + 1));
                 }
                 mma_commit(bar(V_EMPTY + st));
                 if (has1 && nxt) {
@@ -247,6 +254,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t r[2][32];
             tmem_ld32(ts, r[0]);
             tmem_wait_ld();
+            const int kt = (t ? lo1 : lo0) + j;     // key tile
+            const int d0 = (qt - kt) * BM + row;    // query - key at column 0 of the tile
             auto exp_tile = [&](auto masked) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
@@ -259,8 +268,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float p0 = ex2(fmaf(__uint_as_float(rc[e]), scale_log2, -mfix_log2));
                         float p1 = ex2(fmaf(__uint_as_float(rc[e + 1]), scale_log2, -mfix_log2));
                         if constexpr (decltype(masked)::value) {
-                            if (c * 32 + e > row) p0 = 0.f;
-                            if (c * 32 + e + 1 > row) p1 = 0.f;
+                            // visible: 0 <= query - key < W
+                            const int dd = d0 - (c * 32 + e);
+                            if (dd < 0 || dd >= W) p0 = 0.f;
+                            if (dd - 1 < 0 || dd - 1 >= W) p1 = 0.f;
                         }
                         // the normaliser sums the bf16-ROUNDED probabilities that the
                         // PV product consumes, so each row's weights sum to exactly 1
@@ -274,10 +285,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c + 1 < BN / 32) tmem_wait_ld();
                 }
             };
-            if (j == qt)
-                exp_tile(std::true_type{});
-            else
+            // every (query, key) pair of the tile visible: the plain loop
+            if (kt < qt && (qt - kt) * BM + BM - 1 < W)
                 exp_tile(std::false_type{});
+            else
+                exp_tile(std::true_type{});
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive_warp(bar(P_FULL + t));

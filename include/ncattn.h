@@ -153,6 +153,29 @@ int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new,
                    nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
                    int B, int H, int D, int Tcap, float eps, float rope_base, nc_stream_t stream);
 
+/* Sliding-window variants of the three calls above (same arguments, plus
+ * `window`).  Query i sees key j exactly when 0 <= i - j < window: the
+ * window's W most recent positions, its own included.  The pages run most
+ * layers with a short window of a quarter of the context (ai.flicky.cc,
+ * "nanochat: свой ChatGPT от токенизатора до чата", section "Модель: что
+ * изменилось со времён GPT-2", window-pattern bullet: pattern SSSL, the last
+ * layer always full); the boundary convention is this library's reading.
+ * window == 0 (or >= the sequence length / cache capacity) is the plain
+ * causal mask, exactly the calls above; window < 0 is NC_EINVAL.  Key tiles
+ * that no query of a tile can see are skipped, so the work shrinks with the
+ * window.  For decode, position p = lens[b] - 1 attends slots
+ * max(0, p - window + 1) .. p. */
+int nc_attn_fwd_sw(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
+                   float *lse, nc_f16 *qhat, nc_f16 *khat, float *rstd, void *workspace, size_t workspace_bytes,
+                   int B, int T, int H, int D, float eps, float rope_base, int window, nc_stream_t stream);
+int nc_attn_bwd_sw(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
+                   const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
+                   nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
+                   float eps, float rope_base, int window, nc_stream_t stream);
+int nc_attn_decode_sw(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+                      nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
+                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream);
+
 /* Decode without any device allocation.  The pages have no counterpart to
  * this call; it exists for callers that cannot provide a workspace: a
  * token-by-token serving loop that must not call cudaMalloc (which

@@ -79,6 +79,25 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert f(*args, 16, 1, 128, 2, 64, 1e-6, 1e4, None) == -1          # workspace too small
 
 
+def test_window_calls_reject_a_negative_window(lib):
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    f = lib.nc_attn_fwd_sw
+    f.argtypes = [P] * 10 + [SZ, I, I, I, I, F, F, I, P]
+    f.restype = I
+    args = [fake] * 3 + [None] + [fake] * 4 + [None] + [fake]
+    assert f(*args, 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -1, None) == -1
+    assert f(*([None] * 10), 0, 0, 128, 2, 64, 1e-6, 1e4, 32, None) == 0  # empty problem, any window
+    g = lib.nc_attn_bwd_sw
+    g.argtypes = [P] * 13 + [SZ, I, I, I, I, F, F, I, P]
+    g.restype = I
+    assert g(*([fake] * 3 + [None] + [fake] * 9), 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -5, None) == -1
+    d = lib.nc_attn_decode_sw
+    d.argtypes = [P] * 8 + [SZ, I, I, I, I, F, F, I, P]
+    d.restype = I
+    assert d(fake, None, None, fake, fake, fake, fake, fake, 1 << 30, 2, 2, 128, 64, 1e-6, 1e4, -1, None) == -1
+
+
 def test_empty_problem_is_a_no_op(lib):
     f = _fwd(lib)
     assert f(*([None] * 10), 0, 0, 128, 2, 64, 1e-6, 1e4, None) == 0
