@@ -193,9 +193,12 @@ def bench_ours(args, ws_n, rank, local):
     value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
 
     # ---- decode (same rank, own timing; L2 flushed between calls) ----
-    dec = e2e = None
+    dec = e2e = win = None
     if not args.no_extras:
         dec = bench_decode(nc, dev, args, rank)
+        # ---- the short-window layers: the same step with W = T / 4 ----
+        win = bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv, ws_f, ws_b, stream)
+        win["decode"] = bench_decode(nc, dev, args, rank, window=w.T // 4)
         # ---- end to end through the public API with host buffers ----
         e2e = bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b)
 
@@ -217,8 +220,9 @@ def bench_ours(args, ws_n, rank, local):
     roof = None
     if name in alg:
         ach = alg[name] / (per_launch_ms * 1e-3) / 1e12
+        tr = DRAM_TRAFFIC.get(name) if args.workload == "d20" else None
         roof = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_t,
-                "unit": "TFLOP/s", "frac": round(ach / peak_t, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(ach / peak_t, 4), "traffic": tr,
                 "peak_kind": f"{pk_kind} {'sustained' if timed_s > 2.0 else 'burst'} bf16"}
     kernels = {k_: {"launches": n_, "avg_us": round(1e3 * t_ / max(n_, 1), 2),
                     "share": round(t_ / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
@@ -250,6 +254,7 @@ def bench_ours(args, ws_n, rank, local):
         "roofline": roof,
         "kernels": kernels,
         "decode": dec,
+        "window": win,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -257,7 +262,64 @@ def bench_ours(args, ws_n, rank, local):
     return line
 
 
-def bench_decode(nc, dev, args, rank):
+# DRAM bytes (read + write) of one launch of a kernel at the d20 workload,
+# from one ncu capture of the current kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum, summarised under profiles/ with its command).
+# Must go back to None whenever that kernel's code changes.
+DRAM_TRAFFIC = {"attn_bwd_dkdv": 852.95e6 + 311.85e6}
+
+
+def band_pairs(T, W):
+    """Score pairs per (b, h) under a sliding window W, in the convention of
+    the causal count (T^2/2 = the area under the diagonal): T*W - W^2/2."""
+    W = min(W, T)
+    return T * W - W * W / 2.0
+
+
+def bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv, ws_f, ws_b, stream):
+    """The fwd+bwd step through the sliding-window calls with W = T/4 (the
+    short-window layers of the pages' SSSL pattern), timed like the main step;
+    algorithmic FLOPs over the band only (tiles outside it are skipped)."""
+    W = w.T // 4
+    eps, base = workloads.EPS, workloads.ROPE_BASE
+
+    def step():
+        nc.nc_attn_fwd_sw(qd, kd, vd, None, out, lse, qh, kh, None, ws_f, eps, base, W, stream)
+        nc.nc_attn_bwd_sw(qd, kd, vd, None, out, lse, qh, kh, dod, dq, dk, dv, ws_b, eps, base, W, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 5)
+    nc.nc_profile_read()
+    nc.nc_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    nc.nc_profile_enable(False)
+    kern = nc.nc_profile_read()
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during the window leg")
+    ms = e0.elapsed_time(e1) / steps
+    fwd = 4.0 * w.B * w.H * w.D * band_pairs(w.T, W)
+    pk, _ = peaks()
+    alg = {"attn_fwd": fwd, "attn_bwd_dkdv": 2.0 * fwd, "attn_bwd_dq": 0.5 * fwd}
+    kernels = {}
+    for k_, (n_, t_) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
+        kernels[k_] = {"avg_us": round(1e3 * t_ / max(n_, 1), 2)}
+        if k_ in alg:
+            tf = alg[k_] / (t_ / n_ * 1e-3) / 1e12
+            kernels[k_]["tflops"] = round(tf, 1)
+            kernels[k_]["frac_of_peak"] = round(tf / pk["bf16_tflops"], 4)
+    return {"workload": f"{w.name} fwd+bwd with a sliding window W = T/4 = {W}", "W": W,
+            "ms_per_step": round(ms, 4), "value": round(3.5 * fwd / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "flops_per_step": 3.5 * fwd, "kernels": kernels}
+
+
+def bench_decode(nc, dev, args, rank, window=0):
     w = workloads.D20_DECODE
     lens, q, k_raw, v = workloads.decode_workload_inputs(w)
     kcache = nc.qk_norm_rope(k_raw.to(dev), eps=workloads.EPS, rope_base=workloads.ROPE_BASE)
@@ -269,8 +331,12 @@ def bench_decode(nc, dev, args, rank):
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        nc.nc_attn_decode(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
-                          workloads.ROPE_BASE, stream)
+        if window:
+            nc.nc_attn_decode_sw(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
+                                 workloads.ROPE_BASE, window, stream)
+        else:
+            nc.nc_attn_decode(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
+                              workloads.ROPE_BASE, stream)
 
     for _ in range(args.warmup):
         call()
@@ -286,11 +352,14 @@ def bench_decode(nc, dev, args, rank):
         times.append(e0.elapsed_time(e1))
     if nc.device_status() != 0:
         raise RuntimeError("device status set during decode")
-    byt = workloads.decode_bytes(lens, w.H, w.D)
+    byt = workloads.decode_bytes(torch.clamp(lens, max=window) if window else lens, w.H, w.D)
     ms = statistics.median(times)
     pk, kind = peaks()
     gbs = byt / (ms * 1e-3) / 1e9
-    return {"workload": "d20 decode: 32 streams, H=10, D=128, cache capacity 2048, lens ~ U[1,2048] seed 4",
+    name = "d20 decode: 32 streams, H=10, D=128, cache capacity 2048, lens ~ U[1,2048] seed 4"
+    if window:
+        name += f", sliding window W = {window} (the last W slots)"
+    return {"workload": name,
             "bytes": byt, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None},
