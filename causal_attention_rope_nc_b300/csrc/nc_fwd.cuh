@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // the normaliser sums the bf16-ROUNDED probabilities that the
                         // PV product consumes, so each row's weights sum to exactly 1
                         const uint32_t wv = pack_bf16x2(p0, p1);
-                        l_lo += __uint_as_float(wv << 16);
-                        l_hi += __uint_as_float(wv & 0xffff0000u);
+                        l_lo = add_bf16_lo(l_lo, wv);
+                        l_hi = add_bf16_hi(l_hi, wv);
                         w[e / 2] = wv;
                     }
                     // chunk c lands in packed columns [16c, 16c+16): already read
