@@ -306,3 +306,63 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
         }
     return err;
 }
+
+/* Prefill of a chunk: C new tokens per stream b at positions start[b] ..
+ * start[b] + C - 1, each attending (causally, inside the window when W > 0)
+ * over the cache slots 0 .. its own position.  Keys are given RAW for every
+ * slot up to start[b] + C - 1 (the chunk's own keys in its slots): slot j is
+ * normalised and rotated at position j, as the cache holds it.  This is
+ * rows start[b] .. start[b] + C - 1 of the forward over the whole sequence.
+ * q, out [B,C,H,D]; k_raw, v [B,Tcap,H,D]; lse [B,H,C] (may be NULL). */
+int orc_attn_prefill(const double *q, const double *k_raw, const double *v, const int *start,
+                     int B, int C, int H, int D, int Tcap, double eps, double base, int flags, int W,
+                     double *out, double *lse)
+{
+    double scale = 1.0 / sqrt((double)D);
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            int s0 = start[b];
+            if (s0 < 0 || s0 + C > Tcap) { err = -2; continue; }
+            int L = s0 + C;
+            double *qh = malloc((size_t)D * sizeof(double));
+            double *kh = malloc((size_t)L * D * sizeof(double));
+            double *s = malloc((size_t)L * sizeof(double));
+            for (int j = 0; j < L; ++j) {
+                const double *kj = k_raw + at4(b, j, h, 0, Tcap, H, D);
+                double rk = (flags & ORC_NORM) ? rms_of(kj, D, eps) : 1.0;
+                for (int d = 0; d < D; ++d) kh[(size_t)j * D + d] = kj[d] / rk;
+                if (flags & ORC_ROPE) rotate(kh + (size_t)j * D, j, D, base, +1);
+            }
+            for (int t = 0; t < C; ++t) {
+                int p = s0 + t;
+                const double *qi = q + at4(b, t, h, 0, C, H, D);
+                double rq = (flags & ORC_NORM) ? rms_of(qi, D, eps) : 1.0;
+                for (int d = 0; d < D; ++d) qh[d] = qi[d] / rq;
+                if (flags & ORC_ROPE) rotate(qh, p, D, base, +1);
+                double m = -INFINITY;
+                for (int j = 0; j < L; ++j) {
+                    s[j] = -INFINITY;
+                    if (!visible(p, j, W)) continue;
+                    s[j] = dot(qh, kh + (size_t)j * D, D) * scale;
+                    if (s[j] > m) m = s[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < L; ++j) {
+                    s[j] = exp(s[j] - m);
+                    l += s[j];
+                }
+                double *oi = out + at4(b, t, h, 0, C, H, D);
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h, d, Tcap, H, D)];
+                    oi[d] = acc;
+                }
+                if (lse) lse[((size_t)b * H + h) * C + t] = m + log(l);
+            }
+            free(qh); free(kh); free(s);
+        }
+    return err;
+}
+

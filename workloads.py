@@ -126,6 +126,22 @@ def decode_inputs(B: int, H: int, D: int, Tcap: int, seed: int, lens=None):
     return lens, q, k_raw, v
 
 
+def prefill_inputs(B: int, C: int, H: int, D: int, Tcap: int, seed: int, start=None):
+    """start [B] int32 (uniform in [0, Tcap - C] unless given), then the chunk's
+    queries q [B,C,H,D], raw keys [B,Tcap,H,D] and values [B,Tcap,H,D], all bf16
+    CPU tensors.  Stream b's chunk holds positions start[b] .. start[b]+C-1;
+    its own raw keys and values are the slots start[b] .. start[b]+C-1 of
+    k_raw and v, the slots before them the stream's history."""
+    g = _gen(seed)
+    if start is None:
+        start = torch.randint(0, Tcap - C + 1, (B,), generator=g, dtype=torch.int64)
+    start = torch.as_tensor(start, dtype=torch.int32)
+    q = randn_bf16((B, C, H, D), g)
+    k_raw = randn_bf16((B, Tcap, H, D), g)
+    v = randn_bf16((B, Tcap, H, D), g)
+    return start, q, k_raw, v
+
+
 def decode_workload_inputs(w: DecodeWorkload):
     return decode_inputs(w.B, w.H, w.D, w.Tcap, w.seed)
 
