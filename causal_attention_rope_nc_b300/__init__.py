@@ -20,12 +20,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libncattn.so")
 
 NC_OK, NC_EINVAL, NC_EUNSUPPORTED, NC_ELAUNCH, NC_EDEVICE = 0, -1, -2, -3, -4
-NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE = 0, 1, 2, 3
+NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE, NC_OP_PREFILL = 0, 1, 2, 3, 4
 
 EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
             "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
             "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc",
-            "nc_attn_fwd_sw", "nc_attn_bwd_sw", "nc_attn_decode_sw")
+            "nc_attn_fwd_sw", "nc_attn_bwd_sw", "nc_attn_decode_sw", "nc_attn_prefill")
 NC_ETOOLARGE = -5
 
 
@@ -75,6 +75,8 @@ def _load():
     L.nc_attn_bwd_sw.restype = I
     L.nc_attn_decode_sw.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
     L.nc_attn_decode_sw.restype = I
+    L.nc_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, F, F, I, S]
+    L.nc_attn_prefill.restype = I
     return L
 
 
@@ -206,6 +208,17 @@ def nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps
     _check(lib.nc_attn_decode_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_decode_sw")
 
 
+def nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, workspace, eps, rope_base, window=0, stream=None):
+    for n, t in (("q", q), ("k", k), ("v", v), ("vcache", vcache), ("out", out)):
+        _bf16(t, n)
+    _f16(kcache, "kcache")
+    B, C, H, D = q.shape
+    Tcap = kcache.shape[1]
+    _check(lib.nc_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(start), _ptr(kcache), _ptr(vcache), _ptr(out),
+                               _ptr(lse), _ptr(workspace), workspace.numel(), B, C, H, D, Tcap, eps, rope_base,
+                               int(window), _stream(stream)), "nc_attn_prefill")
+
+
 def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
     """nc_attn_decode for callers that cannot supply a workspace (the library
     keeps the scratch in a fixed 16 MiB device array; see include/ncattn.h)."""
@@ -266,3 +279,16 @@ def attn_decode(q, kcache, vcache, lens, k_new=None, v_new=None, eps=1e-6, rope_
     else:
         nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, stream)
     return out
+
+
+def attn_prefill(q, k, v, start, kcache, vcache, eps=1e-6, rope_base=10000.0, window=0, workspace=None,
+                 stream=None):
+    """Chunk prefill: appends the chunk's normalised, rotated keys and its
+    values to the caches in place and returns (out [B,C,H,D], lse [B,H,C])."""
+    B, C, H, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, C), dtype=torch.float32, device=q.device)
+    ws = workspace if workspace is not None else new_workspace(NC_OP_PREFILL, B, C, H, D, q.device)
+    nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, ws, eps, rope_base, window, stream)
+    return out, lse
+

@@ -253,7 +253,44 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
-        float(mfix * log2e), float(mfix), W);
+        float(mfix * log2e), float(mfix), W, nullptr, T);
+    return launch_status();
+}
+
+// Chunk prefill: the prologue writes qhat (workspace) and the chunk's keys
+// and values into the caches, then the forward kernel runs with the chunk's
+// queries at their cache positions and the caches as keys and values.
+template <int D>
+int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* start, nc_bf16* kcache,
+                 nc_bf16* vcache, nc_bf16* out, float* lse, void* ws, int B, int C, int H, int Tcap, float eps,
+                 float base, int W, cudaStream_t s) {
+    nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
+    for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
+    __half* qhat = reinterpret_cast<__half*>(ws);
+    {
+        ProfScope ps("prefill_norm_rope", s);
+        nc::prefill_norm_rope_kernel<D><<<tok_grid(static_cast<long long>(B) * C, D), 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
+            reinterpret_cast<const __nv_bfloat16*>(v), start, qhat, reinterpret_cast<__half*>(kcache),
+            reinterpret_cast<__nv_bfloat16*>(vcache), B, C, H, Tcap, eps, th);
+    }
+    int rc = launch_status();
+    if (rc) return rc;
+    CUtensorMap tq, tk, tv, to;
+    if (make_tmap(&tq, qhat, B, C, H, D, nc::fwd::BM, kF16) || make_tmap(&tk, kcache, B, Tcap, H, D, nc::fwd::BN, kF16) ||
+        make_tmap(&tv, vcache, B, Tcap, H, D, nc::fwd::BN) || make_tmap(&to, out, B, C, H, D, nc::fwd::BM))
+        return NC_EINVAL;
+    const int n_qt = (C + nc::fwd::BM - 1) / nc::fwd::BM;
+    const double scale = 1.0 / std::sqrt(double(D));
+    const double log2e = 1.4426950408889634;
+    const double mfix = std::sqrt(double(D)) * 1.0079;
+    const int n_pairs = (n_qt + 1) / 2;
+    const long long nblk = static_cast<long long>(n_pairs) * B * H;
+    if (nblk > 0x7fffffffLL) return NC_EINVAL;
+    ProfScope ps("attn_prefill", s);
+    nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
+        tq, tk, tv, to, lse, C, H, B, n_qt, tile_group(n_pairs, B * H), float(scale * log2e), float(mfix * log2e),
+        float(mfix), W, start, Tcap);
     return launch_status();
 }
 
@@ -342,7 +379,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
     const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
     const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
     const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
-    nc::dec::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
+    nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
     for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
     ProfScope ps("attn_decode", s);
     nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0, s>>>(
@@ -444,6 +481,7 @@ size_t nc_attn_workspace_size(int op, int B, int T, int H, int D) {
             return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256;
         }
         case NC_OP_DECODE: return decode_ws_layout(B, H, D, T, nullptr, nullptr);
+        case NC_OP_PREFILL: return up256(static_cast<size_t>(B) * T * H * D * 2);  // qhat of the chunk
         default: return 0;
     }
 }
@@ -548,6 +586,29 @@ int nc_attn_decode_sw(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_n
     return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W, s)
                    : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W,
                                       s);
+}
+
+int nc_attn_prefill(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* start, nc_bf16* kcache,
+                    nc_bf16* vcache, nc_bf16* out, float* lse, void* workspace, size_t workspace_bytes, int B, int C,
+                    int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream) {
+    if (!shape_ok(B, C, H, D) || !params_ok(eps, rope_base) || window < 0 || Tcap < C || Tcap > (1 << 24))
+        return NC_EINVAL;
+    if (B == 0 || C == 0 || H == 0) return NC_OK;
+    if (!q || !k || !v || !start || !kcache || !vcache || !out || !workspace) return NC_EINVAL;
+    const void* b16[] = {q, k, v, kcache, vcache, out};
+    for (const void* p : b16)
+        if (!aligned16(p)) return NC_EINVAL;
+    if (!aligned256(workspace) || (reinterpret_cast<uintptr_t>(start) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_PREFILL, B, C, H, D)) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int W = window_eff(window, Tcap);
+    return D == 64 ? prefill_impl<64>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Tcap, eps,
+                                      rope_base, W, s)
+                   : prefill_impl<128>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Tcap, eps,
+                                       rope_base, W, s);
 }
 
 }  // extern "C"

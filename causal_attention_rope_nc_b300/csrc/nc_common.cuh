@@ -484,6 +484,12 @@ __device__ __forceinline__ double rope_theta(int i, int D, double log2_base) {
     return exp2(-(2.0 * i / D) * log2_base);
 }
 
+// RoPE frequencies theta_i = base^(-2i/D), i < D/2, formed on the host in
+// double precision and passed by value.
+struct Theta {
+    double t[64];
+};
+
 __device__ __forceinline__ float2 rope_cos_sin(int p, double theta) {
     const double two_pi = 6.283185307179586476925286766559;
     const double a = static_cast<double>(p) * theta;

@@ -56,12 +56,6 @@ struct Lanes {
     static_assert(NLD >= 1 && BATCH % SPW == 0, "batch shape");
 };
 
-// RoPE frequencies theta_i = base^(-2i/D), i < D/2, formed on the host in
-// double precision and passed by value.
-struct Theta {
-    double t[64];
-};
-
 // 16-byte streaming load (read once: evict first).  A regular coherent global
 // load, so a slot written earlier by the same warp is seen after __syncwarp.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }

@@ -1,7 +1,10 @@
 // Causal attention forward on sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // One CTA computes two consecutive 128-row query tiles (2p and 2p+1) of one
-// (batch, head); both share every K/V tile it streams.  With a sliding window
+// (batch, head); both share every K/V tile it streams.  Query row r of stream
+// b sits at position qoff[b] + r (qoff == nullptr: position r) among Tk key
+// positions: a chunk of new tokens attending over a KV cache, or (offset 0,
+// Tk = T) the whole sequence.  With a sliding window
 // W (query i sees key j when 0 <= i - j < W) the stream starts at the first
 // key tile either query tile can see, and tile 2p+1 may start one K/V tile
 // later than tile 2p:
@@ -86,7 +89,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
                     float* __restrict__ lse, int T, int H, int B, int n_qt, int group, float scale_log2,
-                    float mfix_log2, float mfix, int W) {
+                    float mfix_log2, float mfix, int W, const int* __restrict__ qoff, int Tk) {
     using S = Smem<D>;
     constexpr int NC = D / 64;  // 64-column (128-byte) swizzle spans per row
     extern __shared__ uint8_t smem_raw[];
@@ -103,13 +106,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int qt0 = 2 * (n_pairs - 1 - tc.rank);
     const int b = tc.bh / H, h = tc.bh % H;
     const bool has1 = qt0 + 1 < n_qt;
-    // first key tile a query tile sees (W >= 2^30 means no window)
-    auto first_kt = [&](int qt) { return max(0, qt * BM - W + 1) / BN; };
+    const int qpos0 = qoff ? qoff[b] : 0;  // position of query row 0
+    if (qpos0 < 0 || qpos0 + T > Tk) {     // uniform over the CTA: nothing has started yet
+        if (threadIdx.x == 0) flag_error(2, 0x0f1);
+        return;
+    }
+    // key tiles a query tile sees: from the first key within W of its first
+    // row (W >= 2^30 means no window) to the key at its last row's position
+    auto first_kt = [&](int qt) { return max(0, qpos0 + qt * BM - W + 1) / BN; };
+    auto last_kt = [&](int qt) { return (qpos0 + min(T - 1, qt * BM + BM - 1)) / BN; };
     const int lo0 = first_kt(qt0), lo1 = has1 ? first_kt(qt0 + 1) : lo0;
-    const int f1 = lo1 - lo0;                 // stream index of tile qt0+1's first key tile (0 or 1)
-    const int n0 = qt0 - lo0 + 1;             // key tiles of query tile qt0
-    const int n1 = has1 ? qt0 + 2 - lo1 : 0;  // key tiles of query tile qt0 + 1
-    const int n_kv = has1 ? qt0 + 2 - lo0 : n0;
+    const int hi0 = last_kt(qt0), hi1 = has1 ? last_kt(qt0 + 1) : hi0;
+    const int f1 = lo1 - lo0;               // stream index of tile qt0+1's first key tile (0 or 1)
+    const int n0 = hi0 - lo0 + 1;           // key tiles of query tile qt0
+    const int n1 = has1 ? hi1 - lo1 + 1 : 0;  // key tiles of query tile qt0 + 1
+    const int n_kv = hi1 - lo0 + 1;         // the stream: tile qt0's tiles then tile qt0+1's last
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
 
@@ -254,8 +265,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t r[2][32];
             tmem_ld32(ts, r[0]);
             tmem_wait_ld();
-            const int kt = (t ? lo1 : lo0) + j;     // key tile
-            const int d0 = (qt - kt) * BM + row;    // query - key at column 0 of the tile
+            const int kt = (t ? lo1 : lo0) + j;            // key tile
+            const int d0 = qpos0 + qt * BM + row - kt * BN;  // query - key position at column 0 of the tile
             auto exp_tile = [&](auto masked) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             };
             // every (query, key) pair of the tile visible: the plain loop
-            if (kt < qt && (qt - kt) * BM + BM - 1 < W)
+            if (kt * BN + BN - 1 <= qpos0 + qt * BM && qpos0 + qt * BM + BM - 1 - kt * BN < W)
                 exp_tile(std::false_type{});
             else
                 exp_tile(std::true_type{});
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const float l_sum = l_lo + l_hi;
             const float inv_l = 1.f / l_sum;
-            if (q_idx < T) lse[(static_cast<long long>(b) * H + h) * T + q_idx] = mfix + logf(l_sum);
+            if (lse != nullptr && q_idx < T) lse[(static_cast<long long>(b) * H + h) * T + q_idx] = mfix + logf(l_sum);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) stage_acc_bf16<32>(tmem + lane_base + tm_o<D>(t), inv_l, stage, row, c * 32);
             fence_proxy_async_smem();

@@ -126,6 +126,85 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
     }
 }
 
+// --------------------------------------------- chunk prefill prologue ----
+// For the C new tokens of stream b (positions start[b] + t, t < C):
+//   qhat[b][t][h] = RoPE(RMSNorm(q[b][t][h]), start[b] + t)    (fp16, workspace)
+//   kcache[b][start[b] + t][h] = RoPE(RMSNorm(k[b][t][h]), start[b] + t)  (fp16)
+//   vcache[b][start[b] + t][h] = v[b][t][h]                     (bf16 copy)
+// One group of D/8 lanes owns one token of one stream: it forms the token's
+// rotation (cos, sin of its 8 pair indices) from the frequencies and walks
+// the token's H heads.  A stream whose chunk does not fit its cache
+// (start < 0 or start + C > Tcap) is skipped and recorded (status 2).
+template <int D>
+__global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
+                                                                const __nv_bfloat16* __restrict__ k,
+                                                                const __nv_bfloat16* __restrict__ v,
+                                                                const int* __restrict__ start,
+                                                                __half* __restrict__ qhat, __half* kcache,
+                                                                __nv_bfloat16* vcache, int B, int C, int H, int Tcap,
+                                                                float eps, const __grid_constant__ Theta theta) {
+    using L = RowLanes<D>;
+    const int sub = threadIdx.x % L::LPR;
+    const long long groups = blockDim.x / L::LPR;
+    const long long ntok = static_cast<long long>(B) * C;
+    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
+    const long long stride = static_cast<long long>(gridDim.x) * groups;
+    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
+    const int i0 = (sub % L::HALF) * 8;
+    const bool lo = sub < L::HALF;
+    // every lane of a warp runs the same number of iterations (shuffles)
+    for (long long base = warp_first, tok = first; base < ntok; base += stride, tok += stride) {
+        bool valid = tok < ntok;
+        const int b = valid ? static_cast<int>(tok / C) : 0;
+        const int t = valid ? static_cast<int>(tok % C) : 0;
+        const int s0 = valid ? start[b] : 0;
+        if (valid && (s0 < 0 || s0 + C > Tcap)) {
+            if (t == 0 && sub == 0) flag_error(2, 0x601);
+            valid = false;
+        }
+        const int p = s0 + t;
+        float c[8], sn[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 r = valid ? rope_cos_sin(p, theta.t[i0 + e]) : make_float2(1.f, 0.f);
+            c[e] = r.x;
+            sn[e] = r.y;
+        }
+        const long long tok_in = (static_cast<long long>(b) * C + t) * H * D + sub * 8;
+        const long long slot = (static_cast<long long>(b) * Tcap + p) * H * D + sub * 8;
+        for (int h = 0; h < H; ++h) {
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {  // q, then k
+                float x[8];
+                if (valid)
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>((which ? k : q) + tok_in + h * D), x);
+                else
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                ss = group_sum<L::LPR>(ss);
+                const float rs = rsqrtf(ss / D + eps);
+                float y[8], o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] *= rs;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], L::HALF);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
+                if (valid) {
+                    __half* dst = which ? kcache + slot + h * D : qhat + tok_in + h * D;
+                    *reinterpret_cast<uint4*>(dst) = f32x8_to_f16(o);
+                }
+            }
+            if (valid)
+                *reinterpret_cast<uint4*>(vcache + slot + h * D) =
+                    *reinterpret_cast<const uint4*>(v + tok_in + h * D);
+        }
+    }
+}
+
 // -------------------------------------------------- backward preprocess ----
 // delta[b][h][t] = <dout_t, out_t> (fp32), lse2[b][h][t] = lse * log2(e),
 // both padded to Tpad columns (delta 0, lse2 +inf beyond T so that padded

@@ -72,6 +72,7 @@ typedef struct CUstream_st *nc_stream_t; /* == cudaStream_t */
 #define NC_OP_BWD 1
 #define NC_OP_DECODE 2
 #define NC_OP_NORM_ROPE 3
+#define NC_OP_PREFILL 4
 
 /* Library version, (major << 16) | minor. */
 int nc_version(void);
@@ -85,7 +86,7 @@ int nc_last_cuda_error(void);
 /* Synchronises `stream`, then reads and clears the device status word of
  * the current device.  *status = 0 when no kernel has reported a failure,
  * else (code << 16) | site with code 1 = a bounded wait timed out,
- * 2 = a decode length outside [1, Tcap].  Returns NC_OK or NC_ELAUNCH. */
+ * 2 = a decode length outside [1, Tcap] or a prefill chunk outside its cache.  Returns NC_OK or NC_ELAUNCH. */
 int nc_device_status(nc_stream_t stream, unsigned int *status);
 
 /* Optional per-kernel timing.  While enabled (on != 0), every kernel the
@@ -175,6 +176,26 @@ int nc_attn_bwd_sw(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const i
 int nc_attn_decode_sw(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
                       nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
                       int B, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream);
+
+/* Chunk prefill into a KV cache.  Stream b appends C new tokens at
+ * positions start[b] .. start[b] + C - 1 (start: [B] int32, device): their
+ * raw q, k, v [B][C][H][D] are normalised and rotated at those positions;
+ * the keys (fp16, normalised and rotated, as nc_qk_norm_rope writes them)
+ * and the values go into slots start[b] .. start[b] + C - 1 of kcache /
+ * vcache [B][Tcap][H][D]; each new query attends causally over slots
+ * 0 .. its own position (the last `window` of them when window > 0, as in
+ * the *_sw calls).  out [B][C][H][D] bf16; lse [B][H][C] fp32, natural log,
+ * or NULL.  The slots before start[b] must already hold the stream's keys
+ * and values.  With start[b] = 0 and C = T this is nc_attn_fwd_sw over the
+ * chunk (plus the cache writes); a prompt may also be fed in several chunks,
+ * each starting where the previous one ended.  The pages prefill the KV
+ * cache before decoding (ai.flicky.cc, "nanochat: свой ChatGPT от
+ * токенизатора до чата", section "Карта репозитория", engine.py row).
+ * A stream with start[b] < 0 or start[b] + C > Tcap is skipped and recorded
+ * in the device status word (2).  Workspace: NC_OP_PREFILL with T = C. */
+int nc_attn_prefill(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *start, nc_f16 *kcache,
+                    nc_bf16 *vcache, nc_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, int B,
+                    int C, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream);
 
 /* Decode without any device allocation.  The pages have no counterpart to
  * this call; it exists for callers that cannot provide a workspace: a
