@@ -193,12 +193,14 @@ def bench_ours(args, ws_n, rank, local):
     value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
 
     # ---- decode (same rank, own timing; L2 flushed between calls) ----
-    dec = e2e = win = None
+    dec = e2e = win = pre = None
     if not args.no_extras:
         dec = bench_decode(nc, dev, args, rank)
         # ---- the short-window layers: the same step with W = T / 4 ----
         win = bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv, ws_f, ws_b, stream)
         win["decode"] = bench_decode(nc, dev, args, rank, window=w.T // 4)
+        # ---- a 512-token chunk appended to every stream's cache ----
+        pre = bench_prefill(nc, dev, args)
         # ---- end to end through the public API with host buffers ----
         e2e = bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b)
 
@@ -255,6 +257,7 @@ def bench_ours(args, ws_n, rank, local):
         "kernels": kernels,
         "decode": dec,
         "window": win,
+        "prefill": pre,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -317,6 +320,59 @@ def bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv
     return {"workload": f"{w.name} fwd+bwd with a sliding window W = T/4 = {W}", "W": W,
             "ms_per_step": round(ms, 4), "value": round(3.5 * fwd / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "flops_per_step": 3.5 * fwd, "kernels": kernels}
+
+
+def bench_prefill(nc, dev, args, B=32, H=10, D=128, Tcap=2048, C=512):
+    """nc_attn_prefill of a C-token chunk per stream at position Tcap - C of a
+    full cache (the d20 decode shapes): prologue + attention of the chunk over
+    its cache prefix.  FLOPs: 4 D per visible score pair, pairs counted like the
+    causal forward (C (Tcap - C) + C^2/2 per (b, h))."""
+    eps, base = workloads.EPS, workloads.ROPE_BASE
+    s0 = Tcap - C
+    start_t, q, k_raw, v = workloads.prefill_inputs(B, C, H, D, Tcap, seed=5, start=[s0] * B)
+    kcache = nc.qk_norm_rope(k_raw.to(dev), eps=eps, rope_base=base)
+    vcache = v.to(dev)
+    qd = q.to(dev)
+    kc = k_raw[:, s0:].contiguous().to(dev)
+    vc = v[:, s0:].contiguous().to(dev)
+    st = start_t.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, C), dtype=torch.float32, device=dev)
+    ws = nc.new_workspace(nc.NC_OP_PREFILL, B, C, H, D, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        nc.nc_attn_prefill(qd, kc, vc, st, kcache, vcache, out, lse, ws, eps, base, 0, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 5)
+    nc.nc_profile_read()
+    nc.nc_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    nc.nc_profile_enable(False)
+    kern = nc.nc_profile_read()
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during the prefill leg")
+    ms = e0.elapsed_time(e1) / steps
+    flops = 4.0 * B * H * D * (C * s0 + C * C / 2.0)
+    pk, _ = peaks()
+    kernels = {k_: {"avg_us": round(1e3 * t_ / max(n_, 1), 2)} for k_, (n_, t_) in kern.items()}
+    if "attn_prefill" in kern:
+        n_, t_ = kern["attn_prefill"]
+        tf = flops / (t_ / n_ * 1e-3) / 1e12
+        kernels["attn_prefill"]["tflops"] = round(tf, 1)
+        kernels["attn_prefill"]["frac_of_peak"] = round(tf / pk["bf16_tflops"], 4)
+    return {"workload": f"chunk prefill: {B} streams, H={H}, D={D}, {C} new tokens at position {s0} of a "
+                        f"{Tcap}-slot cache", "us": round(ms * 1e3, 2),
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "tokens_per_s": round(B * C / (ms * 1e-3), 1), "kernels": kernels}
 
 
 def bench_decode(nc, dev, args, rank, window=0):
