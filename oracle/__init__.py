@@ -6,7 +6,9 @@ imports this package.  The arithmetic lives in ``ncattn_oracle.c`` (plain
 loops in double precision); this module only marshals numpy arrays to it.
 
 Every function takes and returns float64 numpy arrays, [B, T, H, D] layout
-for token tensors, [B, H, T] for the log-sum-exp.  ``window`` W > 0 restricts
+for token tensors (k, v and their gradients with Hkv <= H heads: grouped-query
+attention, query head h using key/value head h // (H // Hkv)), [B, H, T] for
+the log-sum-exp.  ``window`` W > 0 restricts
 the causal mask to the last W keys (query i sees key j when 0 <= i - j < W);
 0 means the plain causal mask.
 """
@@ -48,16 +50,21 @@ def _load():
         i, d = ctypes.c_int, ctypes.c_double
         lib.orc_norm_rope.argtypes = [dp, ip, i, i, i, i, d, d, i, dp, dp]
         lib.orc_norm_rope.restype = None
-        lib.orc_attn_fwd.argtypes = [dp, dp, dp, ip, i, i, i, i, d, d, i, i, dp, dp]
+        lib.orc_attn_fwd.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp, dp]
         lib.orc_attn_fwd.restype = ctypes.c_int
-        lib.orc_attn_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, i, d, d, i, i, dp, dp, dp]
+        lib.orc_attn_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp, dp, dp]
         lib.orc_attn_bwd.restype = ctypes.c_int
-        lib.orc_attn_decode.argtypes = [dp, dp, dp, ip, i, i, i, i, d, d, i, i, dp]
+        lib.orc_attn_decode.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp]
         lib.orc_attn_decode.restype = ctypes.c_int
         lib.orc_attn_prefill.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp, dp]
         lib.orc_attn_prefill.restype = ctypes.c_int
         _lib = lib
     return _lib
+
+
+def _check_groups(H, Hkv, Hv):
+    if Hkv != Hv or Hkv < 1 or H % Hkv:
+        raise ValueError("key and value heads must match and divide the query heads")
 
 
 def _f64(x) -> np.ndarray:
@@ -95,7 +102,9 @@ def attn_fwd(q, k, v, pos=None, eps=1e-6, base=10000.0, flags=METHOD, window=0):
     o = np.empty_like(q)
     lse = np.empty((B, H, T), dtype=np.float64)
     p, pp = _pos(pos, T)
-    rc = _load().orc_attn_fwd(_dp(q), _dp(k), _dp(v), pp, B, T, H, D, eps, base, flags, int(window),
+    Hkv = k.shape[2]
+    _check_groups(H, Hkv, v.shape[2])
+    rc = _load().orc_attn_fwd(_dp(q), _dp(k), _dp(v), pp, B, T, H, Hkv, D, eps, base, flags, int(window),
                               _dp(o), _dp(lse))
     if rc != 0:
         raise MemoryError("oracle forward failed")
@@ -106,9 +115,11 @@ def attn_bwd(q, k, v, dout, pos=None, eps=1e-6, base=10000.0, flags=METHOD, wind
     """Causal attention backward: (dq, dk, dv), each [B,T,H,D]."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, T, H, D = q.shape
-    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    Hkv = k.shape[2]
+    _check_groups(H, Hkv, v.shape[2])
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
     p, pp = _pos(pos, T)
-    rc = _load().orc_attn_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), pp, B, T, H, D, eps, base,
+    rc = _load().orc_attn_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), pp, B, T, H, Hkv, D, eps, base,
                               flags, int(window), _dp(dq), _dp(dk), _dp(dv))
     if rc != 0:
         raise MemoryError("oracle backward failed")
@@ -119,12 +130,14 @@ def attn_decode(q, k_raw, v, lens, eps=1e-6, base=10000.0, flags=METHOD, window=
     """Single-token decode: out [B,H,D] for new queries q [B,H,D] at position
     lens-1 over raw keys k_raw and values v [B,Tcap,H,D]."""
     q, k_raw, v = _f64(q), _f64(k_raw), _f64(v)
-    B, Tcap, H, D = k_raw.shape
+    B, Tcap, Hkv, D = k_raw.shape
+    H = q.shape[1]
+    _check_groups(H, Hkv, v.shape[2])
     lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int32).reshape(B))
     out = np.empty((B, H, D), dtype=np.float64)
     rc = _load().orc_attn_decode(_dp(q), _dp(k_raw), _dp(v),
                                  lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
-                                 B, H, D, Tcap, eps, base, flags, int(window), _dp(out))
+                                 B, H, Hkv, D, Tcap, eps, base, flags, int(window), _dp(out))
     if rc != 0:
         raise ValueError("oracle decode: lens out of [1, Tcap]")
     return out

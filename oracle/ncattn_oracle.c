@@ -24,6 +24,11 @@
  *  - Decode: generation with a KV cache (ai.flicky.cc, section
  *    "Карта репозитория", engine.py row; 7minutos.es "Andrej Karpathy lanza
  *    nanochat ...", section "Entrenamiento medio, SFT y uso de herramientas").
+ *  - Grouped-query attention: fewer key/value heads than query heads is an
+ *    option of the model (ai.flicky.cc, section "Модель: что изменилось со
+ *    времён GPT-2", GQA bullet).  Read here as: with Hkv key/value heads,
+ *    query head h uses key/value head h / (H / Hkv) (consecutive query heads
+ *    share one); the key and value gradients sum over the group.
  *  - Sliding windows: most layers attend through a short window of a quarter
  *    of the context (ai.flicky.cc, section "Модель: что изменилось со времён
  *    GPT-2", window-pattern bullet).  Read here as: with window W > 0, query
@@ -107,9 +112,10 @@ static double dot(const double *a, const double *b, int n)
 /* Step 3 for one (b, h): probabilities P[i][j] (zero where j is not
  * visible from i), outputs o and log-sum-exp.  P is T*T, row-major. */
 static void attend_head(const double *qh, const double *kh, const double *v,
-                        int b, int h, int T, int H, int D, int W, double *P,
+                        int b, int h, int T, int H, int Hkv, int D, int W, double *P,
                         double *o, double *lse)
 {
+    int hk = h / (H / Hkv);  /* the key/value head of query head h */
     double scale = 1.0 / sqrt((double)D);
     for (int i = 0; i < T; ++i) {
         double *row = P + (size_t)i * T;
@@ -117,7 +123,7 @@ static void attend_head(const double *qh, const double *kh, const double *v,
         double m = -INFINITY;
         for (int j = 0; j < T; ++j) {
             if (!visible(i, j, W)) continue;
-            row[j] = dot(qi, kh + at4(b, j, h, 0, T, H, D), D) * scale;
+            row[j] = dot(qi, kh + at4(b, j, hk, 0, T, Hkv, D), D) * scale;
             if (row[j] > m) m = row[j];
         }
         double l = 0.0;
@@ -133,7 +139,7 @@ static void attend_head(const double *qh, const double *kh, const double *v,
         double *oi = o + at4(b, i, h, 0, T, H, D);
         for (int d = 0; d < D; ++d) {
             double acc = 0.0;
-            for (int j = 0; j < T; ++j) acc += row[j] * v[at4(b, j, h, d, T, H, D)];
+            for (int j = 0; j < T; ++j) acc += row[j] * v[at4(b, j, hk, d, T, Hkv, D)];
             oi[d] = acc;
         }
         if (lse) lse[((size_t)b * H + h) * T + i] = m + log(l);
@@ -143,21 +149,21 @@ static void attend_head(const double *qh, const double *kh, const double *v,
 /* Forward: o = softmax(qhat khat^T / sqrt(D) + mask) v; lse [B,H,T].  The
  * mask is causal, banded to the last W keys when W > 0. */
 int orc_attn_fwd(const double *q, const double *k, const double *v, const int *pos,
-                 int B, int T, int H, int D, double eps, double base, int flags, int W,
+                 int B, int T, int H, int Hkv, int D, double eps, double base, int flags, int W,
                  double *o, double *lse)
 {
-    size_t n = (size_t)B * T * H * D;
-    double *qh = malloc(n * sizeof(double)), *kh = malloc(n * sizeof(double));
+    size_t n = (size_t)B * T * H * D, nk = (size_t)B * T * Hkv * D;
+    double *qh = malloc(n * sizeof(double)), *kh = malloc(nk * sizeof(double));
     if (!qh || !kh) { free(qh); free(kh); return -1; }
     orc_norm_rope(q, pos, B, T, H, D, eps, base, flags, qh, NULL);
-    orc_norm_rope(k, pos, B, T, H, D, eps, base, flags, kh, NULL);
+    orc_norm_rope(k, pos, B, T, Hkv, D, eps, base, flags, kh, NULL);
     int err = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
         for (int h = 0; h < H; ++h) {
             double *P = malloc((size_t)T * T * sizeof(double));
             if (!P) { err = -1; continue; }
-            attend_head(qh, kh, v, b, h, T, H, D, W, P, o, lse);
+            attend_head(qh, kh, v, b, h, T, H, Hkv, D, W, P, o, lse);
             free(P);
         }
     free(qh);
@@ -192,61 +198,70 @@ static void norm_rope_backward(const double *x, const double *g, int p, int D,
  *   dqhat_i = sum_j dS_ij khat_j / sqrt(D),  dkhat_j = sum_i dS_ij qhat_i / sqrt(D)
  * then back through RoPE and RMSNorm to dq, dk. */
 int orc_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
-                 const int *pos, int B, int T, int H, int D, double eps, double base,
+                 const int *pos, int B, int T, int H, int Hkv, int D, double eps, double base,
                  int flags, int W, double *dq, double *dk, double *dv)
 {
-    size_t n = (size_t)B * T * H * D;
-    double *qh = malloc(n * sizeof(double)), *kh = malloc(n * sizeof(double));
+    size_t n = (size_t)B * T * H * D, nk = (size_t)B * T * Hkv * D;
+    int G = H / Hkv;
+    double *qh = malloc(n * sizeof(double)), *kh = malloc(nk * sizeof(double));
     double *o = malloc(n * sizeof(double));
-    double *dqh = calloc(n, sizeof(double)), *dkh = calloc(n, sizeof(double));
+    double *dqh = calloc(n, sizeof(double)), *dkh = calloc(nk, sizeof(double));
     if (!qh || !kh || !o || !dqh || !dkh) {
         free(qh); free(kh); free(o); free(dqh); free(dkh);
         return -1;
     }
     orc_norm_rope(q, pos, B, T, H, D, eps, base, flags, qh, NULL);
-    orc_norm_rope(k, pos, B, T, H, D, eps, base, flags, kh, NULL);
+    orc_norm_rope(k, pos, B, T, Hkv, D, eps, base, flags, kh, NULL);
+    memset(dv, 0, nk * sizeof(double));
     double scale = 1.0 / sqrt((double)D);
     int err = 0;
+    /* one key/value head per task; its group's query heads in turn, so the
+     * sums over the group into dk and dv need no synchronisation */
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
-        for (int h = 0; h < H; ++h) {
+        for (int hk = 0; hk < Hkv; ++hk) {
             double *P = malloc((size_t)T * T * sizeof(double));
             double *dS = malloc((size_t)T * T * sizeof(double));
             if (!P || !dS) { free(P); free(dS); err = -1; continue; }
-            attend_head(qh, kh, v, b, h, T, H, D, W, P, o, NULL);
-            for (int i = 0; i < T; ++i) {
-                const double *doi = dout + at4(b, i, h, 0, T, H, D);
-                double delta = dot(doi, o + at4(b, i, h, 0, T, H, D), D);
-                for (int j = 0; j < T; ++j) {
-                    double pij = P[(size_t)i * T + j];
-                    double dpij = visible(i, j, W) ? dot(doi, v + at4(b, j, h, 0, T, H, D), D) : 0.0;
-                    dS[(size_t)i * T + j] = pij * (dpij - delta);
+            for (int h = hk * G; h < (hk + 1) * G; ++h) {
+                attend_head(qh, kh, v, b, h, T, H, Hkv, D, W, P, o, NULL);
+                for (int i = 0; i < T; ++i) {
+                    const double *doi = dout + at4(b, i, h, 0, T, H, D);
+                    double delta = dot(doi, o + at4(b, i, h, 0, T, H, D), D);
+                    for (int j = 0; j < T; ++j) {
+                        double pij = P[(size_t)i * T + j];
+                        double dpij = visible(i, j, W) ? dot(doi, v + at4(b, j, hk, 0, T, Hkv, D), D) : 0.0;
+                        dS[(size_t)i * T + j] = pij * (dpij - delta);
+                    }
+                }
+                for (int j = 0; j < T; ++j)
+                    for (int d = 0; d < D; ++d) {
+                        double acc = 0.0;
+                        for (int i = j; i < T; ++i)
+                            acc += P[(size_t)i * T + j] * dout[at4(b, i, h, d, T, H, D)];
+                        dv[at4(b, j, hk, d, T, Hkv, D)] += acc;
+                    }
+                for (int i = 0; i < T; ++i)
+                    for (int d = 0; d < D; ++d) {
+                        double acc = 0.0;
+                        for (int j = 0; j <= i; ++j)
+                            acc += dS[(size_t)i * T + j] * kh[at4(b, j, hk, d, T, Hkv, D)];
+                        dqh[at4(b, i, h, d, T, H, D)] = acc * scale;
+                    }
+                for (int j = 0; j < T; ++j)
+                    for (int d = 0; d < D; ++d) {
+                        double acc = 0.0;
+                        for (int i = j; i < T; ++i)
+                            acc += dS[(size_t)i * T + j] * qh[at4(b, i, h, d, T, H, D)];
+                        dkh[at4(b, j, hk, d, T, Hkv, D)] += acc * scale;
+                    }
+                for (int t = 0; t < T; ++t) {
+                    size_t off = at4(b, t, h, 0, T, H, D);
+                    norm_rope_backward(q + off, dqh + off, position(pos, t), D, eps, base, flags, dq + off);
                 }
             }
-            for (int j = 0; j < T; ++j)
-                for (int d = 0; d < D; ++d) {
-                    double acc = 0.0;
-                    for (int i = j; i < T; ++i)
-                        acc += P[(size_t)i * T + j] * dout[at4(b, i, h, d, T, H, D)];
-                    dv[at4(b, j, h, d, T, H, D)] = acc;
-                }
-            for (int i = 0; i < T; ++i)
-                for (int d = 0; d < D; ++d) {
-                    double acc = 0.0;
-                    for (int j = 0; j <= i; ++j)
-                        acc += dS[(size_t)i * T + j] * kh[at4(b, j, h, d, T, H, D)];
-                    dqh[at4(b, i, h, d, T, H, D)] = acc * scale;
-                }
-            for (int j = 0; j < T; ++j)
-                for (int d = 0; d < D; ++d) {
-                    double acc = 0.0;
-                    for (int i = j; i < T; ++i)
-                        acc += dS[(size_t)i * T + j] * qh[at4(b, i, h, d, T, H, D)];
-                    dkh[at4(b, j, h, d, T, H, D)] = acc * scale;
-                }
             for (int t = 0; t < T; ++t) {
-                size_t off = at4(b, t, h, 0, T, H, D);
-                norm_rope_backward(q + off, dqh + off, position(pos, t), D, eps, base, flags, dq + off);
+                size_t off = at4(b, t, hk, 0, T, Hkv, D);
                 norm_rope_backward(k + off, dkh + off, position(pos, t), D, eps, base, flags, dk + off);
             }
             free(P);
@@ -261,11 +276,12 @@ int orc_attn_bwd(const double *q, const double *k, const double *v, const double
  * last W when W > 0).  Keys are given RAW: slot j is
  * normalised and rotated at position j here, exactly as a prefill over the
  * same raw keys would have stored it; the new token's raw key sits at slot p.
- * q [B,H,D]; k_raw, v [B,Tcap,H,D]; out [B,H,D]. */
+ * q [B,H,D]; k_raw, v [B,Tcap,Hkv,D]; out [B,H,D]. */
 int orc_attn_decode(const double *q, const double *k_raw, const double *v, const int *lens,
-                    int B, int H, int D, int Tcap, double eps, double base, int flags, int W,
+                    int B, int H, int Hkv, int D, int Tcap, double eps, double base, int flags, int W,
                     double *out)
 {
+    int G = H / Hkv;
     double scale = 1.0 / sqrt((double)D);
     int err = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic)
@@ -284,7 +300,7 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
             for (int j = 0; j < L; ++j) {
                 s[j] = -INFINITY;
                 if (!visible(L - 1, j, W)) continue;
-                const double *kj = k_raw + at4(b, j, h, 0, Tcap, H, D);
+                const double *kj = k_raw + at4(b, j, h / G, 0, Tcap, Hkv, D);
                 double rk = (flags & ORC_NORM) ? rms_of(kj, D, eps) : 1.0;
                 for (int d = 0; d < D; ++d) kh[d] = kj[d] / rk;
                 if (flags & ORC_ROPE) rotate(kh, j, D, base, +1);
@@ -299,7 +315,7 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
             double *oi = out + ((size_t)b * H + h) * D;
             for (int d = 0; d < D; ++d) {
                 double acc = 0.0;
-                for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h, d, Tcap, H, D)];
+                for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h / G, d, Tcap, Hkv, D)];
                 oi[d] = acc;
             }
             free(qh); free(kh); free(s);
