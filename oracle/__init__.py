@@ -56,7 +56,7 @@ def _load():
         lib.orc_attn_bwd.restype = ctypes.c_int
         lib.orc_attn_decode.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp]
         lib.orc_attn_decode.restype = ctypes.c_int
-        lib.orc_attn_prefill.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp, dp]
+        lib.orc_attn_prefill.argtypes = [dp, dp, dp, ip, i, i, i, i, i, i, d, d, i, i, dp, dp]
         lib.orc_attn_prefill.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -146,16 +146,17 @@ def attn_decode(q, k_raw, v, lens, eps=1e-6, base=10000.0, flags=METHOD, window=
 def attn_prefill(q, k_raw, v, start, eps=1e-6, base=10000.0, flags=METHOD, window=0):
     """Prefill of a chunk: (out [B,C,H,D], lse [B,H,C]) for the C new queries
     q [B,C,H,D] of stream b at positions start[b] .. start[b]+C-1, over raw
-    keys k_raw and values v [B,Tcap,H,D] (the chunk's own keys and values in
-    their slots)."""
+    keys k_raw and values v [B,Tcap,Hkv,D] (the chunk's own keys and values in
+    their slots; Hkv < H: grouped-query attention)."""
     q, k_raw, v = _f64(q), _f64(k_raw), _f64(v)
     B, C, H, D = q.shape
-    Tcap = k_raw.shape[1]
+    Tcap, Hkv = k_raw.shape[1], k_raw.shape[2]
+    _check_groups(H, Hkv, v.shape[2])
     start = np.ascontiguousarray(np.asarray(start, dtype=np.int32).reshape(B))
     out = np.empty((B, C, H, D), dtype=np.float64)
     lse = np.empty((B, H, C), dtype=np.float64)
     rc = _load().orc_attn_prefill(_dp(q), _dp(k_raw), _dp(v), start.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
-                                  B, C, H, D, Tcap, eps, base, flags, int(window), _dp(out), _dp(lse))
+                                  B, C, H, Hkv, D, Tcap, eps, base, flags, int(window), _dp(out), _dp(lse))
     if rc != 0:
         raise ValueError("oracle prefill: start + C outside [0, Tcap]")
     return out, lse

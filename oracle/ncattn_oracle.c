@@ -329,11 +329,14 @@ int orc_attn_decode(const double *q, const double *k_raw, const double *v, const
  * slot up to start[b] + C - 1 (the chunk's own keys in its slots): slot j is
  * normalised and rotated at position j, as the cache holds it.  This is
  * rows start[b] .. start[b] + C - 1 of the forward over the whole sequence.
- * q, out [B,C,H,D]; k_raw, v [B,Tcap,H,D]; lse [B,H,C] (may be NULL). */
+ * q, out [B,C,H,D]; k_raw, v [B,Tcap,Hkv,D] (query head h reads key/value
+ * head h / (H / Hkv)); lse [B,H,C] (may be NULL). */
 int orc_attn_prefill(const double *q, const double *k_raw, const double *v, const int *start,
-                     int B, int C, int H, int D, int Tcap, double eps, double base, int flags, int W,
+                     int B, int C, int H, int Hkv, int D, int Tcap, double eps, double base, int flags, int W,
                      double *out, double *lse)
 {
+    if (Hkv < 1 || H % Hkv) return -1;
+    const int G = H / Hkv;
     double scale = 1.0 / sqrt((double)D);
     int err = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic)
@@ -346,7 +349,7 @@ int orc_attn_prefill(const double *q, const double *k_raw, const double *v, cons
             double *kh = malloc((size_t)L * D * sizeof(double));
             double *s = malloc((size_t)L * sizeof(double));
             for (int j = 0; j < L; ++j) {
-                const double *kj = k_raw + at4(b, j, h, 0, Tcap, H, D);
+                const double *kj = k_raw + at4(b, j, h / G, 0, Tcap, Hkv, D);
                 double rk = (flags & ORC_NORM) ? rms_of(kj, D, eps) : 1.0;
                 for (int d = 0; d < D; ++d) kh[(size_t)j * D + d] = kj[d] / rk;
                 if (flags & ORC_ROPE) rotate(kh + (size_t)j * D, j, D, base, +1);
@@ -372,7 +375,7 @@ int orc_attn_prefill(const double *q, const double *k_raw, const double *v, cons
                 double *oi = out + at4(b, t, h, 0, C, H, D);
                 for (int d = 0; d < D; ++d) {
                     double acc = 0.0;
-                    for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h, d, Tcap, H, D)];
+                    for (int j = 0; j < L; ++j) acc += s[j] / l * v[at4(b, j, h / G, d, Tcap, Hkv, D)];
                     oi[d] = acc;
                 }
                 if (lse) lse[((size_t)b * H + h) * C + t] = m + log(l);

@@ -76,3 +76,24 @@ def test_gqa_decode_equals_repeated_cache():
 def test_gqa_rejects_heads_that_do_not_divide():
     with pytest.raises(ValueError):
         oracle.attn_fwd(_rand((1, 4, 5, 8), 1), _rand((1, 4, 2, 8), 2), _rand((1, 4, 2, 8), 3))
+
+
+@pytest.mark.parametrize("W", [0, 7])
+def test_gqa_prefill_equals_repeated_cache_and_forward_rows(W):
+    """A chunk with Hkv < H key/value heads: the MHA prefill over the heads
+    repeated per group, and rows start .. start+C-1 of the GQA forward over
+    the whole sequence."""
+    B, C, H, Hkv, D, Tcap = 2, 5, 6, 2, 16, 24
+    start = [0, 11]
+    q = _rand((B, C, H, D), 20)
+    k, v = _rand((B, Tcap, Hkv, D), 21), _rand((B, Tcap, Hkv, D), 22)
+    out, lse = oracle.attn_prefill(q, k, v, start, window=W)
+    out_r, lse_r = oracle.attn_prefill(q, _rep(k, H // Hkv), _rep(v, H // Hkv), start, window=W)
+    assert np.allclose(out, out_r, atol=1e-13) and np.allclose(lse, lse_r, atol=1e-13)
+    for b, s in enumerate(start):
+        T = s + C
+        qf = _rand((1, T, H, D), 23)
+        qf[0, s:] = q[b]
+        o_f, lse_f = oracle.attn_fwd(qf, k[b:b + 1, :T], v[b:b + 1, :T], window=W)
+        assert np.allclose(out[b], o_f[0, s:], atol=1e-12)
+        assert np.allclose(lse[b], lse_f[0, :, s:], atol=1e-12)
