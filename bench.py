@@ -287,8 +287,8 @@ def bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv
     eps, base = workloads.EPS, workloads.ROPE_BASE
 
     def step():
-        nc.nc_attn_fwd_sw(qd, kd, vd, None, out, lse, qh, kh, None, ws_f, eps, base, W, stream)
-        nc.nc_attn_bwd_sw(qd, kd, vd, None, out, lse, qh, kh, dod, dq, dk, dv, ws_b, eps, base, W, stream)
+        nc.nc_attn_fwd_ex(qd, kd, vd, None, out, lse, qh, kh, None, ws_f, eps, base, W, stream)
+        nc.nc_attn_bwd_ex(qd, kd, vd, None, out, lse, qh, kh, dod, dq, dk, dv, ws_b, eps, base, W, stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -388,7 +388,7 @@ def bench_decode(nc, dev, args, rank, window=0):
 
     def call():
         if window:
-            nc.nc_attn_decode_sw(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
+            nc.nc_attn_decode_ex(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
                                  workloads.ROPE_BASE, window, stream)
         else:
             nc.nc_attn_decode(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,

@@ -25,7 +25,7 @@ NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE, NC_OP_PREFILL = 0, 1, 2, 3,
 EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
             "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
             "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc",
-            "nc_attn_fwd_sw", "nc_attn_bwd_sw", "nc_attn_decode_sw", "nc_attn_prefill")
+            "nc_attn_fwd_ex", "nc_attn_bwd_ex", "nc_attn_decode_ex", "nc_attn_prefill")
 NC_ETOOLARGE = -5
 
 
@@ -69,13 +69,13 @@ def _load():
     L.nc_profile_read.restype = I
     L.nc_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, F, S]
     L.nc_attn_decode_noalloc.restype = I
-    L.nc_attn_fwd_sw.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
-    L.nc_attn_fwd_sw.restype = I
-    L.nc_attn_bwd_sw.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
-    L.nc_attn_bwd_sw.restype = I
-    L.nc_attn_decode_sw.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, S]
-    L.nc_attn_decode_sw.restype = I
-    L.nc_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, F, F, I, S]
+    L.nc_attn_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, I, S]
+    L.nc_attn_fwd_ex.restype = I
+    L.nc_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, I, S]
+    L.nc_attn_bwd_ex.restype = I
+    L.nc_attn_decode_ex.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, I, S]
+    L.nc_attn_decode_ex.restype = I
+    L.nc_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, F, F, I, I, S]
     L.nc_attn_prefill.restype = I
     return L
 
@@ -147,23 +147,43 @@ def nc_qk_norm_rope(x, pos, xhat, rstd, workspace, eps, rope_base, stream=None):
            "nc_qk_norm_rope")
 
 
+def _shape(t, name, shape):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _kv_heads(q, k):
+    """Key/value heads of a (q, k) pair: k.shape[2], which must divide H."""
+    H, Hkv = q.shape[2], k.shape[2]
+    if Hkv < 1 or H % Hkv:
+        raise ValueError(f"{Hkv} key/value heads do not divide {H} query heads")
+    return Hkv
+
+
 def _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace):
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         _bf16(t, n)
     _f16(qhat, "qhat"), _f16(khat, "khat")
     B, T, H, D = q.shape
+    Hkv = _kv_heads(q, k)
+    for n, t in (("k", k), ("v", v), ("khat", khat)):
+        _shape(t, n, (B, T, Hkv, D))
+    _shape(out, "out", q.shape), _shape(qhat, "qhat", q.shape)
     return (_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat), _ptr(khat), _ptr(rstd),
             _ptr(workspace), workspace.numel(), B, T, H, D)
 
 
 def nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, stream=None):
     args = _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace)
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("nc_attn_fwd takes H key/value heads; use nc_attn_fwd_ex for fewer")
     _check(lib.nc_attn_fwd(*args, eps, rope_base, _stream(stream)), "nc_attn_fwd")
 
 
-def nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, window, stream=None):
+def nc_attn_fwd_ex(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, eps, rope_base, window=0, stream=None):
+    """kv_heads is k.shape[2] (grouped-query attention when it is below H)."""
     args = _fwd_args(q, k, v, pos, out, lse, qhat, khat, rstd, workspace)
-    _check(lib.nc_attn_fwd_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_fwd_sw")
+    _check(lib.nc_attn_fwd_ex(*args, eps, rope_base, int(window), k.shape[2], _stream(stream)), "nc_attn_fwd_ex")
 
 
 def _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace):
@@ -172,6 +192,11 @@ def _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace):
         _bf16(t, n)
     _f16(qhat, "qhat"), _f16(khat, "khat")
     B, T, H, D = q.shape
+    Hkv = _kv_heads(q, k)
+    for n, t in (("k", k), ("v", v), ("khat", khat), ("dk", dk), ("dv", dv)):
+        _shape(t, n, (B, T, Hkv, D))
+    for n, t in (("out", out), ("qhat", qhat), ("dout", dout), ("dq", dq)):
+        _shape(t, n, q.shape)
     return (_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(qhat), _ptr(khat), _ptr(dout),
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, T, H, D)
 
@@ -179,33 +204,45 @@ def _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace):
 def nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base,
                 stream=None):
     args = _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace)
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("nc_attn_bwd takes H key/value heads; use nc_attn_bwd_ex for fewer")
     _check(lib.nc_attn_bwd(*args, eps, rope_base, _stream(stream)), "nc_attn_bwd")
 
 
-def nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base, window,
+def nc_attn_bwd_ex(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base, window=0,
                    stream=None):
+    """kv_heads is k.shape[2] (grouped-query attention when it is below H)."""
     args = _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace)
-    _check(lib.nc_attn_bwd_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_bwd_sw")
+    _check(lib.nc_attn_bwd_ex(*args, eps, rope_base, int(window), k.shape[2], _stream(stream)), "nc_attn_bwd_ex")
 
 
 def _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace):
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
         _bf16(t, n)
     _f16(kcache, "kcache")
-    B, Tcap, H, D = kcache.shape
+    B, Tcap, Hkv, D = kcache.shape
+    H = q.shape[1]
+    if H % Hkv:
+        raise ValueError(f"{Hkv} key/value heads do not divide {H} query heads")
+    _shape(q, "q", (B, H, D)), _shape(out, "out", (B, H, D)), _shape(vcache, "vcache", kcache.shape)
+    _shape(k_new, "k_new", (B, Hkv, D)), _shape(v_new, "v_new", (B, Hkv, D))
     return (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(lens), _ptr(out),
             _ptr(workspace), workspace.numel(), B, H, D, Tcap)
 
 
 def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, stream=None):
     args = _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace)
+    if kcache.shape[2] != q.shape[1]:
+        raise ValueError("nc_attn_decode takes H key/value heads; use nc_attn_decode_ex for fewer")
     _check(lib.nc_attn_decode(*args, eps, rope_base, _stream(stream)), "nc_attn_decode")
 
 
-def nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, window,
+def nc_attn_decode_ex(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, window=0,
                       stream=None):
+    """kv_heads is kcache.shape[2] (grouped-query attention when it is below H)."""
     args = _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace)
-    _check(lib.nc_attn_decode_sw(*args, eps, rope_base, int(window), _stream(stream)), "nc_attn_decode_sw")
+    _check(lib.nc_attn_decode_ex(*args, eps, rope_base, int(window), kcache.shape[2], _stream(stream)),
+           "nc_attn_decode_ex")
 
 
 def nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, workspace, eps, rope_base, window=0, stream=None):
@@ -214,9 +251,12 @@ def nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, workspace, eps, ro
     _f16(kcache, "kcache")
     B, C, H, D = q.shape
     Tcap = kcache.shape[1]
+    Hkv = _kv_heads(q, k)
+    _shape(k, "k", (B, C, Hkv, D)), _shape(v, "v", (B, C, Hkv, D)), _shape(out, "out", q.shape)
+    _shape(kcache, "kcache", (B, Tcap, Hkv, D)), _shape(vcache, "vcache", (B, Tcap, Hkv, D))
     _check(lib.nc_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(start), _ptr(kcache), _ptr(vcache), _ptr(out),
                                _ptr(lse), _ptr(workspace), workspace.numel(), B, C, H, D, Tcap, eps, rope_base,
-                               int(window), _stream(stream)), "nc_attn_prefill")
+                               int(window), Hkv, _stream(stream)), "nc_attn_prefill")
 
 
 def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
@@ -234,15 +274,16 @@ def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope
 # -------------------------------------------------------- allocating helpers --
 
 def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, stream=None, window=0):
-    """Returns (out, lse, qhat, khat).  window > 0: sliding-window mask."""
+    """Returns (out, lse, qhat, khat).  window > 0: sliding-window mask; k and
+    v with fewer heads than q: grouped-query attention."""
     B, T, H, D = q.shape
     out = torch.empty_like(q)
     qhat = torch.empty_like(q, dtype=torch.float16)
     khat = torch.empty_like(k, dtype=torch.float16)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     ws = workspace if workspace is not None else new_workspace(NC_OP_FWD, B, T, H, D, q.device)
-    if window:
-        nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, window, stream)
+    if window or k.shape[2] != H:
+        nc_attn_fwd_ex(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, window, stream)
     else:
         nc_attn_fwd(q, k, v, pos, out, lse, qhat, khat, None, ws, eps, rope_base, stream)
     return out, lse, qhat, khat
@@ -250,12 +291,12 @@ def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, str
 
 def attn_bwd(q, k, v, out, lse, qhat, khat, dout, pos=None, eps=1e-6, rope_base=10000.0,
              workspace=None, stream=None, window=0):
-    """Returns (dq, dk, dv).  window: as passed to attn_fwd."""
+    """Returns (dq, dk, dv) (dk, dv with k's heads).  window: as passed to attn_fwd."""
     B, T, H, D = q.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace if workspace is not None else new_workspace(NC_OP_BWD, B, T, H, D, q.device)
-    if window:
-        nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, window, stream)
+    if window or k.shape[2] != H:
+        nc_attn_bwd_ex(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, window, stream)
     else:
         nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, ws, eps, rope_base, stream)
     return dq, dk, dv
@@ -271,11 +312,12 @@ def qk_norm_rope(x, pos=None, eps=1e-6, rope_base=10000.0, stream=None):
 
 def attn_decode(q, kcache, vcache, lens, k_new=None, v_new=None, eps=1e-6, rope_base=10000.0,
                 workspace=None, stream=None, window=0):
-    B, Tcap, H, D = kcache.shape
+    B, Tcap, Hkv, D = kcache.shape
+    H = q.shape[1]
     out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
     ws = workspace if workspace is not None else new_workspace(NC_OP_DECODE, B, Tcap, H, D, q.device)
-    if window:
-        nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, window, stream)
+    if window or Hkv != H:
+        nc_attn_decode_ex(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, window, stream)
     else:
         nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, ws, eps, rope_base, stream)
     return out

@@ -213,14 +213,28 @@ int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base,
     return launch_status();
 }
 
+// qhat (H heads) and, when k is given, khat (Hkv heads).  rstd (optional):
+// the q rows' [B][T][H] followed by the k rows' [B][T][Hkv].  One launch
+// covers both when the head counts agree, else one launch per tensor.
 template <int D>
 int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_bf16* qh, nc_bf16* kh, float* rstd,
-                     int B, int T, int H, float eps, cudaStream_t s) {
+                     int B, int T, int H, int Hkv, float eps, cudaStream_t s) {
     const long long toks = static_cast<long long>(B) * T;
     ProfScope ps("qk_norm_rope", s);
-    nc::qk_norm_rope_kernel<D><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
-        reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, toks, T, H, eps);
+    if (!k || Hkv == H) {
+        nc::qk_norm_rope_kernel<D><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
+            reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, toks, T, H, eps);
+        return launch_status();
+    }
+    nc::qk_norm_rope_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q), nullptr, tab, reinterpret_cast<__half*>(qh), nullptr, rstd, toks,
+        T, H, eps);
+    int rc = launch_status();
+    if (rc) return rc;
+    nc::qk_norm_rope_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(k), nullptr, tab, reinterpret_cast<__half*>(kh), nullptr,
+        rstd ? rstd + toks * H : nullptr, toks, T, Hkv, eps);
     return launch_status();
 }
 
@@ -228,18 +242,27 @@ int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_b
 // there is none (window <= 0, or at least the sequence length).
 int window_eff(int window, int T) { return (window <= 0 || window >= T) ? (1 << 30) : window; }
 
+// Key/value heads as the kernels take them: kv_heads = 0 means H (plain
+// multi-head attention); otherwise it must divide H.  0 on a bad value.
+int kv_heads_of(int kv_heads, int H) {
+    if (kv_heads == 0) return H;
+    if (kv_heads < 0 || kv_heads > H || H % kv_heads != 0) return 0;
+    return kv_heads;
+}
+
 template <int D>
 int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
-             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, float eps, float base, int W,
-             cudaStream_t s) {
+             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, int Hkv, float eps, float base,
+             int W, cudaStream_t s) {
     float2* tab = reinterpret_cast<float2*>(ws);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    rc = launch_norm_rope<D>(q, k, tab, qhat, khat, rstd, B, T, H, eps, s);
+    rc = launch_norm_rope<D>(q, k, tab, qhat, khat, rstd, B, T, H, Hkv, eps, s);
     if (rc) return rc;
     CUtensorMap tq, tk, tv, to;
-    if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) || make_tmap(&tk, khat, B, T, H, D, nc::fwd::BN, kF16) ||
-        make_tmap(&tv, v, B, T, H, D, nc::fwd::BN) || make_tmap(&to, out, B, T, H, D, nc::fwd::BM))
+    if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) ||
+        make_tmap(&tk, khat, B, T, Hkv, D, nc::fwd::BN, kF16) || make_tmap(&tv, v, B, T, Hkv, D, nc::fwd::BN) ||
+        make_tmap(&to, out, B, T, H, D, nc::fwd::BM))
         return NC_EINVAL;
     const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
     const double scale = 1.0 / std::sqrt(double(D));
@@ -253,7 +276,7 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
-        float(mfix * log2e), float(mfix), W, nullptr, T);
+        float(mfix * log2e), float(mfix), W, nullptr, T, H / Hkv);
     return launch_status();
 }
 
@@ -262,8 +285,8 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
 // queries at their cache positions and the caches as keys and values.
 template <int D>
 int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* start, nc_bf16* kcache,
-                 nc_bf16* vcache, nc_bf16* out, float* lse, void* ws, int B, int C, int H, int Tcap, float eps,
-                 float base, int W, cudaStream_t s) {
+                 nc_bf16* vcache, nc_bf16* out, float* lse, void* ws, int B, int C, int H, int Hkv, int Tcap,
+                 float eps, float base, int W, cudaStream_t s) {
     nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
     for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
     __half* qhat = reinterpret_cast<__half*>(ws);
@@ -272,13 +295,14 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
         nc::prefill_norm_rope_kernel<D><<<tok_grid(static_cast<long long>(B) * C, D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
             reinterpret_cast<const __nv_bfloat16*>(v), start, qhat, reinterpret_cast<__half*>(kcache),
-            reinterpret_cast<__nv_bfloat16*>(vcache), B, C, H, Tcap, eps, th);
+            reinterpret_cast<__nv_bfloat16*>(vcache), B, C, H, Hkv, Tcap, eps, th);
     }
     int rc = launch_status();
     if (rc) return rc;
     CUtensorMap tq, tk, tv, to;
-    if (make_tmap(&tq, qhat, B, C, H, D, nc::fwd::BM, kF16) || make_tmap(&tk, kcache, B, Tcap, H, D, nc::fwd::BN, kF16) ||
-        make_tmap(&tv, vcache, B, Tcap, H, D, nc::fwd::BN) || make_tmap(&to, out, B, C, H, D, nc::fwd::BM))
+    if (make_tmap(&tq, qhat, B, C, H, D, nc::fwd::BM, kF16) ||
+        make_tmap(&tk, kcache, B, Tcap, Hkv, D, nc::fwd::BN, kF16) ||
+        make_tmap(&tv, vcache, B, Tcap, Hkv, D, nc::fwd::BN) || make_tmap(&to, out, B, C, H, D, nc::fwd::BM))
         return NC_EINVAL;
     const int n_qt = (C + nc::fwd::BM - 1) / nc::fwd::BM;
     const double scale = 1.0 / std::sqrt(double(D));
@@ -290,14 +314,15 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
     ProfScope ps("attn_prefill", s);
     nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, C, H, B, n_qt, tile_group(n_pairs, B * H), float(scale * log2e), float(mfix * log2e),
-        float(mfix), W, start, Tcap);
+        float(mfix), W, start, Tcap, H / Hkv);
     return launch_status();
 }
 
 template <int D>
 int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
              const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
-             nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, float eps, float base, int W, cudaStream_t s) {
+             nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, int Hkv, float eps, float base, int W,
+             cudaStream_t s) {
     const int Tpad = tpad_of(T);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
     float2* tab = reinterpret_cast<float2*>(w);
@@ -319,24 +344,27 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     }
     if ((rc = launch_status())) return rc;
     CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv;
-    if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, H, D, 128, kF16) ||
-        make_tmap(&tv, v, B, T, H, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
-        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, H, D, 128) || make_tab_tmap(&ttab, tab, T, D) ||
-        make_tmap(&tdq, dq, B, T, H, D, 128) || make_tmap(&tdk, dk, B, T, H, D, 128) ||
-        make_tmap(&tdv, dv, B, T, H, D, 128))
+    if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, Hkv, D, 128, kF16) ||
+        make_tmap(&tv, v, B, T, Hkv, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
+        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, Hkv, D, 128) ||
+        make_tab_tmap(&ttab, tab, T, D) || make_tmap(&tdq, dq, B, T, H, D, 128) ||
+        make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
+    const long long nblk_kv = n_t * B * Hkv;
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
     const double scale = 1.0 / std::sqrt(double(D));
+    const int G = H / Hkv;
     const int group = tile_group(static_cast<int>(n_t), B * H);
     {
-        // key side: dk, dv (one CTA per key tile, longest walks first)
+        // key side: dk, dv (one CTA per key tile of a key/value head, longest
+        // walks first; it walks the query blocks of all G heads that share it)
         ProfScope ps("attn_bwd_dkdv", s);
-        nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk), nc::bwd::NUM_THREADS,
+        nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk_kv), nc::bwd::NUM_THREADS,
                                            nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, T, H, B, Tpad, group,
-            float(scale), float(scale * 1.4426950408889634), eps, W);
+            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, T, H, B, Tpad,
+            tile_group(static_cast<int>(n_t), B * Hkv), float(scale), float(scale * 1.4426950408889634), eps, W, G);
     }
     if ((rc = launch_status())) return rc;
     {
@@ -346,7 +374,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
                                           nc::bwdq::Smem<D>::ALLOC, s>>>(
             tq, tk, tv, tdo, tqr, ttab, tdq, lse2, delta, gmax, T, H, B, Tpad, group, float(scale),
-            float(scale * 1.4426950408889634), eps, W);
+            float(scale * 1.4426950408889634), eps, W, G);
     }
     return launch_status();
 }
@@ -373,8 +401,8 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
 
 template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
-                const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Tcap, float eps, float base,
-                int W, cudaStream_t s) {
+                const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Hkv, int Tcap, float eps,
+                float base, int W, cudaStream_t s) {
     const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
     const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
     const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
@@ -386,7 +414,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
         reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2), W);
+        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2), W, H / Hkv);
     return launch_status();
 }
 
@@ -498,21 +526,23 @@ int nc_qk_norm_rope(const nc_bf16* x, const int32_t* pos, nc_bf16* xhat, float* 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float2* tab = reinterpret_cast<float2*>(workspace);
     if ((rc = launch_rope_table(tab, pos, T, D, rope_base, s))) return rc;
-    return D == 64 ? launch_norm_rope<64>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, eps, s)
-                   : launch_norm_rope<128>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, eps, s);
+    return D == 64 ? launch_norm_rope<64>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s)
+                   : launch_norm_rope<128>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s);
 }
 
 int nc_attn_fwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
                 float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
                 int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream) {
-    return nc_attn_fwd_sw(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, workspace_bytes, B, T, H, D, eps,
-                          rope_base, 0, stream);
+    return nc_attn_fwd_ex(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, workspace_bytes, B, T, H, D, eps,
+                          rope_base, 0, 0, stream);
 }
 
-int nc_attn_fwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
+int nc_attn_fwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
                    float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
-                   int B, int T, int H, int D, float eps, float rope_base, int window, nc_stream_t stream) {
+                   int B, int T, int H, int D, float eps, float rope_base, int window, int kv_heads,
+                   nc_stream_t stream) {
     if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
+    if (H > 0 && !kv_heads_of(kv_heads, H)) return NC_EINVAL;
     if (B == 0 || T == 0 || H == 0) return NC_OK;
     if (!q || !k || !v || !out || !lse || !qhat || !khat || !workspace) return NC_EINVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(qhat) || !aligned16(khat) ||
@@ -523,23 +553,27 @@ int nc_attn_fwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, T);
-    return D == 64 ? fwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, W, s)
-                   : fwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, eps, rope_base, W, s);
+    const int Hkv = kv_heads_of(kv_heads, H);
+    return D == 64 ? fwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, Hkv, eps, rope_base,
+                                  W, s)
+                   : fwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, B, T, H, Hkv, eps, rope_base,
+                                   W, s);
 }
 
 int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
                 const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
                 nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
                 float eps, float rope_base, nc_stream_t stream) {
-    return nc_attn_bwd_sw(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, workspace_bytes, B, T, H,
-                          D, eps, rope_base, 0, stream);
+    return nc_attn_bwd_ex(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, workspace_bytes, B, T, H,
+                          D, eps, rope_base, 0, 0, stream);
 }
 
-int nc_attn_bwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
+int nc_attn_bwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
                    const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
                    nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
-                   float eps, float rope_base, int window, nc_stream_t stream) {
+                   float eps, float rope_base, int window, int kv_heads, nc_stream_t stream) {
     if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
+    if (H > 0 && !kv_heads_of(kv_heads, H)) return NC_EINVAL;
     if (B == 0 || T == 0 || H == 0) return NC_OK;
     if (!q || !k || !v || !out || !lse || !qhat || !khat || !dout || !dq || !dk || !dv || !workspace)
         return NC_EINVAL;
@@ -552,23 +586,26 @@ int nc_attn_bwd_sw(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, T);
-    return D == 64 ? bwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
+    const int Hkv = kv_heads_of(kv_heads, H);
+    return D == 64 ? bwd_impl<64>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, Hkv, eps,
                                   rope_base, W, s)
-                   : bwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, eps,
+                   : bwd_impl<128>(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, B, T, H, Hkv, eps,
                                    rope_base, W, s);
 }
 
 int nc_attn_decode(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                    const int32_t* lens, nc_bf16* out, void* workspace, size_t workspace_bytes, int B, int H, int D,
                    int Tcap, float eps, float rope_base, nc_stream_t stream) {
-    return nc_attn_decode_sw(q, k_new, v_new, kcache, vcache, lens, out, workspace, workspace_bytes, B, H, D, Tcap,
-                             eps, rope_base, 0, stream);
+    return nc_attn_decode_ex(q, k_new, v_new, kcache, vcache, lens, out, workspace, workspace_bytes, B, H, D, Tcap,
+                             eps, rope_base, 0, 0, stream);
 }
 
-int nc_attn_decode_sw(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache,
+int nc_attn_decode_ex(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache,
                       nc_bf16* vcache, const int32_t* lens, nc_bf16* out, void* workspace, size_t workspace_bytes,
-                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream) {
+                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
+                      nc_stream_t stream) {
     if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
+    if (H > 0 && !kv_heads_of(kv_heads, H)) return NC_EINVAL;
     if (B == 0 || H == 0 || Tcap == 0) return NC_OK;
     if (!q || !kcache || !vcache || !lens || !out || !workspace) return NC_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr)) return NC_EINVAL;
@@ -583,16 +620,20 @@ int nc_attn_decode_sw(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_n
     decode_ws_layout(B, H, D, Tcap, &ws, workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, Tcap);
-    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W, s)
-                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W,
-                                      s);
+    const int Hkv = kv_heads_of(kv_heads, H);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Hkv, Tcap, eps, rope_base,
+                                     W, s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Hkv, Tcap, eps,
+                                      rope_base, W, s);
 }
 
 int nc_attn_prefill(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* start, nc_bf16* kcache,
                     nc_bf16* vcache, nc_bf16* out, float* lse, void* workspace, size_t workspace_bytes, int B, int C,
-                    int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream) {
+                    int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
+                    nc_stream_t stream) {
     if (!shape_ok(B, C, H, D) || !params_ok(eps, rope_base) || window < 0 || Tcap < C || Tcap > (1 << 24))
         return NC_EINVAL;
+    if (H > 0 && !kv_heads_of(kv_heads, H)) return NC_EINVAL;
     if (B == 0 || C == 0 || H == 0) return NC_OK;
     if (!q || !k || !v || !start || !kcache || !vcache || !out || !workspace) return NC_EINVAL;
     const void* b16[] = {q, k, v, kcache, vcache, out};
@@ -605,9 +646,10 @@ int nc_attn_prefill(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const 
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, Tcap);
-    return D == 64 ? prefill_impl<64>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Tcap, eps,
+    const int Hkv = kv_heads_of(kv_heads, H);
+    return D == 64 ? prefill_impl<64>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Hkv, Tcap, eps,
                                       rope_base, W, s)
-                   : prefill_impl<128>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Tcap, eps,
+                   : prefill_impl<128>(q, k, v, start, kcache, vcache, out, lse, workspace, B, C, H, Hkv, Tcap, eps,
                                        rope_base, W, s);
 }
 
@@ -682,9 +724,10 @@ int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16
     if (cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), s) != cudaSuccess)
         return launch_status();
     const int W = window_eff(0, Tcap);
-    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W, s)
-                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Tcap, eps, rope_base, W,
-                                      s);
+    return D == 64 ? decode_impl<64>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, H, Tcap, eps, rope_base, W,
+                                     s)
+                   : decode_impl<128>(q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, H, Tcap, eps, rope_base,
+                                      W, s);
 }
 
 }  // extern "C"

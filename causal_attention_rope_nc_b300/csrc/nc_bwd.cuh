@@ -3,8 +3,9 @@
 // (nc_bwd_dq.cuh), so that no gradient is accumulated through global
 // atomics: each output element is owned by exactly one CTA.
 //
-// One CTA owns one 128-key tile j of one (batch, head) and walks the
-// 128-query blocks i >= j that can see it (all of them, or with a sliding
+// One CTA owns one 128-key tile j of one (batch, key/value head) and walks,
+// for each of the G query heads that share that key/value head (grouped-query
+// attention; G = 1 without it), the 128-query blocks i >= j that can see it (all of them, or with a sliding
 // window W -- query q sees key k when 0 <= q - k < W -- those up to the block
 // of the last query within W of the tile's last key).  Everything is computed transposed (keys on the
 // TMEM lanes):
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                          const float* __restrict__ lse2, const float* __restrict__ delta,
                          unsigned int* __restrict__ gmax, int T, int H, int B, int Tpad, int group, float scale,
-                         float scale_log2, float eps, int W) {
+                         float scale_log2, float eps, int W, int G) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
     constexpr uint32_t TM_DK = TM_DV + D;
@@ -132,20 +133,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grouped (b, h) order, longest walks (key tile 0) first in a group
+    // grouped (b, key/value head) order, longest walks (key tile 0) first in a group
     const int nqb = (T + BM - 1) / BM;
-    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, nqb, group);
+    const int Hkv = H / G;
+    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * Hkv, nqb, group);
     const int kt = tc.rank;
-    const int b = tc.bh / H, h = tc.bh % H;
+    const int b = tc.bh / Hkv, hk = tc.bh % Hkv;
     const int qb0 = kt;  // BM == BN: the diagonal query block
     const int qb_last = min(nqb - 1, (kt * BN + BN - 1 + W - 1) / BM);  // W >= 2^30 means no window
-    const int n_it = qb_last - qb0 + 1;
+    const int n_it = qb_last - qb0 + 1;  // query blocks per query head
+    const int n_tot = G * n_it;          // blocks of the whole walk: head hk*G + itf / n_it, block itf % n_it
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
-    const long long bh = static_cast<long long>(b) * H + h;
-    const int sp = n_it & 1;             // query stage the last block does not use
-    const int st_last = (n_it - 1) & 1;  // the last block's query stage
+    const int sp = n_tot & 1;             // query stage the last block does not use
+    const int st_last = (n_tot - 1) & 1;  // the last block's query stage
 
     if (threadIdx.x == 0) {
         mbar_init(bar(KV_FULL), 1);
@@ -178,13 +180,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int issued[2] = {0, 0};
             mbar_expect_tx(bar(KV_FULL), 2 * S::KBYTES);
             for (int c = 0; c < NC; ++c) {
-                tma_load_4d(sb + S::OFF_K + c * (BN * 128), &tm_k, c * 64, h, kt * BN, b, bar(KV_FULL));
-                tma_load_4d(sb + S::OFF_V + c * (BN * 128), &tm_v, c * 64, h, kt * BN, b, bar(KV_FULL));
+                tma_load_4d(sb + S::OFF_K + c * (BN * 128), &tm_k, c * 64, hk, kt * BN, b, bar(KV_FULL));
+                tma_load_4d(sb + S::OFF_V + c * (BN * 128), &tm_v, c * 64, hk, kt * BN, b, bar(KV_FULL));
             }
-            for (int it = 0; it < n_it; ++it) {
-                const int st = it & 1, use = it >> 1;
-                if (it >= 2 && !mbar_wait(bar(QE + st), (use - 1) & 1, 0x111)) break;
-                const int q0 = (qb0 + it) * BM;
+            for (int itf = 0; itf < n_tot; ++itf) {
+                const int st = itf & 1, use = itf >> 1;
+                if (itf >= 2 && !mbar_wait(bar(QE + st), (use - 1) & 1, 0x111)) break;
+                const int h = hk * G + itf / n_it;  // query head of this block
+                const long long bh = static_cast<long long>(b) * H + h;
+                const int q0 = (qb0 + itf % n_it) * BM;
                 mbar_expect_tx(bar(QF + st), 2 * S::QBYTES + 2 * BM * 4);
                 for (int c = 0; c < NC; ++c) {
                     tma_load_4d(sb + S::OFF_Q + st * S::QBYTES + c * (BM * 128), &tm_q, c * 64, h, q0, b,
@@ -197,10 +201,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++issued[st];
             }
             // dk epilogue tiles, each as soon as its space is free: the RoPE
-            // table rows over stage sp (free once block n_it-2 is done), the
+            // table rows over stage sp (free once block n_tot-2 is done), the
             // raw k rows over the khat tile
             mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
-            bool epi = n_it < 2 || mbar_wait(bar(QE + sp), ((n_it - 2) >> 1) & 1, 0x117);
+            bool epi = n_tot < 2 || mbar_wait(bar(QE + sp), ((n_tot - 2) >> 1) & 1, 0x117);
             if (epi) {
                 for (int c = 0; c < D / 32; ++c) {
                     const uint32_t dst = c < NC ? S::OFF_Q + sp * S::QBYTES + c * (BN * 128)
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             epi = epi && mbar_wait(bar(KV_FREE), 0, 0x118);
             if (epi) {
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + c * (BN * 128), &tm_kraw, c * 64, h, kt * BN, b, bar(EPI_FULL));
+                    tma_load_4d(sb + S::OFF_K + c * (BN * 128), &tm_kraw, c * 64, hk, kt * BN, b, bar(EPI_FULL));
             }
             // never leave the CTA with a bulk copy still in flight
             mbar_wait(bar(KV_FULL), 0, 0x112);
@@ -254,11 +258,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 issue_s(0);
                 issue_dp(0);
-                if (n_it == 1) mma_commit(bar(KV_FREE));
+                if (n_tot == 1) mma_commit(bar(KV_FREE));
             }
-            for (int it = 0; ok && it < n_it; ++it) {
+            for (int it = 0; ok && it < n_tot; ++it) {
                 const int st = it & 1;
-                const bool more = it + 1 < n_it;
+                const bool more = it + 1 < n_tot;
                 // dV += P^T dout, then S^T of the next block over P^T
                 if (!mbar_wait(bar(P_FULL), it & 1, 0x213)) { ok = false; break; }
                 tc_fence_after();
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (more) {
                     issue_dp(st ^ 1);
-                    if (it + 2 == n_it) mma_commit(bar(KV_FREE));  // that was the last dP
+                    if (it + 2 == n_tot) mma_commit(bar(KV_FREE));  // that was the last dP
                 }
             }
             if (ok) mma_commit(bar(DKV_FULL));
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (threadIdx.x == 0) atomicMax(gmax + 2, __float_as_uint(vmax));  // non-negative: bit order
         const float alpha = ds_scale_for(__uint_as_float(gmax[0]) * (vmax + __uint_as_float(gmax[1])) * 1.0625f);
         const uint32_t ts = tmem + lane_base + TM_S, tdp = tmem + lane_base + TM_DP;
-        for (int it = 0; ok && it < n_it; ++it) {
+        for (int it = 0; ok && it < n_tot; ++it) {
             const int st = it & 1, use = it >> 1;
             if (!mbar_wait_warp(bar(QF + st), use & 1, 0x311)) { ok = false; break; }
             if (!mbar_wait_warp(bar(S_FULL), it & 1, 0x312)) { ok = false; break; }
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // columns.  Blocks with masked entries (the diagonal one: query <
             // key; at the far end of a window: query - key >= W) take their
             // own copy of the loop, so the other blocks pay nothing for the mask.
-            const int qb = qb0 + it;
+            const int qb = qb0 + it % n_it;  // query block of this step
             const int d0 = (qb - kt) * BM + cbase - row;  // query - key at this thread's first column
             uint32_t pk[32];
             {
@@ -426,7 +430,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const bool epi_dk = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), 0, 0x316));
         if (epi && threadIdx.x == 0) {
-            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dv, sb + S::OFF_V + c * (BN * 128), c * 64, h, kt * BN, b);
+            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dv, sb + S::OFF_V + c * (BN * 128), c * 64, hk, kt * BN, b);
             bulk_commit();
         }
         // dk = RMSNorm^T(RoPE^T(dKhat * scale / alpha))
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (threadIdx.x == 0) {
             if (epi_dk) {
                 for (int c = 0; c < NC; ++c)
-                    tma_store_4d(&tm_dk, smem_u32(dk_stage) + c * (BN * 128), c * 64, h, kt * BN, b);
+                    tma_store_4d(&tm_dk, smem_u32(dk_stage) + c * (BN * 128), c * 64, hk, kt * BN, b);
                 bulk_commit();
             }
             bulk_wait_read_all();  // the staged tiles stay valid until the stores have read them

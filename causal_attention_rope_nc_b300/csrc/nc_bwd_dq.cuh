@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
                        const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
                        const float* __restrict__ delta, const unsigned int* __restrict__ gmax, int T, int H, int B,
-                       int Tpad, int group, float scale, float scale_log2, float eps, int W) {
+                       int Tpad, int group, float scale, float scale_log2, float eps, int W, int G) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
     extern __shared__ uint8_t smem_raw[];
@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_qt, group);
     const int qt = n_qt - 1 - tc.rank;
     const int b = tc.bh / H, h = tc.bh % H;
+    const int hk = h / G;  // key/value head (grouped-query attention; G = 1: hk = h)
     const int kt_lo = max(0, qt * BM - W + 1) / BN;  // first visible key tile (W >= 2^30: none cut)
     const int n_kv = qt - kt_lo + 1;                  // BM == BN: key tiles kt_lo..qt
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
@@ -175,13 +176,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (j >= KSTAGES && !mbar_wait(bar(K_EMPTY + ks), (j / KSTAGES - 1) & 1, 0x121)) break;
                 mbar_expect_tx(bar(K_FULL + ks), S::TBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + ks * S::TBYTES + c * (BN * 128), &tm_k, c * 64, h, (kt_lo + j) * BN, b,
+                    tma_load_4d(sb + S::OFF_K + ks * S::TBYTES + c * (BN * 128), &tm_k, c * 64, hk, (kt_lo + j) * BN, b,
                                 bar(K_FULL + ks));
                 ++issued_k[ks];
                 if (j >= 2 && !mbar_wait(bar(V_EMPTY + vs), ((j >> 1) - 1) & 1, 0x122)) break;
                 mbar_expect_tx(bar(V_FULL + vs), S::TBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + vs * S::TBYTES + c * (BN * 128), &tm_v, c * 64, h, (kt_lo + j) * BN, b,
+                    tma_load_4d(sb + S::OFF_V + vs * S::TBYTES + c * (BN * 128), &tm_v, c * 64, hk, (kt_lo + j) * BN, b,
                                 bar(V_FULL + vs));
                 ++issued_v[vs];
             }

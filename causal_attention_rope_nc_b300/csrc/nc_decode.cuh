@@ -1,7 +1,9 @@
 // Single-token decode over a KV cache (memory bound, CUDA cores).
 //
-// Cache layout [B][Tcap][H][D]: one cache slot holds all H heads of one
-// position contiguously (2*H*D bytes).  Keys are cached normalised and
+// Cache layout [B][Tcap][Hkv][D]: one cache slot holds all Hkv key/value
+// heads of one position contiguously (2*Hkv*D bytes).  Query head h reads
+// key/value head h / G (grouped-query attention, G = H / Hkv; G = 1 is plain
+// multi-head attention).  Keys are cached normalised and
 // rotated, in IEEE fp16 (elements bounded by sqrt(D)); values raw, in bf16.
 //
 // Split over the cache: one CTA per (chunk c of CH slots, stream b), grid
@@ -33,7 +35,10 @@
 // The new token (position p = lens[b] - 1): the CTA that owns the last chunk
 // normalises and rotates k_new, writes it (fp16) and v_new into slot p, and
 // reads them back through the cache like every other slot, so the score at p
-// uses exactly the stored fp16 key.
+// uses exactly the stored fp16 key.  With G = 1 each warp writes the slot of
+// its own head; with G > 1 the CTA writes every key/value head of the slot
+// first, and the G warps of a group then read the same rows (cached loads
+// instead of evict-first ones, so the group's later readers hit in L2).
 #pragma once
 
 #include "nc_common.cuh"
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
     unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
-    const __grid_constant__ Theta theta, float scale_log2, int W) {
+    const __grid_constant__ Theta theta, float scale_log2, int W, int G) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
     __shared__ float2 s_cs[D / 2];  // rotation at the new token's position
@@ -92,9 +97,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const int g = lane / LPS;    // slot of this lane group within a warp load
     const int sub = lane % LPS;  // 16-byte piece of the row
     const int e0 = sub * 8;      // first head-dim element of this lane
-    const long long slot_elems = static_cast<long long>(H) * D;
-    auto head_base = [&](int h) -> long long {
-        return static_cast<long long>(b) * Tcap * slot_elems + static_cast<long long>(h) * D + e0;
+    const int Hkv = H / G;
+    const long long slot_elems = static_cast<long long>(Hkv) * D;
+    auto head_base = [&](int h) -> long long {  // query head h -> its key/value head's row in slot 0
+        return static_cast<long long>(b) * Tcap * slot_elems + static_cast<long long>(h / G) * D + e0;
     };
 
     // RoPE(RMSNorm(x)) of row x (D bf16) at the new token's position: the 8
@@ -127,8 +133,13 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             const int s = j + g + SPW * u;
             if (s < s1) {
                 const long long at = base + static_cast<long long>(s) * slot_elems;
-                kr[u] = ld_stream16(kcache + at);
-                vr[u] = ld_stream16(vcache + at);
+                if (G == 1) {
+                    kr[u] = ld_stream16(kcache + at);
+                    vr[u] = ld_stream16(vcache + at);
+                } else {
+                    kr[u] = __ldcg(reinterpret_cast<const uint4*>(kcache + at));
+                    vr[u] = __ldcg(reinterpret_cast<const uint4*>(vcache + at));
+                }
             } else {
                 kr[u] = make_uint4(0u, 0u, 0u, 0u);
                 vr[u] = kr[u];
@@ -142,6 +153,21 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     if (!own_new && warp < H) load_batch(head_base(warp), s0, ka, va);
     for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
     __syncthreads();
+    // RoPE(RMSNorm(k_new)) (fp16) and v_new into slot p, key/value head hk
+    auto store_new = [&](int hk) {
+        const long long row = (static_cast<long long>(b) * Hkv + hk) * D;
+        float kv[8];
+        norm_rope8(k_new + row, kv);
+        if (g == 0) {
+            const long long at = (static_cast<long long>(b) * Tcap + p_new) * slot_elems + static_cast<long long>(hk) * D + e0;
+            *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_f16(kv);
+            *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
+        }
+    };
+    if (own_new && G > 1) {  // uniform over the CTA
+        for (int hk = warp; hk < Hkv; hk += NW) store_new(hk);
+        __syncthreads();  // every head of the slot is stored before any warp reads it
+    }
 
     for (int h = warp; h < H; h += NW) {
         const long long row_bh = (static_cast<long long>(b) * H + h) * D;
@@ -150,14 +176,8 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale_log2;
         const long long base = head_base(h);
-        if (own_new) {
-            float kv[8];
-            norm_rope8(k_new + row_bh, kv);
-            if (g == 0) {
-                const long long at = base + static_cast<long long>(p_new) * slot_elems;
-                *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_f16(kv);
-                *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row_bh + e0);
-            }
+        if (own_new && G == 1) {
+            store_new(h);
             __syncwarp();  // orders the slot's stores before the warp's loads below
         }
         if (own_new || h != warp) load_batch(base, s0, ka, va);

@@ -1,7 +1,8 @@
 // Causal attention forward on sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // One CTA computes two consecutive 128-row query tiles (2p and 2p+1) of one
-// (batch, head); both share every K/V tile it streams.  Query row r of stream
+// (batch, head); both share every K/V tile it streams (those of key/value
+// head h / G: grouped-query attention shares one among G query heads).  Query row r of stream
 // b sits at position qoff[b] + r (qoff == nullptr: position r) among Tk key
 // positions: a chunk of new tokens attending over a KV cache, or (offset 0,
 // Tk = T) the whole sequence.  With a sliding window
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
                     float* __restrict__ lse, int T, int H, int B, int n_qt, int group, float scale_log2,
-                    float mfix_log2, float mfix, int W, const int* __restrict__ qoff, int Tk) {
+                    float mfix_log2, float mfix, int W, const int* __restrict__ qoff, int Tk, int G) {
     using S = Smem<D>;
     constexpr int NC = D / 64;  // 64-column (128-byte) swizzle spans per row
     extern __shared__ uint8_t smem_raw[];
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_pairs, group);
     const int qt0 = 2 * (n_pairs - 1 - tc.rank);
     const int b = tc.bh / H, h = tc.bh % H;
+    const int hk = h / G;  // key/value head (grouped-query attention; G = 1: hk = h)
     const bool has1 = qt0 + 1 < n_qt;
     const int qpos0 = qoff ? qoff[b] : 0;  // position of query row 0
     if (qpos0 < 0 || qpos0 + T > Tk) {     // uniform over the CTA: nothing has started yet
@@ -161,13 +163,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (j >= 2 && !mbar_wait(bar(K_EMPTY + st), (use - 1) & 1, 0x101)) break;
                 mbar_expect_tx(bar(K_FULL + st), S::KBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + st * S::KBYTES + c * (BN * 128), &tm_k, c * 64, h, (lo0 + j) * BN, b,
+                    tma_load_4d(sb + S::OFF_K + st * S::KBYTES + c * (BN * 128), &tm_k, c * 64, hk, (lo0 + j) * BN, b,
                                 bar(K_FULL + st));
                 ++issued_k[st];
                 if (j >= 2 && !mbar_wait(bar(V_EMPTY + st), (use - 1) & 1, 0x102)) break;
                 mbar_expect_tx(bar(V_FULL + st), S::KBYTES);
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + st * S::KBYTES + c * (BN * 128), &tm_v, c * 64, h, (lo0 + j) * BN, b,
+                    tma_load_4d(sb + S::OFF_V + st * S::KBYTES + c * (BN * 128), &tm_v, c * 64, hk, (lo0 + j) * BN, b,
                                 bar(V_FULL + st));
                 ++issued_v[st];
             }

@@ -128,12 +128,12 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
 
 // --------------------------------------------- chunk prefill prologue ----
 // For the C new tokens of stream b (positions start[b] + t, t < C):
-//   qhat[b][t][h] = RoPE(RMSNorm(q[b][t][h]), start[b] + t)    (fp16, workspace)
-//   kcache[b][start[b] + t][h] = RoPE(RMSNorm(k[b][t][h]), start[b] + t)  (fp16)
-//   vcache[b][start[b] + t][h] = v[b][t][h]                     (bf16 copy)
+//   qhat[b][t][h] = RoPE(RMSNorm(q[b][t][h]), start[b] + t)    (fp16, workspace; h < H)
+//   kcache[b][start[b] + t][g] = RoPE(RMSNorm(k[b][t][g]), start[b] + t)  (fp16; g < Hkv)
+//   vcache[b][start[b] + t][g] = v[b][t][g]                     (bf16 copy)
 // One group of D/8 lanes owns one token of one stream: it forms the token's
 // rotation (cos, sin of its 8 pair indices) from the frequencies and walks
-// the token's H heads.  A stream whose chunk does not fit its cache
+// the token's H query heads and Hkv key/value heads.  A stream whose chunk does not fit its cache
 // (start < 0 or start + C > Tcap) is skipped and recorded (status 2).
 template <int D>
 __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
@@ -141,8 +141,9 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
                                                                 const __nv_bfloat16* __restrict__ v,
                                                                 const int* __restrict__ start,
                                                                 __half* __restrict__ qhat, __half* kcache,
-                                                                __nv_bfloat16* vcache, int B, int C, int H, int Tcap,
-                                                                float eps, const __grid_constant__ Theta theta) {
+                                                                __nv_bfloat16* vcache, int B, int C, int H, int Hkv,
+                                                                int Tcap, float eps,
+                                                                const __grid_constant__ Theta theta) {
     using L = RowLanes<D>;
     const int sub = threadIdx.x % L::LPR;
     const long long groups = blockDim.x / L::LPR;
@@ -170,14 +171,16 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
             c[e] = r.x;
             sn[e] = r.y;
         }
-        const long long tok_in = (static_cast<long long>(b) * C + t) * H * D + sub * 8;
-        const long long slot = (static_cast<long long>(b) * Tcap + p) * H * D + sub * 8;
+        const long long tok_q = (static_cast<long long>(b) * C + t) * H * D + sub * 8;
+        const long long tok_kv = (static_cast<long long>(b) * C + t) * Hkv * D + sub * 8;
+        const long long slot = (static_cast<long long>(b) * Tcap + p) * Hkv * D + sub * 8;
         for (int h = 0; h < H; ++h) {
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {  // q, then k
+            for (int which = 0; which < 2; ++which) {  // q, then k (key/value heads: the first Hkv)
+                if (which && h >= Hkv) break;  // uniform
                 float x[8];
                 if (valid)
-                    bf16x8_to_f32(*reinterpret_cast<const uint4*>((which ? k : q) + tok_in + h * D), x);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(which ? k + tok_kv + h * D : q + tok_q + h * D), x);
                 else
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = 0.f;
@@ -194,13 +197,13 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
                 if (valid) {
-                    __half* dst = which ? kcache + slot + h * D : qhat + tok_in + h * D;
+                    __half* dst = which ? kcache + slot + h * D : qhat + tok_q + h * D;
                     *reinterpret_cast<uint4*>(dst) = f32x8_to_f16(o);
                 }
             }
-            if (valid)
+            if (valid && h < Hkv)
                 *reinterpret_cast<uint4*>(vcache + slot + h * D) =
-                    *reinterpret_cast<const uint4*>(v + tok_in + h * D);
+                    *reinterpret_cast<const uint4*>(v + tok_kv + h * D);
         }
     }
 }

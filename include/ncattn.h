@@ -154,9 +154,12 @@ int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new,
                    nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
                    int B, int H, int D, int Tcap, float eps, float rope_base, nc_stream_t stream);
 
-/* Sliding-window variants of the three calls above (same arguments, plus
- * `window`).  Query i sees key j exactly when 0 <= i - j < window: the
- * window's W most recent positions, its own included.  The pages run most
+/* Sliding-window and grouped-query variants of the three calls above (same
+ * arguments, plus `window` and `kv_heads`; window = kv_heads = 0 gives
+ * exactly the calls above).
+ *
+ * window: query i sees key j exactly when 0 <= i - j < window: the
+ * window's most recent positions, its own included.  The pages run most
  * layers with a short window of a quarter of the context (ai.flicky.cc,
  * "nanochat: свой ChatGPT от токенизатора до чата", section "Модель: что
  * изменилось со времён GPT-2", window-pattern bullet: pattern SSSL, the last
@@ -165,28 +168,44 @@ int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new,
  * causal mask, exactly the calls above; window < 0 is NC_EINVAL.  Key tiles
  * that no query of a tile can see are skipped, so the work shrinks with the
  * window.  For decode, position p = lens[b] - 1 attends slots
- * max(0, p - window + 1) .. p. */
-int nc_attn_fwd_sw(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
+ * max(0, p - window + 1) .. p.
+ *
+ * kv_heads: the number Hkv of key/value heads (grouped-query attention, an
+ * option of the pages' model: ai.flicky.cc, "nanochat: свой ChatGPT от
+ * токенизатора до чата", section "Модель: что изменилось со времён GPT-2",
+ * GQA bullet).  0 means H (plain multi-head attention); otherwise it must
+ * divide H, else NC_EINVAL.  Query head h uses key/value head h / (H / Hkv):
+ * consecutive query heads share one.  Every key-side tensor then has Hkv
+ * heads instead of H: k, v, khat, dk, dv [B][T][Hkv][D], k_new and v_new
+ * [B][Hkv][D], kcache and vcache [B][Tcap][Hkv][D]; rstd is the q rows'
+ * [B][T][H] followed by the k rows' [B][T][Hkv].  dk and dv sum the
+ * gradients of the query heads of each group (the key-side kernel walks all
+ * of them for its key tile, still without atomics).  Workspace sizes are
+ * those of the plain calls with H query heads. */
+int nc_attn_fwd_ex(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
                    float *lse, nc_f16 *qhat, nc_f16 *khat, float *rstd, void *workspace, size_t workspace_bytes,
-                   int B, int T, int H, int D, float eps, float rope_base, int window, nc_stream_t stream);
-int nc_attn_bwd_sw(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
+                   int B, int T, int H, int D, float eps, float rope_base, int window, int kv_heads,
+                   nc_stream_t stream);
+int nc_attn_bwd_ex(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
                    const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
                    nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
-                   float eps, float rope_base, int window, nc_stream_t stream);
-int nc_attn_decode_sw(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+                   float eps, float rope_base, int window, int kv_heads, nc_stream_t stream);
+int nc_attn_decode_ex(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
                       nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
-                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream);
+                      int B, int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
+                      nc_stream_t stream);
 
 /* Chunk prefill into a KV cache.  Stream b appends C new tokens at
  * positions start[b] .. start[b] + C - 1 (start: [B] int32, device): their
- * raw q, k, v [B][C][H][D] are normalised and rotated at those positions;
+ * raw q [B][C][H][D] and k, v [B][C][Hkv][D] are normalised and rotated
+ * at those positions (Hkv = kv_heads, 0 meaning H, as in the *_ex calls);
  * the keys (fp16, normalised and rotated, as nc_qk_norm_rope writes them)
  * and the values go into slots start[b] .. start[b] + C - 1 of kcache /
- * vcache [B][Tcap][H][D]; each new query attends causally over slots
+ * vcache [B][Tcap][Hkv][D]; each new query attends causally over slots
  * 0 .. its own position (the last `window` of them when window > 0, as in
- * the *_sw calls).  out [B][C][H][D] bf16; lse [B][H][C] fp32, natural log,
+ * the *_ex calls).  out [B][C][H][D] bf16; lse [B][H][C] fp32, natural log,
  * or NULL.  The slots before start[b] must already hold the stream's keys
- * and values.  With start[b] = 0 and C = T this is nc_attn_fwd_sw over the
+ * and values.  With start[b] = 0 and C = T this is nc_attn_fwd_ex over the
  * chunk (plus the cache writes); a prompt may also be fed in several chunks,
  * each starting where the previous one ended.  The pages prefill the KV
  * cache before decoding (ai.flicky.cc, "nanochat: свой ChatGPT от
@@ -195,7 +214,8 @@ int nc_attn_decode_sw(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_n
  * in the device status word (2).  Workspace: NC_OP_PREFILL with T = C. */
 int nc_attn_prefill(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *start, nc_f16 *kcache,
                     nc_bf16 *vcache, nc_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, int B,
-                    int C, int H, int D, int Tcap, float eps, float rope_base, int window, nc_stream_t stream);
+                    int C, int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
+                    nc_stream_t stream);
 
 /* Decode without any device allocation.  The pages have no counterpart to
  * this call; it exists for callers that cannot provide a workspace: a

@@ -79,23 +79,49 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert f(*args, 16, 1, 128, 2, 64, 1e-6, 1e4, None) == -1          # workspace too small
 
 
-def test_window_calls_reject_a_negative_window(lib):
+def _ex_calls(lib):
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
-    f = lib.nc_attn_fwd_sw
-    f.argtypes = [P] * 10 + [SZ, I, I, I, I, F, F, I, P]
+    f = lib.nc_attn_fwd_ex
+    f.argtypes = [P] * 10 + [SZ, I, I, I, I, F, F, I, I, P]
     f.restype = I
-    args = [fake] * 3 + [None] + [fake] * 4 + [None] + [fake]
-    assert f(*args, 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -1, None) == -1
-    assert f(*([None] * 10), 0, 0, 128, 2, 64, 1e-6, 1e4, 32, None) == 0  # empty problem, any window
-    g = lib.nc_attn_bwd_sw
-    g.argtypes = [P] * 13 + [SZ, I, I, I, I, F, F, I, P]
+    g = lib.nc_attn_bwd_ex
+    g.argtypes = [P] * 13 + [SZ, I, I, I, I, F, F, I, I, P]
     g.restype = I
-    assert g(*([fake] * 3 + [None] + [fake] * 9), 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -5, None) == -1
-    d = lib.nc_attn_decode_sw
-    d.argtypes = [P] * 8 + [SZ, I, I, I, I, F, F, I, P]
+    d = lib.nc_attn_decode_ex
+    d.argtypes = [P] * 8 + [SZ, I, I, I, I, F, F, I, I, P]
     d.restype = I
-    assert d(fake, None, None, fake, fake, fake, fake, fake, 1 << 30, 2, 2, 128, 64, 1e-6, 1e4, -1, None) == -1
+    pf = lib.nc_attn_prefill
+    pf.argtypes = [P] * 9 + [SZ, I, I, I, I, I, F, F, I, I, P]
+    pf.restype = I
+    return f, g, d, pf
+
+
+def test_ex_calls_reject_a_negative_window(lib):
+    f, g, d, _ = _ex_calls(lib)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    args = [fake] * 3 + [None] + [fake] * 4 + [None] + [fake]
+    assert f(*args, 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -1, 0, None) == -1
+    assert f(*([None] * 10), 0, 0, 128, 2, 64, 1e-6, 1e4, 32, 0, None) == 0  # empty problem, any window
+    assert g(*([fake] * 3 + [None] + [fake] * 9), 1 << 30, 1, 128, 2, 64, 1e-6, 1e4, -5, 0, None) == -1
+    assert d(fake, None, None, fake, fake, fake, fake, fake, 1 << 30, 2, 2, 128, 64, 1e-6, 1e4, -1, 0, None) == -1
+
+
+def test_ex_calls_reject_kv_heads_that_do_not_divide_h(lib):
+    """Grouped-query attention: kv_heads must divide H (0 means H)."""
+    f, g, d, pf = _ex_calls(lib)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    args = [fake] * 3 + [None] + [fake] * 4 + [None] + [fake]
+    for bad in (-1, 3, 8, 5):  # H = 4
+        assert f(*args, 1 << 30, 1, 128, 4, 64, 1e-6, 1e4, 0, bad, None) == -1, bad
+        assert g(*([fake] * 3 + [None] + [fake] * 9), 1 << 30, 1, 128, 4, 64, 1e-6, 1e4, 0, bad, None) == -1
+        assert d(fake, None, None, fake, fake, fake, fake, fake, 1 << 30, 2, 4, 64, 128, 1e-6, 1e4, 0, bad,
+                 None) == -1
+        assert pf(*([fake] * 9), 1 << 30, 1, 128, 4, 64, 256, 1e-6, 1e4, 0, bad, None) == -1
+        # the head check comes before the empty-problem shortcut
+        assert f(*([None] * 10), 0, 0, 128, 4, 64, 1e-6, 1e4, 0, bad, None) == -1
+    for ok in (0, 1, 2, 4):  # divisors of H = 4 (0 meaning H): an empty problem is a no-op
+        assert f(*([None] * 10), 0, 0, 128, 4, 64, 1e-6, 1e4, 0, ok, None) == 0
+        assert g(*([None] * 13), 0, 0, 128, 4, 64, 1e-6, 1e4, 0, ok, None) == 0
 
 
 def test_empty_problem_is_a_no_op(lib):

@@ -1,5 +1,5 @@
-"""GPU parity of the sliding-window calls (nc_attn_fwd_sw, nc_attn_bwd_sw,
-nc_attn_decode_sw) against the fp64 oracle with the same window, on the same
+"""GPU parity of the sliding-window calls (nc_attn_fwd_ex, nc_attn_bwd_ex,
+nc_attn_decode_ex) against the fp64 oracle with the same window, on the same
 seeded bf16 inputs and with the tolerances of tests/test_gpu_parity.py.
 Windows are chosen so that the band edge falls inside a 128-key tile (W not a
 multiple of 128), on a tile boundary (W = 512, the quarter of a 2048 context),

@@ -94,12 +94,14 @@ def randn_bf16(shape, gen: torch.Generator) -> torch.Tensor:
     return torch.randn(*shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
 
 
-def attn_inputs(B: int, T: int, H: int, D: int, seed: int, with_dout: bool = True):
-    """q, k, v (and dout) as bf16 CPU tensors [B, T, H, D], drawn in that order."""
+def attn_inputs(B: int, T: int, H: int, D: int, seed: int, with_dout: bool = True, kv_heads: int | None = None):
+    """q, k, v (and dout) as bf16 CPU tensors [B, T, H, D], drawn in that order
+    (k and v with kv_heads heads when given)."""
     g = _gen(seed)
+    Hkv = H if kv_heads is None else kv_heads
     q = randn_bf16((B, T, H, D), g)
-    k = randn_bf16((B, T, H, D), g)
-    v = randn_bf16((B, T, H, D), g)
+    k = randn_bf16((B, T, Hkv, D), g)
+    v = randn_bf16((B, T, Hkv, D), g)
     dout = randn_bf16((B, T, H, D), g) if with_dout else None
     return q, k, v, dout
 
@@ -108,9 +110,10 @@ def workload_inputs(w: AttnWorkload, with_dout: bool = True):
     return attn_inputs(w.B, w.T, w.H, w.D, w.seed, with_dout)
 
 
-def decode_inputs(B: int, H: int, D: int, Tcap: int, seed: int, lens=None):
+def decode_inputs(B: int, H: int, D: int, Tcap: int, seed: int, lens=None, kv_heads: int | None = None):
     """lens [B] int32 (uniform in [1, Tcap] unless given), then q [B,H,D],
-    raw keys [B,Tcap,H,D] and values [B,Tcap,H,D], all bf16 CPU tensors.
+    raw keys [B,Tcap,Hkv,D] and values [B,Tcap,Hkv,D] (Hkv = kv_heads, default
+    H), all bf16 CPU tensors.
 
     ``lens[b]`` counts the valid cache slots of stream b including the new
     token, whose position is ``lens[b] - 1``.  The raw key at that slot is the
@@ -120,25 +123,27 @@ def decode_inputs(B: int, H: int, D: int, Tcap: int, seed: int, lens=None):
     if lens is None:
         lens = torch.randint(1, Tcap + 1, (B,), generator=g, dtype=torch.int64)
     lens = torch.as_tensor(lens, dtype=torch.int32)
+    Hkv = H if kv_heads is None else kv_heads
     q = randn_bf16((B, H, D), g)
-    k_raw = randn_bf16((B, Tcap, H, D), g)
-    v = randn_bf16((B, Tcap, H, D), g)
+    k_raw = randn_bf16((B, Tcap, Hkv, D), g)
+    v = randn_bf16((B, Tcap, Hkv, D), g)
     return lens, q, k_raw, v
 
 
-def prefill_inputs(B: int, C: int, H: int, D: int, Tcap: int, seed: int, start=None):
+def prefill_inputs(B: int, C: int, H: int, D: int, Tcap: int, seed: int, start=None, kv_heads: int | None = None):
     """start [B] int32 (uniform in [0, Tcap - C] unless given), then the chunk's
-    queries q [B,C,H,D], raw keys [B,Tcap,H,D] and values [B,Tcap,H,D], all bf16
-    CPU tensors.  Stream b's chunk holds positions start[b] .. start[b]+C-1;
+    queries q [B,C,H,D], raw keys [B,Tcap,Hkv,D] and values [B,Tcap,Hkv,D]
+    (Hkv = kv_heads, default H), all bf16 CPU tensors.  Stream b's chunk holds positions start[b] .. start[b]+C-1;
     its own raw keys and values are the slots start[b] .. start[b]+C-1 of
     k_raw and v, the slots before them the stream's history."""
     g = _gen(seed)
     if start is None:
         start = torch.randint(0, Tcap - C + 1, (B,), generator=g, dtype=torch.int64)
     start = torch.as_tensor(start, dtype=torch.int32)
+    Hkv = H if kv_heads is None else kv_heads
     q = randn_bf16((B, C, H, D), g)
-    k_raw = randn_bf16((B, Tcap, H, D), g)
-    v = randn_bf16((B, Tcap, H, D), g)
+    k_raw = randn_bf16((B, Tcap, Hkv, D), g)
+    v = randn_bf16((B, Tcap, Hkv, D), g)
     return start, q, k_raw, v
 
 
