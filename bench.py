@@ -193,7 +193,7 @@ def bench_ours(args, ws_n, rank, local):
     value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
 
     # ---- decode (same rank, own timing; L2 flushed between calls) ----
-    dec = e2e = win = pre = None
+    dec = e2e = win = pre = gqa = None
     if not args.no_extras:
         dec = bench_decode(nc, dev, args, rank)
         # ---- the short-window layers: the same step with W = T / 4 ----
@@ -201,6 +201,9 @@ def bench_ours(args, ws_n, rank, local):
         win["decode"] = bench_decode(nc, dev, args, rank, window=w.T // 4)
         # ---- a 512-token chunk appended to every stream's cache ----
         pre = bench_prefill(nc, dev, args)
+        # ---- grouped-query attention: 2 key/value heads for the 10 query heads ----
+        gqa = bench_gqa(nc, dev, args, w, GQA_KV_HEADS)
+        gqa["decode"] = bench_decode(nc, dev, args, rank, kv_heads=GQA_KV_HEADS)
         # ---- end to end through the public API with host buffers ----
         e2e = bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b)
 
@@ -258,6 +261,7 @@ def bench_ours(args, ws_n, rank, local):
         "decode": dec,
         "window": win,
         "prefill": pre,
+        "gqa": gqa,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -269,7 +273,7 @@ def bench_ours(args, ws_n, rank, local):
 # from one ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum, summarised under profiles/ with its command).
 # Must go back to None whenever that kernel's code changes.
-DRAM_TRAFFIC = {"attn_bwd_dkdv": 852.95e6 + 311.85e6}
+DRAM_TRAFFIC = {"attn_bwd_dkdv": 853.19e6 + 311.68e6}
 
 
 def band_pairs(T, W):
@@ -320,6 +324,63 @@ def bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv
     return {"workload": f"{w.name} fwd+bwd with a sliding window W = T/4 = {W}", "W": W,
             "ms_per_step": round(ms, 4), "value": round(3.5 * fwd / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "flops_per_step": 3.5 * fwd, "kernels": kernels}
+
+
+GQA_KV_HEADS = 2  # key/value heads of the grouped-query leg (d20: groups of 5 query heads)
+
+
+def bench_gqa(nc, dev, args, w, Hkv):
+    """The fwd+bwd step through the grouped-query calls with Hkv key/value
+    heads for the workload's H query heads, timed like the main step.  The
+    score matmuls are those of the multi-head step (every query head still
+    meets every visible key), so the algorithmic FLOPs are the same."""
+    eps, base = workloads.EPS, workloads.ROPE_BASE
+    q, k, v, dout = workloads.attn_inputs(w.B, w.T, w.H, w.D, w.seed, kv_heads=Hkv)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, dout))
+    del q, k, v, dout
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    qh = torch.empty_like(qd, dtype=torch.float16)
+    kh = torch.empty_like(kd, dtype=torch.float16)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = nc.new_workspace(nc.NC_OP_FWD, w.B, w.T, w.H, w.D, dev)
+    ws_b = nc.new_workspace(nc.NC_OP_BWD, w.B, w.T, w.H, w.D, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nc.nc_attn_fwd_ex(qd, kd, vd, None, out, lse, qh, kh, None, ws_f, eps, base, 0, stream)
+        nc.nc_attn_bwd_ex(qd, kd, vd, None, out, lse, qh, kh, dod, dq, dk, dv, ws_b, eps, base, 0, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 5)
+    nc.nc_profile_read()
+    nc.nc_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    nc.nc_profile_enable(False)
+    kern = nc.nc_profile_read()
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during the grouped-query leg")
+    ms = e0.elapsed_time(e1) / steps
+    fwd = w.fwd_flops()
+    pk, _ = peaks()
+    alg = {"attn_fwd": fwd, "attn_bwd_dkdv": 2.0 * fwd, "attn_bwd_dq": 0.5 * fwd}
+    kernels = {}
+    for k_, (n_, t_) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
+        kernels[k_] = {"launches_per_step": n_ // steps, "avg_us": round(1e3 * t_ / max(n_, 1), 2)}
+        if k_ in alg:
+            tf = alg[k_] / (t_ / n_ * 1e-3) / 1e12
+            kernels[k_]["tflops"] = round(tf, 1)
+            kernels[k_]["frac_of_peak"] = round(tf / pk["bf16_tflops"], 4)
+    return {"workload": f"{w.name} fwd+bwd, grouped-query: H={w.H} query heads, {Hkv} key/value heads",
+            "kv_heads": Hkv, "ms_per_step": round(ms, 4), "value": round(3.5 * fwd / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "kernels": kernels}
 
 
 def bench_prefill(nc, dev, args, B=32, H=10, D=128, Tcap=2048, C=512):
@@ -375,9 +436,9 @@ def bench_prefill(nc, dev, args, B=32, H=10, D=128, Tcap=2048, C=512):
             "tokens_per_s": round(B * C / (ms * 1e-3), 1), "kernels": kernels}
 
 
-def bench_decode(nc, dev, args, rank, window=0):
+def bench_decode(nc, dev, args, rank, window=0, kv_heads=None):
     w = workloads.D20_DECODE
-    lens, q, k_raw, v = workloads.decode_workload_inputs(w)
+    lens, q, k_raw, v = workloads.decode_workload_inputs(w, kv_heads=kv_heads)
     kcache = nc.qk_norm_rope(k_raw.to(dev), eps=workloads.EPS, rope_base=workloads.ROPE_BASE)
     vcache = v.to(dev)
     qd, lens_d = q.to(dev), lens.to(dev)
@@ -387,7 +448,7 @@ def bench_decode(nc, dev, args, rank, window=0):
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        if window:
+        if window or kv_heads:
             nc.nc_attn_decode_ex(qd, None, None, kcache, vcache, lens_d, out, ws, workloads.EPS,
                                  workloads.ROPE_BASE, window, stream)
         else:
@@ -408,13 +469,15 @@ def bench_decode(nc, dev, args, rank, window=0):
         times.append(e0.elapsed_time(e1))
     if nc.device_status() != 0:
         raise RuntimeError("device status set during decode")
-    byt = workloads.decode_bytes(torch.clamp(lens, max=window) if window else lens, w.H, w.D)
+    byt = workloads.decode_bytes(torch.clamp(lens, max=window) if window else lens, w.H, w.D, kv_heads)
     ms = statistics.median(times)
     pk, kind = peaks()
     gbs = byt / (ms * 1e-3) / 1e9
     name = "d20 decode: 32 streams, H=10, D=128, cache capacity 2048, lens ~ U[1,2048] seed 4"
     if window:
         name += f", sliding window W = {window} (the last W slots)"
+    if kv_heads:
+        name += f", {kv_heads} key/value heads (grouped-query)"
     return {"workload": name,
             "bytes": byt, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -423,42 +486,77 @@ def bench_decode(nc, dev, args, rank, window=0):
 
 
 def bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b):
-    """fwd+bwd through the public API with pinned host inputs: H2D of q, k, v,
-    dout and D2H of dq, dk, dv inside the timed region."""
+    """fwd+bwd through the public API with pinned host buffers: every step
+    copies its q, k, v, dout host->device and its dq, dk, dv device->host
+    inside the timed region.  Steps are pipelined over two device buffer sets
+    and three streams (host->device copies, compute, device->host copies), so
+    one step's copies overlap its neighbours' compute and the other copy
+    direction; the region ends when the last step's results are on the host."""
     hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, dout))
-    hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
-    stream = torch.cuda.current_stream(dev)
-    dq_, dk_, dv_ = (torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
-    qd_, kd_, vd_, do_ = (torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for _ in range(4))
-    out = torch.empty_like(qd_)
-    qh, kh = torch.empty_like(qd_, dtype=torch.float16), torch.empty_like(qd_, dtype=torch.float16)
+    hout = [[torch.empty_like(hq).pin_memory() for _ in range(3)] for _ in range(2)]
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def dbuf(dtype=torch.bfloat16):
+        return torch.empty(q.shape, dtype=dtype, device=dev)
+
+    ins = [[dbuf() for _ in range(4)] for _ in range(2)]    # q, k, v, dout
+    outs = [[dbuf() for _ in range(3)] for _ in range(2)]   # dq, dk, dv
+    out = dbuf()
+    qh, kh = dbuf(torch.float16), dbuf(torch.float16)
     lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "comp", "out")}
+    used = [False, False]
 
-    def step():
-        for d_, h_ in ((qd_, hq), (kd_, hk), (vd_, hv), (do_, hdo)):
-            d_.copy_(h_, non_blocking=True)
+    def step(i):
+        j = i % 2
+        qd_, kd_, vd_, do_ = ins[j]
+        dq_, dk_, dv_ = outs[j]
+        with torch.cuda.stream(s_in):
+            if used[j]:
+                s_in.wait_event(ev["comp"][j])  # step i-2 has finished reading these inputs
+            for d_, h_ in ((qd_, hq), (kd_, hk), (vd_, hv), (do_, hdo)):
+                d_.copy_(h_, non_blocking=True)
+            ev["in"][j].record(s_in)
+        comp.wait_event(ev["in"][j])
+        if used[j]:
+            comp.wait_event(ev["out"][j])  # step i-2's results have left these buffers
         nc.nc_attn_fwd(qd_, kd_, vd_, None, out, lse, qh, kh, None, ws_f, workloads.EPS,
-                       workloads.ROPE_BASE, stream)
+                       workloads.ROPE_BASE, comp)
         nc.nc_attn_bwd(qd_, kd_, vd_, None, out, lse, qh, kh, do_, dq_, dk_, dv_, ws_b, workloads.EPS,
-                       workloads.ROPE_BASE, stream)
-        for h_, d_ in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
-            h_.copy_(d_, non_blocking=True)
+                       workloads.ROPE_BASE, comp)
+        ev["comp"][j].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][j])
+            for h_, d_ in zip(hout[j], (dq_, dk_, dv_)):
+                h_.copy_(d_, non_blocking=True)
+            ev["out"][j].record(s_out)
+        used[j] = True
 
+    def run(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(comp)
+        s_in.wait_event(e0)
+        for i in range(n):
+            step(i)
+        for j in range(2):
+            if used[j]:
+                comp.wait_event(ev["out"][j])
+        e1.record(comp)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    run(3)
     n = max(3, min(args.steps, 10))
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / n
+    ms = run(n) / n
+    if nc.device_status() != 0:
+        raise RuntimeError("device status set during the end-to-end leg")
+    # the last step's results arrived intact
+    assert torch.equal(hout[(n - 1) % 2][0], outs[(n - 1) % 2][0].cpu())
     nbytes = q.numel() * 2
     return {"value": round(w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 3 * nbytes, "ms_per_step": round(ms, 3),
-            "steps": n}
+            "steps": n, "pipeline": "2 buffer sets; H2D, compute and D2H on separate streams"}
 
 
 # ------------------------------------------------------ CPU oracle legs ----

@@ -147,13 +147,15 @@ def prefill_inputs(B: int, C: int, H: int, D: int, Tcap: int, seed: int, start=N
     return start, q, k_raw, v
 
 
-def decode_workload_inputs(w: DecodeWorkload):
-    return decode_inputs(w.B, w.H, w.D, w.Tcap, w.seed)
+def decode_workload_inputs(w: DecodeWorkload, kv_heads: int | None = None):
+    return decode_inputs(w.B, w.H, w.D, w.Tcap, w.seed, kv_heads=kv_heads)
 
 
-def decode_bytes(lens, H: int, D: int) -> int:
+def decode_bytes(lens, H: int, D: int, kv_heads: int | None = None) -> int:
     """Algorithmic HBM bytes of one decode step: every valid K and V cache
-    row read once (bf16), plus q, out and lens."""
+    row read once (16-bit; kv_heads of them per slot, default H), plus q, out
+    and lens."""
+    Hkv = H if kv_heads is None else kv_heads
     n = int(torch.as_tensor(lens).to(torch.int64).sum())
     B = int(torch.as_tensor(lens).numel())
-    return n * H * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B
+    return n * Hkv * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B
