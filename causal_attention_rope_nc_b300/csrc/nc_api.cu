@@ -17,6 +17,10 @@
 
 namespace {
 
+// Dynamic shared memory the decode kernels may use: the per-block opt-in
+// maximum of sm_103 (227 KB) less 1 KB for their static shared arrays.
+constexpr int kDecodeSmemMax = 232448 - 1024;
+
 thread_local int t_last_cuda_error = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -73,6 +77,12 @@ int device_ready() {
     optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<128>), nc::bwd::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<64>), nc::bwdq::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<128>), nc::bwdq::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<64, 1>), kDecodeSmemMax);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<64, 2>), kDecodeSmemMax);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<64, 4>), kDecodeSmemMax);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<128, 1>), kDecodeSmemMax);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<128, 2>), kDecodeSmemMax);
+    optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<128, 4>), kDecodeSmemMax);
     if (r != cudaSuccess) {
         t_last_cuda_error = static_cast<int>(r);
         state[dev] = NC_ELAUNCH;
@@ -399,23 +409,80 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
     return c_bytes + ml_bytes + o_bytes;
 }
 
+// Keys (fp16) or values (bf16) of a [B][Tcap][Hkv][D] cache as a 4D tensor
+// map with [sb][Hkv][D] boxes (no swizzle): one copy brings sb whole slots.
+int make_cache_tmap(CUtensorMap* tm, const void* ptr, int B, int Tcap, int Hkv, int D, int sb,
+                    CUtensorMapDataType dt) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(Tcap), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2,
+                                   static_cast<cuuint64_t>(Tcap) * Hkv * D * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(Hkv),
+                               static_cast<cuuint32_t>(sb), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode_fn()(tm, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
+template <int D, int HPW>
+int launch_decode_tma(const CUtensorMap& tk, const CUtensorMap& tv, const nc_bf16* q, const nc_bf16* k_new,
+                      const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache, const int32_t* lens, nc_bf16* out,
+                      const DecodeWs& ws, int B, int H, int Hkv, int Tcap, float eps, const nc::Theta& th,
+                      float scale_log2, int W, int sb, int nst, cudaStream_t s) {
+    const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
+    const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
+    const int nwc = (H + HPW - 1) / HPW;  // compute warps (<= MAX_CWARPS), plus one producer warp
+    const size_t smem = nc::dec::smem_bytes(Hkv, D, sb, nst);
+    ProfScope ps("attn_decode", s);
+    nc::dec::attn_decode_tma_kernel<D, HPW><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)),
+                                              (nwc + 1) * 32, smem, s>>>(
+        tk, tv, reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
+        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
+        reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
+        ws.part_ml, ws.counters, B, H, Hkv, Tcap, nparts, eps, th, scale_log2, W, sb, nst);
+    return launch_status();
+}
+
 template <int D>
 int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache, nc_bf16* vcache,
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Hkv, int Tcap, float eps,
                 float base, int W, cudaStream_t s) {
-    const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
-    const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
-    const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
-    const double scale_log2 = 1.4426950408889634 / std::sqrt(double(D));
+    const float scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
     nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
     for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
-    ProfScope ps("attn_decode", s);
-    nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
-        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
-        reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-        ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, float(scale_log2), W, H / Hkv);
-    return launch_status();
+    if (Hkv == H) {
+        // multi-head attention: the register-pipelined kernel, one warp per head
+        const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
+        const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
+        const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
+        ProfScope ps("attn_decode", s);
+        nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0,
+                                         s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
+            reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
+            reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
+            ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, scale_log2, W, 1);
+        return launch_status();
+    }
+    // grouped-query attention: the TMA ring kernel
+    const int sb = nc::dec::stage_slots(Hkv, D);
+    const int nst = nc::dec::ring_stages(Hkv, D, sb);
+    if (nc::dec::smem_bytes(Hkv, D, sb, nst) > static_cast<size_t>(kDecodeSmemMax)) return NC_EINVAL;
+    CUtensorMap tk, tv;
+    if (make_cache_tmap(&tk, kcache, B, Tcap, Hkv, D, sb, kF16) ||
+        make_cache_tmap(&tv, vcache, B, Tcap, Hkv, D, sb, kBF16))
+        return NC_EINVAL;
+    switch (nc::dec::heads_per_warp(H)) {
+        case 1: return launch_decode_tma<D, 1>(tk, tv, q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Hkv, Tcap,
+                                           eps, th, scale_log2, W, sb, nst, s);
+        case 2: return launch_decode_tma<D, 2>(tk, tv, q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Hkv, Tcap,
+                                           eps, th, scale_log2, W, sb, nst, s);
+        case 4: return launch_decode_tma<D, 4>(tk, tv, q, k_new, v_new, kcache, vcache, lens, out, ws, B, H, Hkv, Tcap,
+                                           eps, th, scale_log2, W, sb, nst, s);
+        default: return NC_EINVAL;  // more than 4 * MAX_CWARPS heads: rejected by the callers
+    }
 }
 
 }  // namespace

@@ -1,10 +1,10 @@
-// Single-token decode over a KV cache (memory bound, CUDA cores).
+// Single-token decode over a KV cache (memory bound, CUDA cores + TMA).
 //
 // Cache layout [B][Tcap][Hkv][D]: one cache slot holds all Hkv key/value
 // heads of one position contiguously (2*Hkv*D bytes).  Query head h reads
 // key/value head h / G (grouped-query attention, G = H / Hkv; G = 1 is plain
-// multi-head attention).  Keys are cached normalised and
-// rotated, in IEEE fp16 (elements bounded by sqrt(D)); values raw, in bf16.
+// multi-head attention).  Keys are cached normalised and rotated, in IEEE
+// fp16 (elements bounded by sqrt(D)); values raw, in bf16.
 //
 // Split over the cache: one CTA per (chunk c of CH slots, stream b), grid
 // ceil(Tcap / CH) x B; a CTA whose chunk starts at or past the stream's
@@ -12,33 +12,53 @@
 // real chunks to SMs as they free up and every SM streams about the same
 // number of bytes whatever the length mix.
 //
-// Inside a CTA warp w takes heads w, w + NW, ...  For one head it walks the
-// chunk's slots BATCH at a time: a group of D/8 lanes reads one slot's key
-// row (fp16) and value row (bf16) as 16-byte pieces, 32/(D/8) slots per warp
-// load (streaming loads, evict-first).  The batches are software-pipelined
-// over two register buffers: every load of batch n+1 is issued before the
-// arithmetic of batch n, so each lane keeps 2 * BATCH / (32/(D/8)) loads in
-// flight and the rows come straight from HBM into registers.  Scores are
+// Two kernels share this split and the merge below.
+//
+// attn_decode_kernel (plain multi-head attention, G = 1): warp w takes heads
+// w, w + NW, ...  For one head it walks the chunk's slots BATCH at a time: a
+// group of D/8 lanes reads one slot's key row (fp16) and value row (bf16) as
+// 16-byte pieces, 32/(D/8) slots per warp load (streaming loads,
+// evict-first).  The batches are software-pipelined over two register
+// buffers: every load of batch n+1 is issued before the arithmetic of batch
+// n, so the rows come straight from HBM into registers.
+//
+// attn_decode_tma_kernel (grouped-query attention, G > 1): one producer warp
+// streams the chunk through a ring of NST
+// shared-memory stages with TMA: stage n holds slots s0 + n*SB ..
+// s0 + n*SB + SB - 1, all Hkv heads of each, as one [SB][Hkv][D] box of
+// keys and one of values (one tensor-map copy each).  The ring, not the
+// register file, holds the bytes in flight, so a CTA keeps NST * SB * Hkv *
+// D * 4 bytes in flight (about 80 KB, two CTAs per SM) however few warps do
+// the arithmetic, and each cache row leaves HBM once per CTA even when G
+// query heads read it.  Compute warp w takes query heads w*HPW .. w*HPW +
+// HPW - 1 and walks each stage BATCH slots at a time: a group of D/8 lanes
+// reads one slot's key row and value row of the head's key/value head from
+// shared memory as 16-byte pieces, 32/(D/8) slots per warp load.  Scores are
 // formed in log2 units (qhat carries scale * log2 e); each lane group keeps
 // its part of an online softmax state (m shared by the warp, l and o per
-// group) that the groups add up at the end of the chunk.
+// group) that the groups add up at the end of the chunk.  After its last
+// read of a stage every compute warp arrives on the stage's empty barrier;
+// the producer refills the stage once all have.  (Measured on the d20
+// decode: the ring is 18% faster than the register kernel for groups of 5,
+// 4% slower for plain multi-head attention and 29% slower with a 512-slot
+// window, hence the split.)
 //
 // A stream with one chunk writes its output directly.  Otherwise each chunk
 // stores (m, l, o) per head in the workspace, and the last CTA of the stream
-// to finish (per-stream arrival counter) merges the chunks in chunk order
-// (deterministic) and resets the counter for the next call.
+// to finish (per-stream arrival counter) merges the chunks and resets the
+// counter for the next call: per head, lanes read the chunks' (m, l) side by
+// side, and the weighted partial outputs are added in chunk order
+// (deterministic), their loads issued back to back.
 //
 // With a sliding window W only the last W slots are attended (slot j is
 // visible when 0 <= p - j < W); chunks wholly before them exit at once and
 // take no part in the merge.
 //
 // The new token (position p = lens[b] - 1): the CTA that owns the last chunk
-// normalises and rotates k_new, writes it (fp16) and v_new into slot p, and
-// reads them back through the cache like every other slot, so the score at p
-// uses exactly the stored fp16 key.  With G = 1 each warp writes the slot of
-// its own head; with G > 1 the CTA writes every key/value head of the slot
-// first, and the G warps of a group then read the same rows (cached loads
-// instead of evict-first ones, so the group's later readers hit in L2).
+// normalises and rotates k_new, writes it (fp16) and v_new into slot p (in
+// the ring kernel for every key/value head, followed by a proxy fence so the
+// TMA engine sees the writes) and then reads the slot like every other, so
+// the score at p uses exactly the stored fp16 key.
 #pragma once
 
 #include "nc_common.cuh"
@@ -47,23 +67,124 @@
 namespace nc {
 namespace dec {
 
-constexpr int CH = 128;         // cache slots per CTA (one partial result)
-constexpr int PART_SLOTS = 32;  // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / CH) partials
-constexpr int MAX_WARPS = 16;   // warps per CTA (heads beyond this many loop)
-constexpr int BATCH = 8;        // slots per warp batch
-static_assert(CH % BATCH == 0 && CH >= PART_SLOTS, "chunking");
+constexpr int CH = 128;          // cache slots per CTA (one partial result)
+constexpr int PART_SLOTS = 32;   // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / CH) partials
+constexpr int MAX_WARPS = 16;    // warps per CTA of the register kernel (heads beyond this many loop)
+constexpr int MAX_CWARPS = 16;   // compute warps per CTA of the ring kernel
+constexpr int BATCH = 8;         // slots per online-softmax step
+constexpr int MAX_SB = 64;       // slots per stage, at most
+constexpr int STAGE_TARGET = 40 * 1024;  // bytes (keys + values) per stage, about
+constexpr int RING_BUDGET = 96 * 1024;   // bytes of the ring when a stage is small enough for two
+static_assert(CH % MAX_SB == 0 && CH >= PART_SLOTS, "chunking");
+
+// Slots per stage: a power of two in [BATCH, MAX_SB] near STAGE_TARGET bytes.
+inline int stage_slots(int Hkv, int D) {
+    int sb = MAX_SB;
+    while (sb > BATCH && static_cast<long long>(sb) * Hkv * D * 4 > STAGE_TARGET) sb >>= 1;
+    return sb;
+}
+// Stages in the ring: as many as fit RING_BUDGET, 1 to 4.
+inline int ring_stages(int Hkv, int D, int sb) {
+    const long long stage = static_cast<long long>(sb) * Hkv * D * 4;
+    long long n = RING_BUDGET / stage;
+    if (n > 4) n = 4;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+inline size_t smem_bytes(int Hkv, int D, int sb, int nst) {
+    return static_cast<size_t>(nst) * sb * Hkv * D * 4 + 2 * nst * 8;
+}
+// Query heads per compute warp: enough that at most MAX_CWARPS warps cover H.
+inline int heads_per_warp(int H) {
+    int hpw = 1;
+    while (hpw * MAX_CWARPS < H) hpw <<= 1;
+    return hpw;
+}
 
 template <int D>
 struct Lanes {
     static constexpr int LPS = D / 8;        // lanes per slot row (16 bytes each)
     static constexpr int SPW = 32 / LPS;     // slots per warp load
-    static constexpr int NLD = BATCH / SPW;  // key (and value) loads per lane per batch
+    static constexpr int NLD = BATCH / SPW;  // key (and value) reads per lane per batch
     static_assert(NLD >= 1 && BATCH % SPW == 0, "batch shape");
 };
+
+// Make this thread's generic-proxy global writes visible to later
+// async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // 16-byte streaming load (read once: evict first).  A regular coherent global
 // load, so a slot written earlier by the same warp is seen after __syncwarp.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+
+// The last CTA of stream b to finish (per-stream arrival counter) merges the
+// partial results of chunks c_lo .. nch - 1 into out and resets the counter.
+// Called by every thread of a CTA that stored a partial.
+template <int D>
+__device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, int max_parts,
+                                             const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                                             __nv_bfloat16* __restrict__ out, unsigned int* __restrict__ counters,
+                                             int n_parts, int* s_last) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NW = static_cast<int>(blockDim.x >> 5);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_last = atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
+    __syncthreads();
+    if (!*s_last) return;  // uniform
+    __threadfence();
+    for (int h = warp; h < H; h += NW) {
+        // lanes take the partials 32 at a time for (m, l) and the weights;
+        // lane: D/32 consecutive elements of the output
+        constexpr int EPL = D / 32;
+        const long long pstride = static_cast<long long>(H) * 2;  // between one chunk's (m, l) and the next's
+        const float* pmb = part_ml + (static_cast<long long>(b) * max_parts * H + h) * 2;
+        const float* pob = part_o + (static_cast<long long>(b) * max_parts * H + h) * D + lane * EPL;
+        float M = -INFINITY;
+        for (int cc = c_lo + lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(pmb + cc * pstride));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float Ls = 0.f, o[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+        for (int c0 = c_lo; c0 < nch; c0 += 32) {
+            float w = 0.f;
+            if (c0 + lane < nch) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(pmb + (c0 + lane) * pstride));
+                w = ex2(ml.x - M);
+                Ls = fmaf(ml.y, w, Ls);
+            }
+            const int n = min(32, nch - c0);
+            // chunk order, as the partials were written; the loads do not
+            // depend on one another, so they overlap
+#pragma unroll 8
+            for (int i = 0; i < n; ++i) {
+                const float wi = __shfl_sync(0xffffffffu, w, i);
+                const float* po = pob + static_cast<long long>(c0 + i) * H * D;
+                if constexpr (EPL == 4) {
+                    const float4 a = __ldcg(reinterpret_cast<const float4*>(po));
+                    o[0] = fmaf(a.x, wi, o[0]);
+                    o[1] = fmaf(a.y, wi, o[1]);
+                    o[2] = fmaf(a.z, wi, o[2]);
+                    o[3] = fmaf(a.w, wi, o[3]);
+                } else {
+                    const float2 a = __ldcg(reinterpret_cast<const float2*>(po));
+                    o[0] = fmaf(a.x, wi, o[0]);
+                    o[1] = fmaf(a.y, wi, o[1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, k);
+        const float inv = 1.f / Ls;
+        __nv_bfloat16* orow = out + (static_cast<long long>(b) * H + h) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2)
+            *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
+    }
+    if (threadIdx.x == 0) counters[b] = 0u;  // ready for the next call
+}
 
 // Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
 // counters [B] u32 (zero between calls).
@@ -257,48 +378,236 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         }
     }
     if (n_parts == 1) return;  // uniform
+    merge_chunks<D>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts, &s_last);
+}
 
-    // ---- the last chunk of the stream to finish merges every chunk ----
-    __threadfence();
+// Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
+// counters [B] u32 (zero between calls).  blockDim = (compute warps + 1) * 32,
+// compute warps = ceil(H / HPW) <= MAX_CWARPS; dynamic shared memory
+// smem_bytes(Hkv, D, SB, NST).
+template <int D, int HPW>
+__global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
+    const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
+    unsigned int* __restrict__ counters, int B, int H, int Hkv, int Tcap, int max_parts, float eps,
+    const __grid_constant__ Theta theta, float scale_log2, int W, int SB, int NST) {
+    using Ln = Lanes<D>;
+    constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float2 s_cs[D / 2];  // rotation at the new token's position
+    __shared__ int s_last;
+    const int c = blockIdx.x, b = blockIdx.y;
+    const int L = lens[b];
+    if (L < 1 || L > Tcap) {  // never read outside the cache; the stream's output is left untouched
+        if (c == 0 && threadIdx.x == 0) flag_error(2, 0x501);
+        return;
+    }
+    const int nch = (L + CH - 1) / CH;
+    const int s_vis = max(0, L - W);  // first visible slot (W >= 2^30: slot 0)
+    const int c_lo = s_vis / CH;      // first chunk holding a visible slot
+    if (c >= nch || c < c_lo) return;  // uniform over the CTA
+    const int n_parts = nch - c_lo;    // chunks that produce a partial
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NW = static_cast<int>(blockDim.x >> 5);
+    const int nwc = NW - 1;  // compute warps; the last warp is the producer
+    const int G = H / Hkv;
+    const int p_new = L - 1;
+    const bool own_new = (k_new != nullptr) && (c == nch - 1);
+    const int s0 = max(c * CH, s_vis), s1 = min(L, c * CH + CH);
+    const int n_st = (s1 - s0 + SB - 1) / SB;  // stages this chunk streams
+    const int g = lane / LPS;    // slot of this lane group within a warp load
+    const int sub = lane % LPS;  // 16-byte piece of the row
+    const int e0 = sub * 8;      // first head-dim element of this lane
+    const long long slot_elems = static_cast<long long>(Hkv) * D;
+    const uint32_t stage_bytes = static_cast<uint32_t>(SB) * Hkv * D * 2;  // keys (or values) of one stage
+    uint8_t* kst = smem;
+    uint8_t* vst = smem + static_cast<size_t>(NST) * stage_bytes;
+    const uint32_t bar0 = smem_u32(smem + static_cast<size_t>(2) * NST * stage_bytes);
+    auto full_bar = [&](int st) -> uint32_t { return bar0 + 8 * st; };
+    auto empty_bar = [&](int st) -> uint32_t { return bar0 + 8 * (NST + st); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(full_bar(i), 1);
+            mbar_init(empty_bar(i), nwc);
+        }
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
-    __syncthreads();
-    if (!s_last) return;  // uniform
-    __threadfence();
-    for (int h = warp; h < H; h += NW) {
-        // lane: D/32 consecutive elements
-        constexpr int EPL = D / 32;
-        const float* pmb = part_ml + (static_cast<long long>(b) * max_parts * H + h) * 2;
-        const float* pob = part_o + (static_cast<long long>(b) * max_parts * H + h) * D + lane * EPL;
-        float M = -INFINITY;
-        for (int cc = c_lo; cc < nch; ++cc) M = fmaxf(M, __ldcg(pmb + static_cast<long long>(cc) * H * 2));
-        float Ls = 0.f, o[EPL];
+
+    // RoPE(RMSNorm(x)) of row x (D bf16) at the new token's position: the 8
+    // elements [e0, e0 + 8) of this lane (every lane group computes the row).
+    auto norm_rope8 = [&](const __nv_bfloat16* x, float (&o)[8]) {
+        float xv[8], yv[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + e0), xv);
+        float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-        for (int cc = c_lo; cc < nch; ++cc) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pmb + static_cast<long long>(cc) * H * 2));
-            const float w = ex2(ml.x - M);
-            Ls = fmaf(ml.y, w, Ls);
-            const float* po = pob + static_cast<long long>(cc) * H * D;
-            if constexpr (EPL == 4) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(po));
-                o[0] = fmaf(a.x, w, o[0]);
-                o[1] = fmaf(a.y, w, o[1]);
-                o[2] = fmaf(a.z, w, o[2]);
-                o[3] = fmaf(a.w, w, o[3]);
-            } else {
-                const float2 a = __ldcg(reinterpret_cast<const float2*>(po));
-                o[0] = fmaf(a.x, w, o[0]);
-                o[1] = fmaf(a.y, w, o[1]);
+        for (int e = 0; e < 8; ++e) ss = fmaf(xv[e], xv[e], ss);
+        ss = group_sum<LPS>(ss);
+        const float rs = rsqrtf(ss / D + eps);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] *= rs;
+        // pair (i, i + D/2): the partner element sits LPS/2 lanes away
+#pragma unroll
+        for (int e = 0; e < 8; ++e) yv[e] = __shfl_xor_sync(0xffffffffu, xv[e], LPS / 2);
+        const bool lo_half = sub < LPS / 2;
+        const int i0 = (sub % (LPS / 2)) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 cs = s_cs[i0 + e];
+            o[e] = lo_half ? xv[e] * cs.x - yv[e] * cs.y : yv[e] * cs.y + xv[e] * cs.x;
+        }
+    };
+    // RoPE(RMSNorm(k_new)) (fp16) and v_new into slot p of every key/value
+    // head, before the producer's first copy
+    if (own_new) {  // uniform over the CTA
+        for (int hk = warp; hk < Hkv; hk += NW) {
+            const long long row = (static_cast<long long>(b) * Hkv + hk) * D;
+            float kv[8];
+            norm_rope8(k_new + row, kv);
+            if (g == 0) {
+                const long long at = (static_cast<long long>(b) * Tcap + p_new) * slot_elems +
+                                     static_cast<long long>(hk) * D + e0;
+                *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_f16(kv);
+                *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
             }
         }
-        const float inv = 1.f / Ls;
-        __nv_bfloat16* orow = out + (static_cast<long long>(b) * H + h) * D + lane * EPL;
-#pragma unroll
-        for (int e = 0; e < EPL; e += 2)
-            *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
+        fence_proxy_async_global();
+        __syncthreads();
     }
-    if (threadIdx.x == 0) counters[b] = 0u;  // ready for the next call
+
+    if (warp == nwc) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            fence_proxy_async_global();
+            int issued = 0;
+            for (int n = 0; n < n_st; ++n) {
+                const int st = n % NST;
+                if (n >= NST && !mbar_wait(empty_bar(st), ((n / NST) - 1) & 1, 0x511)) break;
+                mbar_expect_tx(full_bar(st), 2 * stage_bytes);
+                tma_load_4d(smem_u32(kst + static_cast<size_t>(st) * stage_bytes), &tm_k, 0, 0, s0 + n * SB, b,
+                            full_bar(st));
+                tma_load_4d(smem_u32(vst + static_cast<size_t>(st) * stage_bytes), &tm_v, 0, 0, s0 + n * SB, b,
+                            full_bar(st));
+                ++issued;
+            }
+            // never leave the CTA with a copy still in flight
+            for (int n = max(0, issued - NST); n < issued; ++n) mbar_wait(full_bar(n % NST), (n / NST) & 1, 0x512);
+        }
+    } else {
+        // --------------------------------------------------- compute warps --
+        const int h0 = warp * HPW;  // first query head of this warp
+        float qv[HPW][8], m[HPW], l[HPW], acc[HPW][8];
+#pragma unroll
+        for (int i = 0; i < HPW; ++i) {
+            m[i] = -INFINITY;
+            l[i] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+            if (h0 + i < H) {  // uniform over the warp
+                norm_rope8(q + (static_cast<long long>(b) * H + h0 + i) * D, qv[i]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qv[i][e] *= scale_log2;
+            }
+        }
+        for (int n = 0; n < n_st; ++n) {
+            const int st = n % NST;
+            if (!mbar_wait_warp(full_bar(st), (n / NST) & 1, 0x513)) break;
+            const uint8_t* ks = kst + static_cast<size_t>(st) * stage_bytes;
+            const uint8_t* vs = vst + static_cast<size_t>(st) * stage_bytes;
+            const int sb0 = s0 + n * SB;  // cache slot of the stage's first row
+            for (int j = 0; j < SB && sb0 + j < s1; j += BATCH) {
+#pragma unroll
+                for (int i = 0; i < HPW; ++i) {
+                    if (h0 + i >= H) break;  // uniform over the warp
+                    const int hk = (h0 + i) / G;
+                    uint4 kr[NLD], vr[NLD];
+#pragma unroll
+                    for (int u = 0; u < NLD; ++u) {
+                        const int r = j + g + SPW * u;  // row of the stage (< SB)
+                        const size_t at = (static_cast<size_t>(r) * Hkv + hk) * (D * 2) + e0 * 2;
+                        kr[u] = *reinterpret_cast<const uint4*>(ks + at);
+                        vr[u] = *reinterpret_cast<const uint4*>(vs + at);
+                        if (sb0 + r >= s1) {  // past the chunk: whatever the cache holds there, read zeros
+                            kr[u] = make_uint4(0u, 0u, 0u, 0u);
+                            vr[u] = kr[u];
+                        }
+                    }
+                    float sc[NLD];
+#pragma unroll
+                    for (int u = 0; u < NLD; ++u) {
+                        float kf[8];
+                        f16x8_to_f32(kr[u], kf);
+                        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            a0 = fmaf(qv[i][e], kf[e], a0);
+                            a1 = fmaf(qv[i][e + 1], kf[e + 1], a1);
+                        }
+                        sc[u] = a0 + a1;
+                    }
+#pragma unroll
+                    for (int u = 0; u < NLD; ++u) {
+                        sc[u] = group_sum<LPS>(sc[u]);
+                        if (sb0 + j + g + SPW * u >= s1) sc[u] = -INFINITY;
+                    }
+                    // the batch maximum over every lane group: one running max per warp
+                    float mx = m[i];
+#pragma unroll
+                    for (int u = 0; u < NLD; ++u) mx = fmaxf(mx, sc[u]);
+#pragma unroll
+                    for (int o = LPS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    const float corr = ex2(m[i] - mx);  // slot sb0 + j is valid: mx is finite
+                    l[i] *= corr;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[i][e] *= corr;
+                    m[i] = mx;
+#pragma unroll
+                    for (int u = 0; u < NLD; ++u) {
+                        const float pe = ex2(sc[u] - mx);
+                        float vf[8];
+                        bf16x8_to_f32(vr[u], vf);
+                        l[i] += pe;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pe, vf[e], acc[i][e]);
+                    }
+                }
+            }
+            mbar_arrive_warp(empty_bar(st));  // this warp is done with the stage
+        }
+#pragma unroll
+        for (int i = 0; i < HPW; ++i) {
+            const int h = h0 + i;
+            if (h >= H) break;  // uniform over the warp
+            // add the lane groups' parts (same m)
+#pragma unroll
+            for (int o = LPS; o < 32; o <<= 1) {
+                l[i] += __shfl_xor_sync(0xffffffffu, l[i], o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
+            }
+            if (g == 0) {
+                if (n_parts == 1) {
+                    float o[8];
+                    const float inv = 1.f / l[i];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = acc[i][e] * inv;
+                    *reinterpret_cast<uint4*>(out + (static_cast<long long>(b) * H + h) * D + e0) = f32x8_to_bf16(o);
+                } else {
+                    const long long pi = (static_cast<long long>(b) * max_parts + c) * H + h;
+                    float4* po = reinterpret_cast<float4*>(part_o + pi * D + e0);
+                    po[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                    po[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+                    if (sub == 0) *reinterpret_cast<float2*>(part_ml + pi * 2) = make_float2(m[i], l[i]);
+                }
+            }
+        }
+    }
+    if (n_parts == 1) return;  // uniform
+    merge_chunks<D>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts, &s_last);
 }
 
 }  // namespace dec
