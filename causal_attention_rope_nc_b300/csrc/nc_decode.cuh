@@ -14,17 +14,19 @@
 //
 // Two kernels share this split and the merge below.
 //
-// attn_decode_kernel (plain multi-head attention, G = 1): warp w takes heads
-// w, w + NW, ...  For one head it walks the chunk's slots BATCH at a time: a
-// group of D/8 lanes reads one slot's key row (fp16) and value row (bf16) as
-// 16-byte pieces, 32/(D/8) slots per warp load (streaming loads,
-// evict-first).  The batches are software-pipelined over two register
-// buffers: every load of batch n+1 is issued before the arithmetic of batch
-// n, so the rows come straight from HBM into registers.
+// attn_decode_kernel (launched for plain multi-head attention, G = 1; it is
+// correct for any G, reading key/value head h / G with cached loads when
+// G > 1 and writing every key/value head of the new slot first): warp w
+// takes heads w, w + NW, ...  For one head it walks the chunk's slots BATCH
+// at a time: a group of D/8 lanes reads one slot's key row (fp16) and value
+// row (bf16) as 16-byte pieces, 32/(D/8) slots per warp load (streaming
+// loads, evict-first).  The batches are software-pipelined over two
+// register buffers: every load of batch n+1 is issued before the arithmetic
+// of batch n, so the rows come straight from HBM into registers.
 //
-// attn_decode_tma_kernel (grouped-query attention, G > 1): one producer warp
-// streams the chunk through a ring of NST
-// shared-memory stages with TMA: stage n holds slots s0 + n*SB ..
+// attn_decode_tma_kernel (grouped-query attention, G > 1): one producer
+// warp streams the chunk through a ring of NST shared-memory stages with
+// TMA: stage n holds slots s0 + n*SB ..
 // s0 + n*SB + SB - 1, all Hkv heads of each, as one [SB][Hkv][D] box of
 // keys and one of values (one tensor-map copy each).  The ring, not the
 // register file, holds the bytes in flight, so a CTA keeps NST * SB * Hkv *
