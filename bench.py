@@ -53,6 +53,24 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's own batch: replicas process independent batches
+    (weak scaling, no data-path collective); rank 0 keeps the workload's."""
+    return seed + 1000 * rank
+
+
+def job_throughput(ms_local: float, ws_n: int, flops_per_step: float, steps: int, device="cpu"):
+    """(max over ranks of the timed region in ms, whole-job TFLOP/s): every
+    rank ran `steps` steps of `flops_per_step`, and the job is as fast as its
+    slowest rank.  Collective only when ws_n > 1 (NCCL on the GPUs, gloo in
+    the CPU tests)."""
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if ws_n > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, ws_n * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -136,7 +154,7 @@ def bench_ours(args, ws_n, rank, local):
     B, T, H, D = w.B, w.T, w.H, w.D
     eps, base = workloads.EPS, workloads.ROPE_BASE
     # weak scaling: every rank runs its own d20 batch (seed offset by rank)
-    q, k, v, dout = workloads.attn_inputs(B, T, H, D, w.seed + 1000 * rank)
+    q, k, v, dout = workloads.attn_inputs(B, T, H, D, rank_seed(w.seed, rank))
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, dout))
     out = torch.empty_like(qd)
     qh, kh = torch.empty_like(qd, dtype=torch.float16), torch.empty_like(kd, dtype=torch.float16)
@@ -184,13 +202,9 @@ def bench_ours(args, ws_n, rank, local):
         raise RuntimeError("device status set during the timed region")
 
     # max over ranks
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if ws_n > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
-    ms_per_step = ms_max / args.steps
     flops = w.fwd_bwd_flops()
-    value = ws_n * flops * args.steps / (ms_max * 1e-3) / 1e12
+    ms_max, value = job_throughput(ms_total, ws_n, flops, args.steps, dev)
+    ms_per_step = ms_max / args.steps
 
     # ---- decode (same rank, own timing; L2 flushed between calls) ----
     dec = e2e = win = pre = gqa = None
