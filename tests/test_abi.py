@@ -146,3 +146,18 @@ def test_strerror(lib):
     lib.nc_strerror.restype = ctypes.c_char_p
     assert lib.nc_strerror(0) == b"ok"
     assert b"invalid" in lib.nc_strerror(-1)
+
+
+def test_binding_checks_grouped_heads_on_the_host():
+    """The binding derives kv_heads from k's shape and refuses a head count
+    that does not divide H before any call reaches the library."""
+    import torch
+    import causal_attention_rope_nc_b300 as nc
+    q = torch.empty((1, 4, 6, 64), dtype=torch.bfloat16)
+    assert nc._kv_heads(q, torch.empty((1, 4, 3, 64))) == 3
+    assert nc._kv_heads(q, torch.empty((1, 4, 6, 64))) == 6
+    with pytest.raises(ValueError):
+        nc._kv_heads(q, torch.empty((1, 4, 4, 64)))
+    with pytest.raises(ValueError):
+        nc._shape(torch.empty((1, 4, 2, 64)), "k", (1, 4, 3, 64))
+    nc._shape(None, "k_new", (1, 3, 64))  # an absent optional tensor passes
