@@ -489,7 +489,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
 
 extern "C" {
 
-int nc_version(void) { return (0 << 16) | 1; }
+int nc_version(void) { return (0 << 16) | 2; }
 
 const char* nc_strerror(int code) {
     switch (code) {

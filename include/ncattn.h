@@ -74,7 +74,9 @@ typedef struct CUstream_st *nc_stream_t; /* == cudaStream_t */
 #define NC_OP_NORM_ROPE 3
 #define NC_OP_PREFILL 4
 
-/* Library version, (major << 16) | minor. */
+/* Library version, (major << 16) | minor.  0.2: the sliding-window calls
+ * became the *_ex calls with a kv_heads argument (grouped-query attention),
+ * and nc_attn_prefill gained kv_heads. */
 int nc_version(void);
 
 /* Human-readable name of an NC_* code. */

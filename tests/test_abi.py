@@ -161,3 +161,8 @@ def test_binding_checks_grouped_heads_on_the_host():
     with pytest.raises(ValueError):
         nc._shape(torch.empty((1, 4, 2, 64)), "k", (1, 4, 3, 64))
     nc._shape(None, "k_new", (1, 3, 64))  # an absent optional tensor passes
+
+
+def test_version_names_the_grouped_query_api(lib):
+    lib.nc_version.restype = ctypes.c_int
+    assert lib.nc_version() == (0 << 16) | 2
