@@ -113,6 +113,8 @@ def test_gqa_full_size_sampled(nc):
     (12, 4, 128, [129, 1, 2048, 1000], 0, True),   # the new token written once per key/value head
     (16, 1, 64, [64, 65, 2000, 513], 0, True),     # multi-query, D = 64
     (10, 5, 128, [2048, 1, 1000, 513], 300, True), # window
+    (32, 8, 128, [2048, 700, 1, 129], 0, True),    # 32 query heads: two per compute warp
+    (48, 16, 64, [1500, 2048, 64, 2], 0, True),    # 48 query heads: four per compute warp
 ])
 def test_gqa_decode_matches_oracle(nc, H, Hkv, D, lens, W, new):
     Tcap = 2048
