@@ -197,6 +197,17 @@ def test_decode_edge_lengths(nc, lens):
     assert np.max(np.abs(f64(out) - ref)) <= FWD_MAX_ABS
 
 
+@pytest.mark.parametrize("H,D,with_new", [(24, 128, True), (40, 64, True), (24, 128, False)])
+def test_decode_more_heads_than_warps(nc, H, D, with_new):
+    """More than 16 heads: the warps of a CTA take a second head each (the
+    first batch of a later head is loaded after the earlier head is done)."""
+    lens_t, q, k_raw, v = decode_inputs(B=3, H=H, D=D, Tcap=600, seed=34, lens=[600, 1, 257])
+    out, kc, vc = _gpu_decode(nc, lens_t, q, k_raw, v, with_new)
+    ref = oracle.attn_decode(q, k_raw, v, lens_t, eps=EPS, base=BASE)
+    assert np.max(np.abs(f64(out) - ref)) <= FWD_MAX_ABS
+    assert rel_frob(f64(out), ref) <= FWD_REL
+
+
 def test_decode_head_dim_64_and_repeat(nc):
     lens_t, q, k_raw, v = decode_inputs(B=4, H=3, D=64, Tcap=300, seed=32, lens=[300, 1, 150, 64])
     out1, *_ = _gpu_decode(nc, lens_t, q, k_raw, v, True)
