@@ -54,6 +54,8 @@ def run(nc, q, k, v, dout, W=0):
     (1, 385, 4, 1, 128, 129, 103),  # one key/value head (multi-query), window edge inside a tile
     (2, 256, 8, 4, 128, 0, 104),    # two full tiles
     (1, 1000, 6, 3, 128, 250, 105), # window not a multiple of the tile, several tiles per group
+    (1, 1, 4, 1, 128, 0, 110),      # single token, one key/value head
+    (2, 128, 4, 2, 64, 0, 111),     # exactly one tile per head
 ])
 def test_gqa_fwd_bwd_matches_oracle(nc, B, T, H, Hkv, D, W, seed):
     q, k, v, dout = attn_inputs(B, T, H, D, seed, kv_heads=Hkv)
