@@ -50,7 +50,9 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // tensor only), stored as IEEE fp16: the norm bounds every element by
 // sqrt(D) <= 11.4, well inside fp16's range, and fp16 keeps 3 more mantissa
 // bits than bf16 for the score products.  rstd (optional) receives 1/r,
-// laid out [2][B][T][H] (q then k).
+// laid out [2][B][T][H] (q then k).  (With fewer key/value heads than query
+// heads the host runs one launch per tensor, each with its own head count
+// and its own part of rstd.)
 //
 // One group of D/8 lanes owns one token (b, t) of one tensor: it reads the
 // token's rotation row from the table once and walks the token's H heads,
