@@ -117,6 +117,7 @@ def test_gqa_full_size_sampled(nc):
     (10, 5, 128, [2048, 1, 1000, 513], 300, True), # window
     (32, 8, 128, [2048, 700, 1, 129], 0, True),    # 32 query heads: two per compute warp
     (48, 16, 64, [1500, 2048, 64, 2], 0, True),    # 48 query heads: four per compute warp
+    (32, 16, 128, [2048, 333, 1, 130], 0, True),   # 64 KB stages: a ring of one stage
 ])
 def test_gqa_decode_matches_oracle(nc, H, Hkv, D, lens, W, new):
     Tcap = 2048
