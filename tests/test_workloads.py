@@ -34,3 +34,23 @@ def test_flop_convention():
     assert workloads.D20.fwd_bwd_flops() == pytest.approx(1202.59e9, rel=1e-5)
     assert workloads.D12.fwd_bwd_flops() == pytest.approx(180.39e9, rel=1e-4)
     assert workloads.D26.fwd_bwd_flops() == pytest.approx(781.68e9, rel=1e-5)
+
+
+def test_kv_heads_generators_keep_the_multi_head_draws():
+    """kv_heads = H (or unset) draws exactly the multi-head tensors, so every
+    seeded case keeps its inputs; fewer key/value heads shape k, v (and the
+    caches) with that many heads."""
+    import torch
+    a = workloads.attn_inputs(1, 5, 4, 64, 7)
+    b = workloads.attn_inputs(1, 5, 4, 64, 7, kv_heads=4)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    q, k, v, dout = workloads.attn_inputs(1, 5, 4, 64, 7, kv_heads=2)
+    assert q.shape == (1, 5, 4, 64) and k.shape == v.shape == (1, 5, 2, 64) and dout.shape == q.shape
+    lens, qd, kc, vc = workloads.decode_inputs(2, 6, 64, 16, 8, lens=[3, 16], kv_heads=3)
+    assert qd.shape == (2, 6, 64) and kc.shape == vc.shape == (2, 16, 3, 64)
+    start, qp, kp, vp = workloads.prefill_inputs(2, 4, 6, 64, 16, 9, start=[0, 12], kv_heads=1)
+    assert qp.shape == (2, 4, 6, 64) and kp.shape == vp.shape == (2, 16, 1, 64)
+    # algorithmic decode bytes: key and value rows of Hkv heads, q and out of H
+    assert workloads.decode_bytes([3, 16], 6, 64, 3) == 19 * 3 * 64 * 4 + 2 * 2 * 6 * 64 * 2 + 8
+    assert workloads.decode_bytes([3, 16], 6, 64) == workloads.decode_bytes([3, 16], 6, 64, 6)
