@@ -7,7 +7,18 @@ the import fails, and every call checks the status the library returns.
 
 The functions named ``nc_*`` mirror the C entry points one to one (torch
 tensors in place of pointers, the current CUDA stream by default).  The
-``attn_*`` helpers allocate outputs and workspaces with torch and call them.
+``attn_*`` helpers allocate outputs and workspaces with torch and call them:
+
+    out, lse, qhat, khat = attn_fwd(q, k, v)            # q, k, v [B, T, H, D] bf16, CUDA
+    dq, dk, dv = attn_bwd(q, k, v, out, lse, qhat, khat, dout)
+    out, lse, qhat, khat = attn_fwd(q, k, v, window=512)  # sliding window
+    out, lse, qhat, khat = attn_fwd(q, k2, v2)           # k2, v2 [B, T, 2, D]: 2 key/value heads
+    kcache = qk_norm_rope(k_prompt)                      # prefill a key cache [B, Tcap, Hkv, D] (fp16)
+    o = attn_decode(q1, kcache, vcache, lens, k_new=k1, v_new=v1)   # one new token per stream
+    out, lse = attn_prefill(qc, kc, vc, start, kcache, vcache)      # a chunk at offsets start[b]
+
+Grouped-query attention needs no flag: the key/value heads are read from k's
+(or the cache's) shape and must divide H.
 """
 from __future__ import annotations
 
