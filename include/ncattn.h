@@ -29,8 +29,10 @@
  *    256-byte aligned.
  *  - bf16 tensors are raw bfloat16 bits (nc_bf16), row-major and
  *    contiguous: token tensors [B][T][H][D], lse [B][H][T] (fp32, natural
- *    log), decode tensors [B][H][D], caches [B][Tcap][H][D].  Every 16-bit
- *    tensor must be 16-byte aligned.
+ *    log), decode tensors [B][H][D], caches [B][Tcap][H][D].  (With
+ *    grouped-query attention, through the *_ex calls and nc_attn_prefill,
+ *    the key/value-side tensors and the caches have Hkv heads instead of H.)
+ *    Every 16-bit tensor must be 16-byte aligned.
  *  - Normalised, rotated queries and keys (qhat, khat, the decode key cache)
  *    are IEEE fp16 (nc_f16): RMSNorm bounds each element by sqrt(D), well
  *    inside fp16's range, and fp16 carries 3 more mantissa bits than bf16
@@ -41,8 +43,8 @@
  *    where one is required, misalignment, D not 64/128, a negative size,
  *    eps < 0, rope_base <= 0, or a workspace that is too small; nothing is
  *    launched.  NC_EUNSUPPORTED: the current device is not sm_103.
- *    NC_ELAUNCH: a CUDA launch failed; nc_last_cuda_error() gives the
- *    cudaError_t.  A size of zero in B, T or H (Tcap for decode) is an empty
+ *    NC_ELAUNCH: a CUDA launch (or the library's one-time per-device setup)
+ *    failed; nc_last_cuda_error() gives the cudaError_t.  A size of zero in B, T or H (Tcap for decode) is an empty
  *    problem: NC_OK, nothing launched.
  *  - Kernels never spin unboundedly: a pipeline wait that has not completed
  *    after 2 s records a device-side status word and the kernel unwinds.
