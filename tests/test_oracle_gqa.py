@@ -97,3 +97,16 @@ def test_gqa_prefill_equals_repeated_cache_and_forward_rows(W):
         o_f, lse_f = oracle.attn_fwd(qf, k[b:b + 1, :T], v[b:b + 1, :T], window=W)
         assert np.allclose(out[b], o_f[0, s:], atol=1e-12)
         assert np.allclose(lse[b], lse_f[0, :, s:], atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [1, 6, 40])
+def test_gqa_windowed_decode_is_the_last_row_of_the_windowed_forward(W):
+    """Decode at position L-1 with a window and grouped heads equals row L-1
+    of the forward over the prefix with the same window and heads (W = 40
+    covers the whole prefix: the plain causal row)."""
+    B, H, Hkv, D, L = 1, 6, 2, 16, 23
+    q = _rand((B, L, H, D), 30)
+    k, v = _rand((B, L, Hkv, D), 31), _rand((B, L, Hkv, D), 32)
+    o_f, _ = oracle.attn_fwd(q, k, v, window=W)
+    o_d = oracle.attn_decode(q[:, L - 1], k, v, np.array([L], dtype=np.int32), window=W)
+    assert np.allclose(o_d, o_f[:, L - 1], atol=1e-12)
