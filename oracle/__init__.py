@@ -58,6 +58,10 @@ def _load():
         lib.orc_attn_decode.restype = ctypes.c_int
         lib.orc_attn_prefill.argtypes = [dp, dp, dp, ip, i, i, i, i, i, i, d, d, i, i, dp, dp]
         lib.orc_attn_prefill.restype = ctypes.c_int
+        lib.orc_attn_fwd_fp8.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, d, i, i, dp, dp]
+        lib.orc_attn_fwd_fp8.restype = ctypes.c_int
+        lib.orc_e4m3.argtypes = [d]
+        lib.orc_e4m3.restype = d
         _lib = lib
     return _lib
 
@@ -161,3 +165,29 @@ def attn_prefill(q, k_raw, v, start, eps=1e-6, base=10000.0, flags=METHOD, windo
         raise ValueError("oracle prefill: start + C outside [0, Tcap]")
     return out, lse
 
+
+
+def e4m3(x) -> np.ndarray:
+    """The oracle's E4M3 rounding (ties to even, saturating at +-448),
+    elementwise."""
+    a = _f64(x)
+    f = _load().orc_e4m3
+    return np.vectorize(f, otypes=[np.float64])(a) if a.size else a.copy()
+
+
+def attn_fwd_fp8(q, k, v, pos=None, eps=1e-6, base=10000.0, window=0, quant=True):
+    """FP8 forward under this library's quantisation reading (see
+    orc_attn_fwd_fp8): (o [B,T,H,D], lse [B,H,T]).  quant=False is the plain
+    forward."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, T, H, D = q.shape
+    o = np.empty_like(q)
+    lse = np.empty((B, H, T), dtype=np.float64)
+    p, pp = _pos(pos, T)
+    Hkv = k.shape[2]
+    _check_groups(H, Hkv, v.shape[2])
+    rc = _load().orc_attn_fwd_fp8(_dp(q), _dp(k), _dp(v), pp, B, T, H, Hkv, D, eps, base, int(window),
+                                  1 if quant else 0, _dp(o), _dp(lse))
+    if rc != 0:
+        raise MemoryError("oracle fp8 forward failed")
+    return o, lse

@@ -109,11 +109,35 @@ static double dot(const double *a, const double *b, int n)
     return s;
 }
 
+/* E4M3 rounding (the OCP 8-bit float with 4 exponent bits, bias 7 and 3
+ * mantissa bits, "fn" variant: no infinities, largest finite value 448):
+ * round to nearest, ties to even, with saturation to +-448.  Normal numbers
+ * are (1 + m/8) 2^(e-7), e = 1..15; subnormals m/8 2^-6; so the spacing of
+ * representable values is 2^(E-3) in the binade [2^E, 2^(E+1)), E >= -6, and
+ * 2^-9 below 2^-6. */
+double orc_e4m3(double x)
+{
+    if (x != x) return x;
+    double a = fabs(x);
+    if (a == 0.0) return x;
+    int E;
+    frexp(a, &E);          /* a = f 2^E with f in [0.5, 1): binade [2^(E-1), 2^E) */
+    E -= 1;
+    if (E < -6) E = -6;    /* subnormal spacing below 2^-6 */
+    double quantum = ldexp(1.0, E - 3);
+    double r = nearbyint(a / quantum) * quantum;  /* default rounding mode: ties to even */
+    if (r > 448.0) r = 448.0;
+    return x < 0 ? -r : r;
+}
+
 /* Step 3 for one (b, h): probabilities P[i][j] (zero where j is not
- * visible from i), outputs o and log-sum-exp.  P is T*T, row-major. */
-static void attend_head(const double *qh, const double *kh, const double *v,
-                        int b, int h, int T, int H, int Hkv, int D, int W, double *P,
-                        double *o, double *lse)
+ * visible from i), outputs o and log-sum-exp.  P is T*T, row-major.
+ * pquant (the fp8 reading only): each probability p = exp(s - max) is
+ * replaced by E4M3(p 2^8) 2^-8 before it weights v, the output divides by
+ * the sum of those quantised weights, and lse uses the sum of the exact p. */
+static void attend_head_q(const double *qh, const double *kh, const double *v,
+                          int b, int h, int T, int H, int Hkv, int D, int W, int pquant, double *P,
+                          double *o, double *lse)
 {
     int hk = h / (H / Hkv);  /* the key/value head of query head h */
     double scale = 1.0 / sqrt((double)D);
@@ -126,13 +150,15 @@ static void attend_head(const double *qh, const double *kh, const double *v,
             row[j] = dot(qi, kh + at4(b, j, hk, 0, T, Hkv, D), D) * scale;
             if (row[j] > m) m = row[j];
         }
-        double l = 0.0;
+        double l = 0.0, lexact = 0.0;
         for (int j = 0; j < T; ++j) {
             if (!visible(i, j, W)) {
                 row[j] = 0.0;
                 continue;
             }
             row[j] = exp(row[j] - m);
+            lexact += row[j];
+            if (pquant) row[j] = orc_e4m3(row[j] * 256.0) / 256.0;
             l += row[j];
         }
         for (int j = 0; j < T; ++j) row[j] /= l;
@@ -142,8 +168,15 @@ static void attend_head(const double *qh, const double *kh, const double *v,
             for (int j = 0; j < T; ++j) acc += row[j] * v[at4(b, j, hk, d, T, Hkv, D)];
             oi[d] = acc;
         }
-        if (lse) lse[((size_t)b * H + h) * T + i] = m + log(l);
+        if (lse) lse[((size_t)b * H + h) * T + i] = m + log(lexact);
     }
+}
+
+static void attend_head(const double *qh, const double *kh, const double *v,
+                        int b, int h, int T, int H, int Hkv, int D, int W, double *P,
+                        double *o, double *lse)
+{
+    attend_head_q(qh, kh, v, b, h, T, H, Hkv, D, W, 0, P, o, lse);
 }
 
 /* Forward: o = softmax(qhat khat^T / sqrt(D) + mask) v; lse [B,H,T].  The
@@ -168,6 +201,65 @@ int orc_attn_fwd(const double *q, const double *k, const double *v, const int *p
         }
     free(qh);
     free(kh);
+    return err;
+}
+
+/* FP8 forward (this library's reading of fp8 attention; the pages name an
+ * fp8 training path and give no attention scheme).  With quant = 1:
+ *   qhat8 = E4M3(qhat 2^5) 2^-5, khat8 likewise (QK-norm bounds every element
+ *     by sqrt(D) <= 11.32, so 2^5 keeps them within E4M3's 448);
+ *   v8 = E4M3(v 2^tau) 2^-tau per (batch, key/value head), tau the largest
+ *     integer with max |v| 2^tau <= 448 (0 for an all-zero head);
+ *   s = qhat8 . khat8 / sqrt(D); p = exp(s - max over the row's visible keys);
+ *   P8 = E4M3(p 2^8) 2^-8; o = sum P8 v8 / sum P8; lse = max + ln sum p.
+ * quant = 0 skips every rounding: the function is then orc_attn_fwd. */
+int orc_attn_fwd_fp8(const double *q, const double *k, const double *v, const int *pos,
+                     int B, int T, int H, int Hkv, int D, double eps, double base, int W, int quant,
+                     double *o, double *lse)
+{
+    size_t n = (size_t)B * T * H * D, nk = (size_t)B * T * Hkv * D;
+    double *qh = malloc(n * sizeof(double)), *kh = malloc(nk * sizeof(double));
+    double *vq = malloc(nk * sizeof(double));
+    if (!qh || !kh || !vq) { free(qh); free(kh); free(vq); return -1; }
+    orc_norm_rope(q, pos, B, T, H, D, eps, base, ORC_NORM | ORC_ROPE, qh, NULL);
+    orc_norm_rope(k, pos, B, T, Hkv, D, eps, base, ORC_NORM | ORC_ROPE, kh, NULL);
+    memcpy(vq, v, nk * sizeof(double));
+    if (quant) {
+        for (size_t e = 0; e < n; ++e) qh[e] = orc_e4m3(qh[e] * 32.0) / 32.0;
+        for (size_t e = 0; e < nk; ++e) kh[e] = orc_e4m3(kh[e] * 32.0) / 32.0;
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < Hkv; ++g) {
+                double mx = 0.0;
+                for (int t = 0; t < T; ++t)
+                    for (int d = 0; d < D; ++d) {
+                        double a = fabs(v[at4(b, t, g, d, T, Hkv, D)]);
+                        if (a > mx) mx = a;
+                    }
+                int tau = 0;
+                if (mx > 0.0) {
+                    tau = (int)floor(log2(448.0 / mx));
+                    while (ldexp(mx, tau) > 448.0) --tau;  /* guard the log2 rounding */
+                    while (ldexp(mx, tau + 1) <= 448.0) ++tau;
+                }
+                for (int t = 0; t < T; ++t)
+                    for (int d = 0; d < D; ++d) {
+                        size_t e = at4(b, t, g, d, T, Hkv, D);
+                        vq[e] = ldexp(orc_e4m3(ldexp(v[e], tau)), -tau);
+                    }
+            }
+    }
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            double *P = malloc((size_t)T * T * sizeof(double));
+            if (!P) { err = -1; continue; }
+            attend_head_q(qh, kh, vq, b, h, T, H, Hkv, D, W, quant, P, o, lse);
+            free(P);
+        }
+    free(qh);
+    free(kh);
+    free(vq);
     return err;
 }
 
