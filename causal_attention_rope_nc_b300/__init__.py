@@ -9,13 +9,14 @@ The functions named ``nc_*`` mirror the C entry points one to one (torch
 tensors in place of pointers, the current CUDA stream by default).  The
 ``attn_*`` helpers allocate outputs and workspaces with torch and call them:
 
-    out, lse, qhat, khat = attn_fwd(q, k, v)            # q, k, v [B, T, H, D] bf16, CUDA
+    out, lse, qhat, khat = attn_fwd(q, k, v)            # q, k, v [B, T, H, D] bf16, CUDA (qhat, khat fp16)
     dq, dk, dv = attn_bwd(q, k, v, out, lse, qhat, khat, dout)
     out, lse, qhat, khat = attn_fwd(q, k, v, window=512)  # sliding window
     out, lse, qhat, khat = attn_fwd(q, k2, v2)           # k2, v2 [B, T, 2, D]: 2 key/value heads
-    kcache = qk_norm_rope(k_prompt)                      # prefill a key cache [B, Tcap, Hkv, D] (fp16)
+    kcache = qk_norm_rope(k_prompt)                      # prefill a key cache [B, Tcap, Hkv, D] (bf16)
     o = attn_decode(q1, kcache, vcache, lens, k_new=k1, v_new=v1)   # one new token per stream
     out, lse = attn_prefill(qc, kc, vc, start, kcache, vcache)      # a chunk at offsets start[b]
+    out, lse = attn_fwd_fp8(q, k, v)                     # E4M3 products (head dim 128)
 
 Grouped-query attention needs no flag: the key/value heads are read from k's
 (or the cache's) shape and must divide H.
@@ -31,12 +32,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libncattn.so")
 
 NC_OK, NC_EINVAL, NC_EUNSUPPORTED, NC_ELAUNCH, NC_EDEVICE = 0, -1, -2, -3, -4
-NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE, NC_OP_PREFILL = 0, 1, 2, 3, 4
+NC_OP_FWD, NC_OP_BWD, NC_OP_DECODE, NC_OP_NORM_ROPE, NC_OP_PREFILL, NC_OP_FWD_FP8 = 0, 1, 2, 3, 4, 5
 
 EXPORTED = ("nc_version", "nc_strerror", "nc_last_cuda_error", "nc_device_status",
             "nc_attn_workspace_size", "nc_qk_norm_rope", "nc_attn_fwd", "nc_attn_bwd",
             "nc_attn_decode", "nc_profile_enable", "nc_profile_read", "nc_attn_decode_noalloc",
-            "nc_attn_fwd_ex", "nc_attn_bwd_ex", "nc_attn_decode_ex", "nc_attn_prefill")
+            "nc_attn_fwd_ex", "nc_attn_bwd_ex", "nc_attn_decode_ex", "nc_attn_prefill", "nc_attn_fwd_fp8")
 NC_ETOOLARGE = -5
 
 
@@ -53,10 +54,17 @@ class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
-    L = ctypes.CDLL(LIB_PATH)
+LIB_CHECK_PATH = os.path.join(_HERE, "libncattn_check.so")
+
+
+def _load(path=None):
+    """The library's ctypes handle with every entry point typed.  path:
+    LIB_PATH by default; LIB_CHECK_PATH gives the bounds-checked debug build
+    (same entry points), which the bounds tests load beside the normal one."""
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(path)
     P, I, F, S, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
     L.nc_version.restype = I
     L.nc_strerror.argtypes = [I]
@@ -88,6 +96,8 @@ def _load():
     L.nc_attn_decode_ex.restype = I
     L.nc_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, F, F, I, I, S]
     L.nc_attn_prefill.restype = I
+    L.nc_attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, SZ, I, I, I, I, F, F, I, I, S]
+    L.nc_attn_fwd_fp8.restype = I
     return L
 
 
@@ -151,7 +161,7 @@ def nc_profile_read() -> dict:
 # ------------------------------------------------------ C entry points 1:1 --
 
 def nc_qk_norm_rope(x, pos, xhat, rstd, workspace, eps, rope_base, stream=None):
-    _bf16(x, "x"), _f16(xhat, "xhat")
+    _bf16(x, "x"), _bf16(xhat, "xhat")
     B, T, H, D = x.shape
     _check(lib.nc_qk_norm_rope(_ptr(x), _ptr(pos), _ptr(xhat), _ptr(rstd), _ptr(workspace),
                                workspace.numel(), B, T, H, D, eps, rope_base, _stream(stream)),
@@ -212,6 +222,19 @@ def _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace):
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, T, H, D)
 
 
+def nc_attn_fwd_fp8(q, k, v, pos, out, lse, workspace, eps, rope_base, window=0, stream=None):
+    """FP8 forward (E4M3 products; head dim 128); kv_heads is k.shape[2]."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _bf16(t, n)
+    B, T, H, D = q.shape
+    Hkv = _kv_heads(q, k)
+    _shape(k, "k", (B, T, Hkv, D)), _shape(v, "v", (B, T, Hkv, D)), _shape(out, "out", q.shape)
+    _shape(lse, "lse", (B, H, T))
+    _check(lib.nc_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(out), _ptr(lse), _ptr(workspace),
+                               workspace.numel(), B, T, H, D, eps, rope_base, int(window), Hkv, _stream(stream)),
+           "nc_attn_fwd_fp8")
+
+
 def nc_attn_bwd(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, eps, rope_base,
                 stream=None):
     args = _bwd_args(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace)
@@ -228,17 +251,19 @@ def nc_attn_bwd_ex(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspa
 
 
 def _decode_args(q, k_new, v_new, kcache, vcache, lens, out, workspace):
-    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("kcache", kcache), ("vcache", vcache),
+                 ("out", out)):
         _bf16(t, n)
-    _f16(kcache, "kcache")
     B, Tcap, Hkv, D = kcache.shape
     H = q.shape[1]
     if H % Hkv:
         raise ValueError(f"{Hkv} key/value heads do not divide {H} query heads")
     _shape(q, "q", (B, H, D)), _shape(out, "out", (B, H, D)), _shape(vcache, "vcache", kcache.shape)
     _shape(k_new, "k_new", (B, Hkv, D)), _shape(v_new, "v_new", (B, Hkv, D))
+    if lens is None or lens.dtype != torch.int32 or not lens.is_cuda or tuple(lens.shape) != (B,):
+        raise ValueError(f"lens must be a CUDA int32 tensor of shape ({B},)")
     return (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(lens), _ptr(out),
-            _ptr(workspace), workspace.numel(), B, H, D, Tcap)
+            _ptr(workspace), 0 if workspace is None else workspace.numel(), B, H, D, Tcap)
 
 
 def nc_attn_decode(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps, rope_base, stream=None):
@@ -257,9 +282,8 @@ def nc_attn_decode_ex(q, k_new, v_new, kcache, vcache, lens, out, workspace, eps
 
 
 def nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, workspace, eps, rope_base, window=0, stream=None):
-    for n, t in (("q", q), ("k", k), ("v", v), ("vcache", vcache), ("out", out)):
+    for n, t in (("q", q), ("k", k), ("v", v), ("kcache", kcache), ("vcache", vcache), ("out", out)):
         _bf16(t, n)
-    _f16(kcache, "kcache")
     B, C, H, D = q.shape
     Tcap = kcache.shape[1]
     Hkv = _kv_heads(q, k)
@@ -272,11 +296,11 @@ def nc_attn_prefill(q, k, v, start, kcache, vcache, out, lse, workspace, eps, ro
 
 def nc_attn_decode_noalloc(q, k_new, v_new, kcache, vcache, lens, out, eps, rope_base, stream=None):
     """nc_attn_decode for callers that cannot supply a workspace (the library
-    keeps the scratch in a fixed 16 MiB device array; see include/ncattn.h)."""
-    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("vcache", vcache), ("out", out)):
-        _bf16(t, n)
-    _f16(kcache, "kcache")
-    B, Tcap, H, D = kcache.shape
+    keeps the scratch in a fixed 16 MiB device array; see include/ncattn.h).
+    Multi-head attention only: the cache has H key/value heads."""
+    if kcache.shape[2] != q.shape[1]:
+        raise ValueError("nc_attn_decode_noalloc takes H key/value heads (no grouped-query attention)")
+    B, H, D, Tcap = _decode_args(q, k_new, v_new, kcache, vcache, lens, out, None)[-4:]
     _check(lib.nc_attn_decode_noalloc(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
                                       _ptr(lens), _ptr(out), B, H, D, Tcap, eps, rope_base,
                                       _stream(stream)), "nc_attn_decode_noalloc")
@@ -300,6 +324,17 @@ def attn_fwd(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, str
     return out, lse, qhat, khat
 
 
+def attn_fwd_fp8(q, k, v, pos=None, eps=1e-6, rope_base=10000.0, workspace=None, stream=None, window=0):
+    """FP8 forward: returns (out, lse); see nc_attn_fwd_fp8 in include/ncattn.h
+    for the quantisation."""
+    B, T, H, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    ws = workspace if workspace is not None else new_workspace(NC_OP_FWD_FP8, B, T, H, D, q.device)
+    nc_attn_fwd_fp8(q, k, v, pos, out, lse, ws, eps, rope_base, window, stream)
+    return out, lse
+
+
 def attn_bwd(q, k, v, out, lse, qhat, khat, dout, pos=None, eps=1e-6, rope_base=10000.0,
              workspace=None, stream=None, window=0):
     """Returns (dq, dk, dv) (dk, dv with k's heads).  window: as passed to attn_fwd."""
@@ -315,7 +350,7 @@ def attn_bwd(q, k, v, out, lse, qhat, khat, dout, pos=None, eps=1e-6, rope_base=
 
 def qk_norm_rope(x, pos=None, eps=1e-6, rope_base=10000.0, stream=None):
     B, T, H, D = x.shape
-    xhat = torch.empty_like(x, dtype=torch.float16)
+    xhat = torch.empty_like(x)
     ws = new_workspace(NC_OP_NORM_ROPE, B, T, H, D, x.device)
     nc_qk_norm_rope(x, pos, xhat, None, ws, eps, rope_base, stream)
     return xhat

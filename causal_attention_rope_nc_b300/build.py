@@ -18,6 +18,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libncattn.so")
+# the bounds-checked debug build (-DNC_CHECK): every raw global store and the
+# decode kernels' raw cache loads are checked against the tensors the call
+# registered; a stray access is skipped and recorded in the status word
+LIB_CHECK = os.path.join(HERE, "libncattn_check.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 FLAGS = [
@@ -33,23 +37,32 @@ def _sources():
             + [os.path.join(INCLUDE, "ncattn.h")])
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(s) > t for s in _sources())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
-    cmd = [NVCC, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-o", LIB, os.path.join(CSRC, "nc_api.cu")]
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    lib = LIB_CHECK if checked else LIB
+    if not force and not needs_build(lib):
+        return lib
+    cmd = [NVCC, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-o", lib, os.path.join(CSRC, "nc_api.cu")]
+    if checked:
+        cmd[1:1] = ["-DNC_CHECK"]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     subprocess.run(cmd, check=True)
-    return LIB
+    return lib
+
+
+def build_all(force: bool = False) -> None:
+    """The library and its bounds-checked debug build."""
+    build(force=force)
+    build(force=force, checked=True)
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv)
-    print(LIB)
+    build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, checked="--checked" in sys.argv)
+    print(LIB_CHECK if "--checked" in sys.argv else LIB)

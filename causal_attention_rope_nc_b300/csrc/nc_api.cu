@@ -13,6 +13,7 @@
 #include "nc_common.cuh"
 #include "nc_decode.cuh"
 #include "nc_fwd.cuh"
+#include "nc_fwd_fp8.cuh"
 #include "nc_rowops.cuh"
 
 namespace {
@@ -71,8 +72,11 @@ int device_ready() {
         cudaError_t x = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (x != cudaSuccess) r = x;
     };
-    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64>), nc::fwd::Smem<64>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128>), nc::fwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64, false>), nc::fwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128, false>), nc::fwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64, true>), nc::fwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd8::attn_fwd_fp8_kernel), nc::fwd8::Smem::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128, true>), nc::fwd::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<64>), nc::bwd::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<128>), nc::bwd::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<64>), nc::bwdq::Smem<64>::ALLOC);
@@ -91,6 +95,37 @@ int device_ready() {
     state[dev] = 1;
     return NC_OK;
 }
+
+// Bounds-checked build: the tensors of one call, registered on its stream
+// before its kernels (see nc::CheckRanges).  A no-op in the normal build.
+struct CallRanges {
+    nc::CheckRanges w{}, r{};
+    void add(const void* p, size_t bytes, bool writable) {
+        if (!p || !bytes) return;
+        const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+        if (r.n < nc::CHECK_MAX_RANGES) r.lo[r.n] = a, r.hi[r.n] = a + bytes, ++r.n;
+        if (writable && w.n < nc::CHECK_MAX_RANGES) w.lo[w.n] = a, w.hi[w.n] = a + bytes, ++w.n;
+    }
+    void in(const void* p, size_t bytes) { add(p, bytes, false); }
+    void out(const void* p, size_t bytes) { add(p, bytes, true); }
+    int publish(cudaStream_t s) const {
+#ifdef NC_CHECK
+        if (cudaMemcpyToSymbolAsync(nc::g_check_write, &w, sizeof(w), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyToSymbolAsync(nc::g_check_read, &r, sizeof(r), 0, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            t_last_cuda_error = static_cast<int>(cudaGetLastError());
+            return NC_ELAUNCH;
+        }
+#else
+        (void)s;
+#endif
+        return NC_OK;
+    }
+};
+#ifdef NC_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -165,6 +200,22 @@ int make_tmap(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D, int 
     return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
 }
 
+// The backward's dS^T scratch (fp16) as rows of 64 values: each block is
+// two [128 keys][64 queries] halves (bwdq::ds_offset); boxes of 64 values x
+// 128 rows (one half), 128-byte swizzled.
+int make_ds_tmap(CUtensorMap* tm, const void* ds, long long rows) {
+    const long long rows64 = 2 * rows;  // rows of 64 values
+    if (rows <= 0 || rows64 >= (1LL << 31)) return NC_EINVAL;  // TMA row coordinates are int32
+    const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows64)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode_fn()(tm, kF16, 2, const_cast<void*>(ds), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
 // The RoPE table [T][D/2] (cos, sin) viewed as an fp32 [T][D] tensor: boxes
 // of 32 values x 128 rows, 128-byte swizzled.  Rows past T read as zero.
 int make_tab_tmap(CUtensorMap* tm, const float2* tab, int T, int D) {
@@ -187,6 +238,21 @@ bool params_ok(float eps, float base) { return std::isfinite(eps) && eps >= 0.f 
 
 size_t tab_bytes(int T, int D) { return up256(static_cast<size_t>(T) * (D / 2) * sizeof(float2)); }
 int tpad_of(int T) { return ((T + 127) / 128) * 128; }  // query blocks of 128
+
+// Rows of 128 bf16 in the backward's dS^T scratch: one [128][128] block per
+// (query tile, key tile <= query tile) of every (batch, query head).
+long long ds_rows(int B, int T, int H) {
+    const long long n_t = (T + 127) / 128;
+    return static_cast<long long>(B) * H * (n_t * (n_t + 1) / 2) * 128;
+}
+
+// Backward workspace: RoPE table, delta, lse * log2(e), two norm maxima,
+// dS^T scratch.
+size_t bwd_ws_bytes(int B, int T, int H, int D) {
+    const int Tpad = tpad_of(T);
+    return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256 +
+           static_cast<size_t>(ds_rows(B, T, H)) * 128 * 2;
+}
 
 int rows_grid(long long rows, int D) {
     const long long groups = 256 / (D / 8);
@@ -226,25 +292,25 @@ int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base,
 // qhat (H heads) and, when k is given, khat (Hkv heads).  rstd (optional):
 // the q rows' [B][T][H] followed by the k rows' [B][T][Hkv].  One launch
 // covers both when the head counts agree, else one launch per tensor.
-template <int D>
-int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, nc_bf16* qh, nc_bf16* kh, float* rstd,
-                     int B, int T, int H, int Hkv, float eps, cudaStream_t s) {
+template <int D, typename OutT>
+int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, void* qh, void* kh, float* rstd,
+                     int B, int T, int H, int Hkv, float eps, cudaStream_t s, float out_scale = 1.f) {
     const long long toks = static_cast<long long>(B) * T;
     ProfScope ps("qk_norm_rope", s);
     if (!k || Hkv == H) {
-        nc::qk_norm_rope_kernel<D><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
+        nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
-            reinterpret_cast<__half*>(qh), reinterpret_cast<__half*>(kh), rstd, toks, T, H, eps);
+            reinterpret_cast<OutT*>(qh), reinterpret_cast<OutT*>(kh), rstd, toks, T, H, eps, out_scale);
         return launch_status();
     }
-    nc::qk_norm_rope_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(q), nullptr, tab, reinterpret_cast<__half*>(qh), nullptr, rstd, toks,
-        T, H, eps);
+    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q), nullptr, tab, reinterpret_cast<OutT*>(qh), nullptr, rstd, toks,
+        T, H, eps, out_scale);
     int rc = launch_status();
     if (rc) return rc;
-    nc::qk_norm_rope_kernel<D><<<tok_grid(toks, D), 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(k), nullptr, tab, reinterpret_cast<__half*>(kh), nullptr,
-        rstd ? rstd + toks * H : nullptr, toks, T, Hkv, eps);
+    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(k), nullptr, tab, reinterpret_cast<OutT*>(kh), nullptr,
+        rstd ? rstd + toks * H : nullptr, toks, T, Hkv, eps, out_scale);
     return launch_status();
 }
 
@@ -262,12 +328,12 @@ int kv_heads_of(int kv_heads, int H) {
 
 template <int D>
 int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
-             nc_bf16* qhat, nc_bf16* khat, float* rstd, void* ws, int B, int T, int H, int Hkv, float eps, float base,
+             nc_f16* qhat, nc_f16* khat, float* rstd, void* ws, int B, int T, int H, int Hkv, float eps, float base,
              int W, cudaStream_t s) {
     float2* tab = reinterpret_cast<float2*>(ws);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    rc = launch_norm_rope<D>(q, k, tab, qhat, khat, rstd, B, T, H, Hkv, eps, s);
+    rc = launch_norm_rope<D, __half>(q, k, tab, qhat, khat, rstd, B, T, H, Hkv, eps, s);
     if (rc) return rc;
     CUtensorMap tq, tk, tv, to;
     if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) ||
@@ -283,7 +349,7 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     const long long nblk = static_cast<long long>(n_pairs) * B * H;
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
     ProfScope ps("attn_fwd", s);
-    nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
+    nc::fwd::attn_fwd_kernel<D, false><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
         float(scale * log2e),
         float(mfix * log2e), float(mfix), W, nullptr, T, H / Hkv);
@@ -299,19 +365,19 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
                  float eps, float base, int W, cudaStream_t s) {
     nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
     for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
-    __half* qhat = reinterpret_cast<__half*>(ws);
+    __nv_bfloat16* qhat = reinterpret_cast<__nv_bfloat16*>(ws);
     {
         ProfScope ps("prefill_norm_rope", s);
         nc::prefill_norm_rope_kernel<D><<<tok_grid(static_cast<long long>(B) * C, D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
-            reinterpret_cast<const __nv_bfloat16*>(v), start, qhat, reinterpret_cast<__half*>(kcache),
+            reinterpret_cast<const __nv_bfloat16*>(v), start, qhat, reinterpret_cast<__nv_bfloat16*>(kcache),
             reinterpret_cast<__nv_bfloat16*>(vcache), B, C, H, Hkv, Tcap, eps, th);
     }
     int rc = launch_status();
     if (rc) return rc;
     CUtensorMap tq, tk, tv, to;
-    if (make_tmap(&tq, qhat, B, C, H, D, nc::fwd::BM, kF16) ||
-        make_tmap(&tk, kcache, B, Tcap, Hkv, D, nc::fwd::BN, kF16) ||
+    if (make_tmap(&tq, qhat, B, C, H, D, nc::fwd::BM) ||
+        make_tmap(&tk, kcache, B, Tcap, Hkv, D, nc::fwd::BN) ||
         make_tmap(&tv, vcache, B, Tcap, Hkv, D, nc::fwd::BN) || make_tmap(&to, out, B, C, H, D, nc::fwd::BM))
         return NC_EINVAL;
     const int n_qt = (C + nc::fwd::BM - 1) / nc::fwd::BM;
@@ -322,7 +388,7 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
     const long long nblk = static_cast<long long>(n_pairs) * B * H;
     if (nblk > 0x7fffffffLL) return NC_EINVAL;
     ProfScope ps("attn_prefill", s);
-    nc::fwd::attn_fwd_kernel<D><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
+    nc::fwd::attn_fwd_kernel<D, true><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
         tq, tk, tv, to, lse, C, H, B, n_qt, tile_group(n_pairs, B * H), float(scale * log2e), float(mfix * log2e),
         float(mfix), W, start, Tcap, H / Hkv);
     return launch_status();
@@ -330,7 +396,7 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
 
 template <int D>
 int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
-             const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+             const float* lse, const nc_f16* qhat, const nc_f16* khat, const nc_bf16* dout, nc_bf16* dq,
              nc_bf16* dk, nc_bf16* dv, void* ws, int B, int T, int H, int Hkv, float eps, float base, int W,
              cudaStream_t s) {
     const int Tpad = tpad_of(T);
@@ -341,24 +407,27 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
     float* lse2 = reinterpret_cast<float*>(w);
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
-    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||out_t||, max ||v_t||
+    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||v_t||
+    w += 256;
+    nc_f16* ds = reinterpret_cast<nc_f16*>(w);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    if (cudaMemsetAsync(gmax, 0, 3 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    if (cudaMemsetAsync(gmax, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
     const long long rows = static_cast<long long>(B) * T * H;
     {
         ProfScope ps("attn_bwd_pre", s);
         nc::bwd_pre_kernel<D><<<rows_grid(rows / 4 + 1, D), 256, 0, s>>>(
-            reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout), lse, delta,
-            lse2, gmax, B, T, H, Tpad);
+            reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
+            reinterpret_cast<const __nv_bfloat16*>(v), lse, delta, lse2, gmax, B, T, H, Hkv, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tds;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, Hkv, D, 128, kF16) ||
         make_tmap(&tv, v, B, T, Hkv, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
         make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, Hkv, D, 128) ||
         make_tab_tmap(&ttab, tab, T, D) || make_tmap(&tdq, dq, B, T, H, D, 128) ||
-        make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128))
+        make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128) ||
+        make_ds_tmap(&tds, ds, ds_rows(B, T, H)))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -373,19 +442,110 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         ProfScope ps("attn_bwd_dkdv", s);
         nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk_kv), nc::bwd::NUM_THREADS,
                                            nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, T, H, B, Tpad,
+            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, reinterpret_cast<__half*>(ds), T, H, B, Tpad,
             tile_group(static_cast<int>(n_t), B * Hkv), float(scale), float(scale * 1.4426950408889634), eps, W, G);
     }
     if ((rc = launch_status())) return rc;
     {
-        // query side: dq (one CTA per query tile), after the key side has
-        // published max ||v_t|| for the dS bound
+        // query side: dq = dS khat from the key side's dS^T scratch (one CTA
+        // per query tile)
         ProfScope ps("attn_bwd_dq", s);
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
-                                          nc::bwdq::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tqr, ttab, tdq, lse2, delta, gmax, T, H, B, Tpad, group, float(scale),
-            float(scale * 1.4426950408889634), eps, W, G);
+                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk, tqr, ttab, tdq, gmax, T, H, B,
+                                                                         group, float(scale), eps, W, G);
     }
+    return launch_status();
+}
+
+// FP8 forward workspace: RoPE table, q8 [B][T][H][D], k8 [B][T][Hkv][D],
+// v8^T [B][Hkv][D][Tpad] (E4M3 bytes), per-head max |v| and scale 2^-tau.
+// Sized with Hkv = H (an upper bound).
+struct Fp8Ws {
+    float2* tab;
+    uint8_t *q8, *k8, *v8t;
+    unsigned int* vmax;
+    float* vscale;
+};
+
+size_t fp8_ws_layout(int B, int T, int H, int D, Fp8Ws* out, void* base) {
+    const size_t tok = static_cast<size_t>(B) * T * H * D;
+    const size_t vt = static_cast<size_t>(B) * H * D * tpad_of(T);
+    const size_t o_tab = 0, o_q = o_tab + tab_bytes(T, D), o_k = o_q + up256(tok), o_v = o_k + up256(tok);
+    const size_t o_m = o_v + up256(vt), o_s = o_m + up256(static_cast<size_t>(B) * H * 4);
+    const size_t total = o_s + up256(static_cast<size_t>(B) * H * 4);
+    if (out) {
+        uint8_t* w = reinterpret_cast<uint8_t*>(base);
+        out->tab = reinterpret_cast<float2*>(w + o_tab);
+        out->q8 = w + o_q;
+        out->k8 = w + o_k;
+        out->v8t = w + o_v;
+        out->vmax = reinterpret_cast<unsigned int*>(w + o_m);
+        out->vscale = reinterpret_cast<float*>(w + o_s);
+    }
+    return total;
+}
+
+// [B][T][H][128] E4M3 tensor: boxes of 128 bytes (a whole head row) x 128
+// tokens of one (b, h), 128-byte swizzled.  Rows past T read as zero.
+int make_tmap_e4m3(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H) * D,
+                                   static_cast<cuuint64_t>(T) * H * D};
+    const cuuint32_t box[4] = {128, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode_fn()(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
+// v8^T [B Hkv][D][Tpad] E4M3: boxes of 128 keys (bytes) x D rows of one head.
+int make_tmap_vt(CUtensorMap* tm, const void* ptr, int BH, int D, int Tpad) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Tpad), static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Tpad), static_cast<cuuint64_t>(D) * Tpad};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(D), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode_fn()(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
+}
+
+int fwd_fp8_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
+                 void* ws, int B, int T, int H, int Hkv, float eps, float base, int W, cudaStream_t s) {
+    constexpr int D = nc::fwd8::D;
+    Fp8Ws w;
+    fp8_ws_layout(B, T, H, D, &w, ws);
+    const int Tpad = tpad_of(T);
+    int rc = launch_rope_table(w.tab, pos, T, D, base, s);
+    if (rc) return rc;
+    // q8 = E4M3(qhat 2^5), k8 likewise
+    rc = launch_norm_rope<D, __nv_fp8_e4m3>(q, k, w.tab, w.q8, w.k8, nullptr, B, T, H, Hkv, eps, s, 32.f);
+    if (rc) return rc;
+    if (cudaMemsetAsync(w.vmax, 0, static_cast<size_t>(B) * Hkv * 4, s) != cudaSuccess) return launch_status();
+    {
+        ProfScope ps("v_quant", s);
+        nc::v_absmax_kernel<D><<<dim3((T + 255) / 256, B * Hkv), 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(v), w.vmax, T, Hkv);
+        if ((rc = launch_status())) return rc;
+        nc::v_quant_t_kernel<D><<<dim3(Tpad / 128, B * Hkv), 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(v), w.vmax, w.v8t, w.vscale, T, Tpad, Hkv);
+        if ((rc = launch_status())) return rc;
+    }
+    CUtensorMap tq, tk, tvt, to;
+    if (make_tmap_e4m3(&tq, w.q8, B, T, H, D) || make_tmap_e4m3(&tk, w.k8, B, T, Hkv, D) ||
+        make_tmap_vt(&tvt, w.v8t, B * Hkv, D, Tpad) || make_tmap(&to, out, B, T, H, D, nc::fwd8::BM))
+        return NC_EINVAL;
+    const int n_qt = (T + nc::fwd8::BM - 1) / nc::fwd8::BM;
+    const int n_pairs = (n_qt + 1) / 2;
+    const long long nblk = static_cast<long long>(n_pairs) * B * H;
+    if (nblk > 0x7fffffffLL) return NC_EINVAL;
+    const double craw = 1.0 / (1024.0 * std::sqrt(double(D)));  // raw E4M3 score -> scaled score
+    ProfScope ps("attn_fwd_fp8", s);
+    nc::fwd8::attn_fwd_fp8_kernel<<<static_cast<unsigned>(nblk), nc::fwd8::NUM_THREADS, nc::fwd8::Smem::ALLOC, s>>>(
+        tq, tk, tvt, to, w.vscale, lse, T, H, B, n_qt, tile_group(n_pairs, B * H), float(craw * 1.4426950408889634),
+        float(craw), W, H / Hkv);
     return launch_status();
 }
 
@@ -409,7 +569,7 @@ size_t decode_ws_layout(int B, int H, int D, int Tcap, DecodeWs* out, void* base
     return c_bytes + ml_bytes + o_bytes;
 }
 
-// Keys (fp16) or values (bf16) of a [B][Tcap][Hkv][D] cache as a 4D tensor
+// Keys or values (bf16) of a [B][Tcap][Hkv][D] cache as a 4D tensor
 // map with [sb][Hkv][D] boxes (no swizzle): one copy brings sb whole slots.
 int make_cache_tmap(CUtensorMap* tm, const void* ptr, int B, int Tcap, int Hkv, int D, int sb,
                     CUtensorMapDataType dt) {
@@ -439,7 +599,7 @@ int launch_decode_tma(const CUtensorMap& tk, const CUtensorMap& tv, const nc_bf1
     nc::dec::attn_decode_tma_kernel<D, HPW><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)),
                                               (nwc + 1) * 32, smem, s>>>(
         tk, tv, reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
-        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
+        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(kcache),
         reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
         ws.part_ml, ws.counters, B, H, Hkv, Tcap, nparts, eps, th, scale_log2, W, sb, nst);
     return launch_status();
@@ -461,7 +621,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
         nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0,
                                          s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
-            reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__half*>(kcache),
+            reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(kcache),
             reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
             ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, scale_log2, W, 1);
         return launch_status();
@@ -471,7 +631,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
     const int nst = nc::dec::ring_stages(Hkv, D, sb);
     if (nc::dec::smem_bytes(Hkv, D, sb, nst) > static_cast<size_t>(kDecodeSmemMax)) return NC_EINVAL;
     CUtensorMap tk, tv;
-    if (make_cache_tmap(&tk, kcache, B, Tcap, Hkv, D, sb, kF16) ||
+    if (make_cache_tmap(&tk, kcache, B, Tcap, Hkv, D, sb, kBF16) ||
         make_cache_tmap(&tv, vcache, B, Tcap, Hkv, D, sb, kBF16))
         return NC_EINVAL;
     switch (nc::dec::heads_per_warp(H)) {
@@ -489,7 +649,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
 
 extern "C" {
 
-int nc_version(void) { return (0 << 16) | 2; }
+int nc_version(void) { return (0 << 16) | 3; }
 
 const char* nc_strerror(int code) {
     switch (code) {
@@ -571,12 +731,10 @@ size_t nc_attn_workspace_size(int op, int B, int T, int H, int D) {
     switch (op) {
         case NC_OP_NORM_ROPE:
         case NC_OP_FWD: return tab_bytes(T, D);
-        case NC_OP_BWD: {
-            const int Tpad = tpad_of(T);
-            return tab_bytes(T, D) + 2 * up256(static_cast<size_t>(B) * H * Tpad * 4) + 256;
-        }
+        case NC_OP_BWD: return bwd_ws_bytes(B, T, H, D);
         case NC_OP_DECODE: return decode_ws_layout(B, H, D, T, nullptr, nullptr);
         case NC_OP_PREFILL: return up256(static_cast<size_t>(B) * T * H * D * 2);  // qhat of the chunk
+        case NC_OP_FWD_FP8: return D == nc::fwd8::D ? fp8_ws_layout(B, T, H, D, nullptr, nullptr) : 0;
         default: return 0;
     }
 }
@@ -590,22 +748,29 @@ int nc_qk_norm_rope(const nc_bf16* x, const int32_t* pos, nc_bf16* xhat, float* 
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_NORM_ROPE, B, T, H, D)) return NC_EINVAL;
     int rc = device_ready();
     if (rc) return rc;
+    if (kChecked) {
+        const size_t n = static_cast<size_t>(B) * T * H * D * 2;
+        CallRanges cr;
+        cr.in(x, n), cr.in(pos, pos ? T * 4 : 0), cr.out(xhat, n), cr.out(rstd, rstd ? n / (2 * D) * 4 : 0);
+        cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float2* tab = reinterpret_cast<float2*>(workspace);
     if ((rc = launch_rope_table(tab, pos, T, D, rope_base, s))) return rc;
-    return D == 64 ? launch_norm_rope<64>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s)
-                   : launch_norm_rope<128>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s);
+    return D == 64 ? launch_norm_rope<64, __nv_bfloat16>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s)
+                   : launch_norm_rope<128, __nv_bfloat16>(x, nullptr, tab, xhat, nullptr, rstd, B, T, H, H, eps, s);
 }
 
 int nc_attn_fwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
-                float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
+                float* lse, nc_f16* qhat, nc_f16* khat, float* rstd, void* workspace, size_t workspace_bytes,
                 int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream) {
     return nc_attn_fwd_ex(q, k, v, pos, out, lse, qhat, khat, rstd, workspace, workspace_bytes, B, T, H, D, eps,
                           rope_base, 0, 0, stream);
 }
 
 int nc_attn_fwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
-                   float* lse, nc_bf16* qhat, nc_bf16* khat, float* rstd, void* workspace, size_t workspace_bytes,
+                   float* lse, nc_f16* qhat, nc_f16* khat, float* rstd, void* workspace, size_t workspace_bytes,
                    int B, int T, int H, int D, float eps, float rope_base, int window, int kv_heads,
                    nc_stream_t stream) {
     if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
@@ -618,6 +783,14 @@ int nc_attn_fwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_FWD, B, T, H, D)) return NC_EINVAL;
     int rc = device_ready();
     if (rc) return rc;
+    if (kChecked) {
+        const size_t tq = static_cast<size_t>(B) * T * H * D * 2, tk = tq / H * kv_heads_of(kv_heads, H);
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k, tk), cr.in(v, tk), cr.in(pos, pos ? T * 4 : 0);
+        cr.out(out, tq), cr.out(qhat, tq), cr.out(khat, tk), cr.out(lse, static_cast<size_t>(B) * H * T * 4);
+        cr.out(rstd, rstd ? (tq + tk) / (2 * D) * 4 : 0), cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, T);
     const int Hkv = kv_heads_of(kv_heads, H);
@@ -627,8 +800,32 @@ int nc_attn_fwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
                                    W, s);
 }
 
+int nc_attn_fwd_fp8(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out,
+                    float* lse, void* workspace, size_t workspace_bytes, int B, int T, int H, int D, float eps,
+                    float rope_base, int window, int kv_heads, nc_stream_t stream) {
+    if (!shape_ok(B, T, H, D) || D != nc::fwd8::D || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
+    if (H > 0 && !kv_heads_of(kv_heads, H)) return NC_EINVAL;
+    if (B == 0 || T == 0 || H == 0) return NC_OK;
+    if (!q || !k || !v || !out || !workspace) return NC_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned256(workspace) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return NC_EINVAL;
+    if (workspace_bytes < nc_attn_workspace_size(NC_OP_FWD_FP8, B, T, H, D)) return NC_EINVAL;
+    int rc = device_ready();
+    if (rc) return rc;
+    if (kChecked) {
+        const size_t tq = static_cast<size_t>(B) * T * H * D * 2, tk = tq / H * kv_heads_of(kv_heads, H);
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k, tk), cr.in(v, tk), cr.in(pos, pos ? T * 4 : 0);
+        cr.out(out, tq), cr.out(lse, lse ? static_cast<size_t>(B) * H * T * 4 : 0), cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
+    return fwd_fp8_impl(q, k, v, pos, out, lse, workspace, B, T, H, kv_heads_of(kv_heads, H), eps, rope_base,
+                        window_eff(window, T), reinterpret_cast<cudaStream_t>(stream));
+}
+
 int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
-                const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+                const float* lse, const nc_f16* qhat, const nc_f16* khat, const nc_bf16* dout, nc_bf16* dq,
                 nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
                 float eps, float rope_base, nc_stream_t stream) {
     return nc_attn_bwd_ex(q, k, v, pos, out, lse, qhat, khat, dout, dq, dk, dv, workspace, workspace_bytes, B, T, H,
@@ -636,7 +833,7 @@ int nc_attn_bwd(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int3
 }
 
 int nc_attn_bwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, const nc_bf16* out,
-                   const float* lse, const nc_bf16* qhat, const nc_bf16* khat, const nc_bf16* dout, nc_bf16* dq,
+                   const float* lse, const nc_f16* qhat, const nc_f16* khat, const nc_bf16* dout, nc_bf16* dq,
                    nc_bf16* dk, nc_bf16* dv, void* workspace, size_t workspace_bytes, int B, int T, int H, int D,
                    float eps, float rope_base, int window, int kv_heads, nc_stream_t stream) {
     if (!shape_ok(B, T, H, D) || !params_ok(eps, rope_base) || window < 0) return NC_EINVAL;
@@ -648,9 +845,18 @@ int nc_attn_bwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
     for (const void* p : b16)
         if (!aligned16(p)) return NC_EINVAL;
     if (!aligned256(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return NC_EINVAL;
+    if (2 * ds_rows(B, T, H) >= (1LL << 31)) return NC_EINVAL;  // the dS^T scratch's TMA row coordinates
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_BWD, B, T, H, D)) return NC_EINVAL;
     int rc = device_ready();
     if (rc) return rc;
+    if (kChecked) {
+        const size_t tq = static_cast<size_t>(B) * T * H * D * 2, tk = tq / H * kv_heads_of(kv_heads, H);
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k, tk), cr.in(v, tk), cr.in(pos, pos ? T * 4 : 0), cr.in(out, tq);
+        cr.in(lse, static_cast<size_t>(B) * H * T * 4), cr.in(qhat, tq), cr.in(khat, tk), cr.in(dout, tq);
+        cr.out(dq, tq), cr.out(dk, tk), cr.out(dv, tk), cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, T);
     const int Hkv = kv_heads_of(kv_heads, H);
@@ -683,6 +889,15 @@ int nc_attn_decode_ex(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_n
     if (H * (D / 8) > 512) return NC_EINVAL;  // at most 512 / (D/8) heads
     int rc = device_ready();
     if (rc) return rc;
+    if (kChecked) {
+        const int Hkv = kv_heads_of(kv_heads, H);
+        const size_t tq = static_cast<size_t>(B) * H * D * 2, tn = static_cast<size_t>(B) * Hkv * D * 2;
+        const size_t tc = static_cast<size_t>(B) * Tcap * Hkv * D * 2;
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k_new, k_new ? tn : 0), cr.in(v_new, v_new ? tn : 0), cr.in(lens, B * 4);
+        cr.out(kcache, tc), cr.out(vcache, tc), cr.out(out, tq), cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     DecodeWs ws;
     decode_ws_layout(B, H, D, Tcap, &ws, workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -711,6 +926,16 @@ int nc_attn_prefill(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const 
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_PREFILL, B, C, H, D)) return NC_EINVAL;
     int rc = device_ready();
     if (rc) return rc;
+    if (kChecked) {
+        const int Hkv = kv_heads_of(kv_heads, H);
+        const size_t tq = static_cast<size_t>(B) * C * H * D * 2, tk = static_cast<size_t>(B) * C * Hkv * D * 2;
+        const size_t tc = static_cast<size_t>(B) * Tcap * Hkv * D * 2;
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k, tk), cr.in(v, tk), cr.in(start, B * 4);
+        cr.out(kcache, tc), cr.out(vcache, tc), cr.out(out, tq), cr.out(lse, lse ? static_cast<size_t>(B) * H * C * 4 : 0);
+        cr.out(workspace, workspace_bytes);
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = window_eff(window, Tcap);
     const int Hkv = kv_heads_of(kv_heads, H);
@@ -766,7 +991,7 @@ int scratch_address(void** out) {
 
 extern "C" {
 
-int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_f16* kcache,
+int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc_bf16* kcache,
                            nc_bf16* vcache, const int32_t* lens, nc_bf16* out, int B, int H, int D, int Tcap,
                            float eps, float rope_base, nc_stream_t stream) {
     if (!shape_ok(B, Tcap, H, D) || !params_ok(eps, rope_base)) return NC_EINVAL;
@@ -783,6 +1008,14 @@ int nc_attn_decode_noalloc(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16
     if (rc) return rc;
     void* scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
+    if (kChecked) {
+        const size_t tq = static_cast<size_t>(B) * H * D * 2, tc = static_cast<size_t>(B) * Tcap * H * D * 2;
+        CallRanges cr;
+        cr.in(q, tq), cr.in(k_new, k_new ? tq : 0), cr.in(v_new, v_new ? tq : 0), cr.in(lens, B * 4);
+        cr.out(kcache, tc), cr.out(vcache, tc), cr.out(out, tq);
+        cr.out(scratch, nc_attn_workspace_size(NC_OP_DECODE, B, Tcap, H, D));
+        if ((rc = cr.publish(reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
     DecodeWs ws;
     decode_ws_layout(B, H, D, Tcap, &ws, scratch);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -2,46 +2,33 @@
 // (tcgen05 + TMEM + TMA), with the RoPE transpose and the RMSNorm backward
 // fused into the epilogue, so dq leaves the kernel finished (bf16).
 //
-// One CTA owns one 128-query tile i of one (batch, head) and walks the key
-// tiles j <= i that it can see (all of them, or with a sliding window W --
-// query q sees key k when 0 <= q - k < W -- those from the tile of the first
-// query's oldest visible key), recomputing what it needs from the forward's
-// lse:
-//   S_j   = qhat_i khat_j^T                 (M=128 queries, N=128 keys, K=D)
-//   P_j   = exp2(S_j * scale*log2e - lse2_i)
-//   dP_j  = dout_i v_j^T                    (M=128 queries, N=128 keys, K=D)
-//   dS_j  = P_j o (dP_j - delta_i)
-//   dQ_i += dS_j khat_j                     (M=128 queries, N=D, K=128 keys)
-// Every dQ element is produced by exactly one CTA: no atomics, no fp32
-// accumulator in global memory, deterministic results.
+// The key-side kernel (nc_bwd.cuh) forms every visible block of
+//   dS = P o (dP - delta)
+// anyway (for dK), and writes it once, transposed (keys on rows), to a
+// scratch buffer in HBM: the dS^T block of (query tile i, key tile j) of one
+// (batch, query head) is a [128 keys][128 queries] fp16 tile holding
+// alpha * dS (alpha: the call's one power-of-two scale, ds_scale_global,
+// undone in the epilogue).  This kernel
+// is then a streaming GEMM per query tile,
+//   dQhat_i = sum_j dS_ij khat_j          (M=128 queries, N=D, K=128 keys per tile),
+// that reads each dS block once (32 KB per 128 x D x 128 product: it is HBM
+// bound), recomputes nothing and uses no atomics: each dQ element is
+// produced by exactly one CTA.
 //
-// Tensor memory: two S buffers (S_j in buffer j%2; the fp16 dS_j is written
-// over it in place and read from there as the A operand of the dQ product),
-// dP (128 columns) and the dQ accumulator (D columns).
-//
-// Issue order (one thread's MMAs execute in issue order):
-//   S_0, S_1, dP_0 | [dP_j in registers] dP_{j+1} | [dS_j in TMEM] dQ(j), S_{j+2} | ...
-// dS_j is written over S_j, not over dP_j, so the next dP may start as soon
-// as the softmax warps have loaded dP_j: it runs while they form dS_j, and
-// dQ(j) and S_{j+2} run while they form P_{j+1}.  K tiles
-// sit in a 3-stage ring (tile j is read by S_j and by dQ(j) two steps later),
-// V tiles in a 2-stage ring.
-//
-// Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 query rows,
-// key half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end the same
-// eight warps (two threads per query row) stage dq in shared memory and it
-// leaves through TMA stores.  The raw q rows and RoPE table rows it needs
-// are prefetched while the last key tiles are processed, into the v stage
-// and the two k stages the last key tile does not use, as they free up.
-//
-// dS is stored as alpha * dS in fp16 with a per-CTA power of two alpha from
-// the bound |dS_ij| <= P_ij |dP_ij - delta_i| <= ||dout_i|| max_j ||v_j|| +
-// |delta_i| (max_j ||v_j|| over the whole tensor, published by the dK/dV
-// kernel), so |alpha dS| <= 2^14.
+// One CTA per 128-query tile i of one (batch, head), walking the key tiles
+// j it can see (j <= i; with a sliding window W -- query q sees key k when
+// 0 <= q - k < W -- from the tile of the first query's oldest visible key):
+//   warp 8      TMA producer: (dS^T block, khat tile) pairs into an NST-stage ring
+//   warp 9      MMA issuer (one thread): A = alpha dS (the MN-major view of
+//               the dS^T tile), B = khat (MN-major), both fp16, fp32
+//               accumulator in TMEM
+//   warps 0-7   epilogue: two threads per query row apply RoPE^T and the
+//               RMSNorm backward to dQhat, stage dq, TMA store
+// The raw q rows and the RoPE table rows that the epilogue needs are loaded
+// into ring stages as the last tiles free them.
 #pragma once
 
 #include "nc_common.cuh"
-#include <type_traits>
 #include "nc_normrope_bwd.cuh"
 
 namespace nc {
@@ -49,65 +36,63 @@ namespace bwdq {
 
 constexpr int BM = 128;  // queries per CTA
 constexpr int BN = 128;  // keys per tile
-constexpr int KSTAGES = 3;
+constexpr int NST = 3;   // ring stages
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int NUM_THREADS = 10 * 32;
-constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in per block
 
 enum Bar {
-    QD_FULL = 0,   // qhat_i and dout_i landed
-    K_FULL = 1,    // +stage (3)
-    K_EMPTY = 4,   // +stage (3)
-    V_FULL = 7,    // +stage (2)
-    V_EMPTY = 9,   // +stage (2)
-    S_FULL = 11,   // +buffer (2)
-    DP_FULL = 13,
-    DS_FULL = 14,  // softmax read dP_j and wrote dS_j
-    DQ_FULL = 15,
-    MMA_DONE = 16,
-    EPI_FULL = 17,  // raw q tile and RoPE table tile staged for the dq epilogue
-    DP_READ = 18,   // the softmax warps hold dP_j in registers: dP_{j+1} may start
-    NUM_BARS = 19
+    FULL = 0,      // +stage
+    EMPTY = 3,     // +stage
+    DQ_FULL = 6,
+    EPI_FULL = 7,  // raw q tile and RoPE table tile staged for the epilogue
+    MMA_DONE = 8,
+    NUM_BARS = 9
 };
+
+// Index of the dS^T block (query tile i, key tile j <= i) of one (batch,
+// query head) bh in the scratch: the causal triangle of each (b, h), in
+// row-major order.  Both backward kernels address the scratch through it.
+__host__ __device__ __forceinline__ long long ds_block(long long bh, int n_t, int i, int j) {
+    return bh * (static_cast<long long>(n_t) * (n_t + 1) / 2) + static_cast<long long>(i) * (i + 1) / 2 + j;
+}
+
+// Element offset inside one 16384-element dS^T block of dS^T[key][query]:
+// the block is two [128 keys][64 queries] row-major halves (queries
+// 64 h .. 64 h + 63), so that a 128-byte TMA box row is one key's 64 queries.
+__host__ __device__ __forceinline__ int ds_offset(int key, int query) {
+    return (query >> 6) * 8192 + key * 64 + (query & 63);
+}
 
 template <int D>
 struct Smem {
-    static constexpr int TBYTES = BN * D * 2;  // one 128-row tile of D 16-bit values
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_DO = OFF_Q + TBYTES;
-    static constexpr int OFF_K = OFF_DO + TBYTES;         // KSTAGES stages
-    static constexpr int OFF_V = OFF_K + KSTAGES * TBYTES;  // 2 stages
-    static constexpr int OFF_BAR = OFF_V + 2 * TBYTES;
+    static constexpr int DSBYTES = BN * BM * 2;  // one dS^T block
+    static constexpr int KBYTES = BN * D * 2;    // one khat tile
+    static constexpr int STAGE = DSBYTES + KBYTES;
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_BAR = OFF_RING + NST * STAGE;
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
-    static constexpr int OFF_MISC = OFF_TSLOT + 16;  // 4 warp maxima of the dS bound
-    static constexpr int BYTES = OFF_MISC + 32;
-    static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
-    // epilogue: the raw q tile over a v stage, the RoPE table tile (fp32
-    // [128][D]) over two k stages, dq staged over the qhat tile and the
-    // row-half exchange over the dout tile
+    static constexpr int BYTES = OFF_TSLOT + 16;
+    static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
+    // epilogue (over the ring once its stages are free): raw q [128][D] bf16
+    // and the first half of the RoPE table [128][D] fp32 in stage s_a, the
+    // second half of the table in stage s_b (the stages of tiles n_kv - 2 and
+    // n_kv - 3), the dq staging tile and the row-half exchange in the last
+    // tile's stage
+    static constexpr int XBYTES = BM * D * 2;
     static constexpr int CBYTES = BM * D * 4;
-    static_assert(BYTES <= SMEM_LIMIT, "dQ tiles exceed shared memory");
-    static_assert(CBYTES == 2 * TBYTES && 2 * BM * 8 <= TBYTES, "epilogue tiles exceed the rings");
+    static_assert(XBYTES + CBYTES / 2 <= STAGE && XBYTES + 2 * BM * 8 <= STAGE, "epilogue tiles exceed the stages");
+    static_assert(ALLOC <= 232448, "dQ ring exceeds shared memory");
 };
 
-constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t tm_s(int buf) { return static_cast<uint32_t>(buf) * 128u; }
-constexpr uint32_t TM_DP = 256;
-constexpr uint32_t TM_DQ = 384;  // D columns
-
-// TMEM column of the packed pair holding keys (2c, 2c+1) of K-step kk: key
-// half kk/4 sits inside the S columns its own warps read.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8); }
+constexpr uint32_t TMEM_COLS = 128;  // the dQ accumulator (D <= 128 columns)
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
-                       const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
-                       const float* __restrict__ delta, const unsigned int* __restrict__ gmax, int T, int H, int B,
-                       int Tpad, int group, float scale, float scale_log2, float eps, int W, int G) {
+                       const __grid_constant__ CUtensorMap tm_dq, const unsigned int* __restrict__ gmax, int T,
+                       int H, int B, int group, float scale, float eps, int W, int G) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
     extern __shared__ uint8_t smem_raw[];
@@ -127,30 +112,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int kt_lo = max(0, qt * BM - W + 1) / BN;  // first visible key tile (W >= 2^30: none cut)
     const int n_kv = qt - kt_lo + 1;                  // BM == BN: key tiles kt_lo..qt
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
+    auto stage = [&](int s) -> uint32_t { return sb + S::OFF_RING + s * S::STAGE; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
-    float* misc = reinterpret_cast<float*>(smem + S::OFF_MISC);
-    const long long bh = static_cast<long long>(b) * H + h;
-    // epilogue space: the v stage of key tile n_kv-2 and the k stages of
-    // tiles n_kv-3 and n_kv-2 (never used when those tiles do not exist)
-    const int vs_epi = n_kv & 1, ks_a = n_kv % KSTAGES, ks_b = (n_kv + 1) % KSTAGES;
+    const long long blk0 = ds_block(tc.bh, n_qt, qt, 0);  // dS^T block of key tile 0
+    // epilogue space: the stages of tiles n_kv - 2 (s_a) and n_kv - 3 (s_b),
+    // free from the start when those tiles do not exist, and the last tile's
+    const int s_last = (n_kv - 1) % NST, s_a = (n_kv + 1) % NST, s_b = n_kv % NST;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(QD_FULL), 1);
-        for (int s = 0; s < KSTAGES; ++s) {
-            mbar_init(bar(K_FULL + s), 1);
-            mbar_init(bar(K_EMPTY + s), 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar(FULL + s), 1);
+            mbar_init(bar(EMPTY + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(V_FULL + s), 1);
-            mbar_init(bar(V_EMPTY + s), 1);
-            mbar_init(bar(S_FULL + s), 1);
-        }
-        mbar_init(bar(DP_FULL), 1);
-        mbar_init(bar(DS_FULL), 8);   // one arrival per softmax warp
-        mbar_init(bar(DP_READ), 8);
         mbar_init(bar(DQ_FULL), 1);
-        mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
+        mbar_init(bar(MMA_DONE), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -165,128 +141,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_TMA) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
-            int issued_k[KSTAGES] = {0, 0, 0}, issued_v[2] = {0, 0};
-            mbar_expect_tx(bar(QD_FULL), 2 * S::TBYTES);
-            for (int c = 0; c < NC; ++c) {
-                tma_load_4d(sb + S::OFF_Q + c * (BM * 128), &tm_q, c * 64, h, qt * BM, b, bar(QD_FULL));
-                tma_load_4d(sb + S::OFF_DO + c * (BM * 128), &tm_do, c * 64, h, qt * BM, b, bar(QD_FULL));
-            }
+            int issued[NST] = {0, 0, 0};
+            bool ok = true;
             for (int j = 0; j < n_kv; ++j) {
-                const int ks = j % KSTAGES, vs = j & 1;
-                if (j >= KSTAGES && !mbar_wait(bar(K_EMPTY + ks), (j / KSTAGES - 1) & 1, 0x121)) break;
-                mbar_expect_tx(bar(K_FULL + ks), S::TBYTES);
+                const int s = j % NST;
+                if (j >= NST && !mbar_wait(bar(EMPTY + s), (j / NST - 1) & 1, 0x121)) {
+                    ok = false;
+                    break;
+                }
+                const int kt = kt_lo + j;
+                mbar_expect_tx(bar(FULL + s), S::STAGE);
+                const int row = static_cast<int>((blk0 + kt) * 2 * BN);  // < 2^31 (checked by the host)
+                for (int c = 0; c < 2; ++c)
+                    tma_load_2d(stage(s) + c * (BN * 128), &tm_ds, 0, row + c * BN, bar(FULL + s));
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_K + ks * S::TBYTES + c * (BN * 128), &tm_k, c * 64, hk, (kt_lo + j) * BN, b,
-                                bar(K_FULL + ks));
-                ++issued_k[ks];
-                if (j >= 2 && !mbar_wait(bar(V_EMPTY + vs), ((j >> 1) - 1) & 1, 0x122)) break;
-                mbar_expect_tx(bar(V_FULL + vs), S::TBYTES);
-                for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + vs * S::TBYTES + c * (BN * 128), &tm_v, c * 64, hk, (kt_lo + j) * BN, b,
-                                bar(V_FULL + vs));
-                ++issued_v[vs];
+                    tma_load_4d(stage(s) + S::DSBYTES + c * (BN * 128), &tm_k, c * 64, hk, kt * BN, b,
+                                bar(FULL + s));
+                ++issued[s];
             }
-            // dq epilogue tiles, each as soon as its stage is released
-            mbar_expect_tx(bar(EPI_FULL), S::TBYTES + S::CBYTES);
-            bool epi = n_kv < 2 || mbar_wait(bar(V_EMPTY + vs_epi), ((n_kv - 2) >> 1) & 1, 0x128);
+            // epilogue tiles, each as soon as its stage is released
+            mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
+            bool epi = ok && (n_kv < 2 || mbar_wait(bar(EMPTY + s_a), ((n_kv - 2) / NST) & 1, 0x128));
             if (epi) {
                 for (int c = 0; c < NC; ++c)
-                    tma_load_4d(sb + S::OFF_V + vs_epi * S::TBYTES + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM,
-                                b, bar(EPI_FULL));
+                    tma_load_4d(stage(s_a) + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM, b, bar(EPI_FULL));
+                for (int c = 0; c < NC; ++c)
+                    tma_load_2d(stage(s_a) + S::XBYTES + c * (BM * 128), &tm_tab, c * 32, qt * BM, bar(EPI_FULL));
             }
-            epi = epi && (n_kv < 3 || mbar_wait(bar(K_EMPTY + ks_a), ((n_kv - 3) / KSTAGES) & 1, 0x129));
+            epi = epi && (n_kv < 3 || mbar_wait(bar(EMPTY + s_b), ((n_kv - 3) / NST) & 1, 0x129));
             if (epi) {
                 for (int c = 0; c < NC; ++c)
-                    tma_load_2d(sb + S::OFF_K + ks_a * S::TBYTES + c * (BM * 128), &tm_tab, c * 32, qt * BM,
-                                bar(EPI_FULL));
-            }
-            epi = epi && (n_kv < 2 || mbar_wait(bar(K_EMPTY + ks_b), ((n_kv - 2) / KSTAGES) & 1, 0x12a));
-            if (epi) {
-                for (int c = 0; c < NC; ++c)
-                    tma_load_2d(sb + S::OFF_K + ks_b * S::TBYTES + c * (BM * 128), &tm_tab, (NC + c) * 32,
-                                qt * BM, bar(EPI_FULL));
+                    tma_load_2d(stage(s_b) + c * (BM * 128), &tm_tab, (NC + c) * 32, qt * BM, bar(EPI_FULL));
             }
             // never leave the CTA with a bulk copy still in flight
-            mbar_wait(bar(QD_FULL), 0, 0x123);
-            for (int s = 0; s < KSTAGES; ++s)
-                if (issued_k[s]) mbar_wait(bar(K_FULL + s), (issued_k[s] - 1) & 1, 0x124);
-            for (int s = 0; s < 2; ++s)
-                if (issued_v[s]) mbar_wait(bar(V_FULL + s), (issued_v[s] - 1) & 1, 0x125);
+            for (int s = 0; s < NST; ++s)
+                if (issued[s]) mbar_wait(bar(FULL + s), (issued[s] - 1) & 1, 0x124);
             if (epi) mbar_wait(bar(EPI_FULL), 0, 0x127);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------- MMA issuer -----
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);   // qhat x khat^T
-            constexpr uint32_t IDESC_DP = idesc_bf16(BM, BN, 0, 0);  // dout x v^T
-            constexpr uint32_t IDESC_DQ = idesc_f16(BM, D, 0, 1);    // dS (TMEM) x khat (MN-major)
-            auto issue_s = [&](int j) {
-                const uint32_t k_s = sb + S::OFF_K + (j % KSTAGES) * S::TBYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    mma_bf16(tmem + tm_s(j & 1), sdesc_sw128(sb + S::OFF_Q + off, 16, 1024),
-                             sdesc_sw128(k_s + off, 16, 1024), IDESC_S, kk > 0);
+            constexpr uint32_t IDESC = idesc_f16(BM, D, 1, 1);  // alpha dS (MN-major) x khat (MN-major), fp16
+            bool ok = true;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % NST;
+                if (!mbar_wait(bar(FULL + s), (j / NST) & 1, 0x221)) {
+                    ok = false;
+                    break;
                 }
-                mma_commit(bar(S_FULL + (j & 1)));
-            };
-            auto issue_dp = [&](int j) {
-                const uint32_t v_s = sb + S::OFF_V + (j & 1) * S::TBYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_DP, sdesc_sw128(sb + S::OFF_DO + off, 16, 1024),
-                             sdesc_sw128(v_s + off, 16, 1024), IDESC_DP, kk > 0);
-                }
-                mma_commit(bar(DP_FULL));
-                mma_commit(bar(V_EMPTY + (j & 1)));
-            };
-            auto wait_k = [&](int j) { return mbar_wait(bar(K_FULL + j % KSTAGES), (j / KSTAGES) & 1, 0x221); };
-            auto wait_v = [&](int j) { return mbar_wait(bar(V_FULL + (j & 1)), (j >> 1) & 1, 0x222); };
-            bool ok = mbar_wait(bar(QD_FULL), 0, 0x220) && wait_k(0);
-            if (ok) {
                 tc_fence_after();
-                issue_s(0);
-            }
-            if (ok && n_kv > 1) {
-                ok = wait_k(1);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(1);
-                }
-            }
-            if (ok) {
-                ok = wait_v(0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_dp(0);
-                }
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                // dP_{j+1} as soon as the softmax warps hold dP_j
-                if (j + 1 < n_kv) {
-                    if (!mbar_wait(bar(DP_READ), j & 1, 0x225) || !wait_v(j + 1)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_dp(j + 1);
-                }
-                // dQ += dS_j khat_j, dS_j from TMEM
-                if (!mbar_wait(bar(DS_FULL), j & 1, 0x223)) { ok = false; break; }
-                tc_fence_after();
-                {
-                    const uint32_t k_s = sb + S::OFF_K + (j % KSTAGES) * S::TBYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ts(tmem + TM_DQ, tmem + tm_s(j & 1) + packed_col(kk),
-                               sdesc_sw128(k_s + kk * (16 * 128), BN * 128, 1024), IDESC_DQ,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(K_EMPTY + j % KSTAGES));
-                }
-                if (j + 2 < n_kv) {
-                    if (!wait_k(j + 2)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_s(j + 2);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16(tmem, sdesc_sw128(stage(s) + kk * (16 * 128), BN * 128, 1024),
+                             sdesc_sw128(stage(s) + S::DSBYTES + kk * (16 * 128), BN * 128, 1024), IDESC,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(EMPTY + s));
             }
             if (ok) mma_commit(bar(DQ_FULL));
             // all MMAs issued by this thread complete before teardown
@@ -295,116 +205,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------- P, dS ----
-        const int quarter = warp & 3, half = warp >> 2;
-        const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
-        const int q = qt * BM + row;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const int cbase = half * 64;  // this warp's key columns
-        const float lse2_row = lse2[bh * Tpad + q];  // +inf on padded rows: P = 0
-        const float delta_row = delta[bh * Tpad + q];
-        bool ok = mbar_wait_warp(bar(QD_FULL), 0, 0x320);
-        // dS scale: the largest per-row bound over the tile
-        if (half == 0) {
-            float dn = 0.f;
-            if (ok) {
-#pragma unroll 4
-                for (int g = 0; g < D / 8; ++g) {
-                    float f[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(smem + S::OFF_DO + (g >> 3) * (BM * 128) +
-                                                                  sw128_offset(row, g & 7)),
-                                  f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dn = fmaf(f[i], f[i], dn);
-                }
-            }
-            float bound = sqrtf(dn) * __uint_as_float(gmax[2]) + fabsf(delta_row);
-            if (!(bound < 3.0e38f)) bound = 3.0e38f;  // padded rows: delta 0, dout 0
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) bound = fmaxf(bound, __shfl_xor_sync(0xffffffffu, bound, o));
-            if (lane == 0) misc[quarter] = bound;
-        }
-        named_bar_sync(1, 256);
-        const float alpha = ds_scale_for(fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3])) * 1.0625f);
-        // P feeds only dS here (no product reads it), so it stays in fp32
-        // registers, and alpha (a power of two) rides in the exponent:
-        // alpha P = exp2(S scale log2e - (lse2 - log2 alpha)).
-        const float lse2a = lse2_row - static_cast<float>(ilogbf(alpha));
-        for (int j = 0; ok && j < n_kv; ++j) {
-            if (!mbar_wait_warp(bar(S_FULL + (j & 1)), (j >> 1) & 1, 0x321)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t ts = tmem + lane_base + tm_s(j & 1) + cbase;
-            // alpha P over this half's 64 keys.  Tiles with masked entries (the
-            // diagonal one: key > query; at the far end of a window: query - key
-            // >= W) take their own copy of the loop, so the other tiles pay
-            // nothing for the mask.
-            float pa[64];
-            {
-                uint32_t r[2][32];
-                tmem_ld32(ts, r[0]);
-                tmem_ld32(ts + 32, r[1]);
-                tmem_wait_ld();
-                const int kt = kt_lo + j;                     // key tile
-                const int d0 = (qt - kt) * BN + row - cbase;  // query - key at this thread's first column
-                auto exp_tile = [&](auto masked) {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            float p = ex2(fmaf(__uint_as_float(r[c][e]), scale_log2, -lse2a));
-                            if constexpr (decltype(masked)::value) {
-                                const int dd = d0 - (c * 32 + e);  // visible: 0 <= dd < W
-                                if (dd < 0 || dd >= W) p = 0.f;
-                            }
-                            pa[c * 32 + e] = p;
-                        }
-                };
-                if (kt < qt && (qt - kt) * BM + BM - 1 < W)
-                    exp_tile(std::false_type{});
-                else
-                    exp_tile(std::true_type{});
-            }
-            if (!mbar_wait_warp(bar(DP_FULL), j & 1, 0x322)) { ok = false; break; }
-            tc_fence_after();
-            {
-                uint32_t r[2][32];
-                tmem_ld32(tmem + lane_base + TM_DP + cbase, r[0]);
-                tmem_ld32(tmem + lane_base + TM_DP + cbase + 32, r[1]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive_warp(bar(DP_READ));  // dP_j is in registers: the next dP may overwrite it
-                // alpha dS = (alpha P) o (dP - delta) as fp16 pairs
-                uint32_t w[32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float d0 = pa[c * 32 + e] * (__uint_as_float(r[c][e]) - delta_row);
-                        const float d1 = pa[c * 32 + e + 1] * (__uint_as_float(r[c][e + 1]) - delta_row);
-                        w[c * 16 + e / 2] = pack_f16x2(d0, d1);
-                    }
-                // dS over this half's own S columns (already read)
-                tmem_st16(ts, w);
-                tmem_st16(ts + 16, w + 16);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive_warp(bar(DS_FULL));
-        }
-        // ------------------------------------------------------ epilogue ----
+        // ---------------------------------------------------- epilogue ----
         // Every barrier below is reached by all 256 threads; the AND-barriers
         // keep their branches uniform even if a wait timed out somewhere.
-        bool epi = named_bar_and(1, 256, ok && mbar_wait_warp(bar(DQ_FULL), 0, 0x323));
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        bool epi = named_bar_and(1, 256, mbar_wait_warp(bar(DQ_FULL), 0, 0x323));
         epi = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), 0, 0x324));
         if (epi) tc_fence_after();
+        uint8_t* last = smem + S::OFF_RING + s_last * S::STAGE;
+        uint8_t* sa = smem + S::OFF_RING + s_a * S::STAGE;
         // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha))
-        norm_rope_bwd_stage<D>(epi, tmem + lane_base + TM_DQ, scale / alpha, smem + S::OFF_V + vs_epi * S::TBYTES,
-                               smem + S::OFF_K + ks_a * S::TBYTES, smem + S::OFF_K + ks_b * S::TBYTES, row, half,
-                               eps, reinterpret_cast<float2*>(smem + S::OFF_DO), smem + S::OFF_Q, 1, 256);
+        const float alpha = ds_scale_global(gmax);
+        norm_rope_bwd_stage<D>(epi, tmem + lane_base, scale / alpha, sa, sa + S::XBYTES, smem + S::OFF_RING + s_b * S::STAGE,
+                               row, half, eps, reinterpret_cast<float2*>(last + S::XBYTES), last, 1, 256);
         if (epi) fence_proxy_async_smem();
         named_bar_sync(1, 256);
         if (epi && threadIdx.x == 0) {
-            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dq, sb + S::OFF_Q + c * (BM * 128), c * 64, h, qt * BM, b);
+            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dq, smem_u32(last) + c * (BM * 128), c * 64, h, qt * BM, b);
             bulk_commit();
             bulk_wait_read_all();  // the staged tile stays valid until the stores have read it
         }

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace nc {
 
 // ----------------------------------------------------------------- status ---
@@ -18,6 +20,7 @@ __device__ unsigned int g_dev_status = 0;
 
 enum : unsigned int {
     DEV_ERR_TIMEOUT = 1,  // a bounded mbarrier wait gave up
+    DEV_ERR_BOUNDS = 4,   // (bounds-checked build) an access outside every registered tensor
 };
 
 // A wait that has not completed after this long is treated as a failure:
@@ -33,6 +36,39 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ void flag_error(unsigned int code, unsigned int site) {
     atomicCAS(&g_dev_status, 0u, (code << 16) | (site & 0xffffu));
 }
+
+// ------------------------------------------------------- bounds checking --
+// The bounds-checked build (compiled with -DNC_CHECK) keeps, per device, the
+// byte ranges of the tensors the current call may write (its outputs and
+// workspace) and may read (all of its tensors), registered by the entry point
+// on the launch stream before its kernels.  Every raw global store goes
+// through NC_IN_RANGE and the decode kernels' raw cache loads through
+// NC_IN_RANGE_LOAD: an access outside every registered range is skipped and
+// recorded as DEV_ERR_BOUNDS with its site.  TMA copies need no check: the tensor maps
+// clip them to their tensors.  In the normal build NC_IN_RANGE is `true` and
+// the code is unchanged.
+constexpr int CHECK_MAX_RANGES = 24;
+struct CheckRanges {
+    unsigned long long lo[CHECK_MAX_RANGES], hi[CHECK_MAX_RANGES];
+    int n;
+};
+#ifdef NC_CHECK
+__device__ CheckRanges g_check_write;  // outputs and workspace of the current call
+__device__ CheckRanges g_check_read;   // every tensor of the current call
+__device__ __forceinline__ bool in_range(const CheckRanges& r, const void* p, unsigned long long bytes,
+                                         unsigned int site) {
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p), e = a + bytes;
+    for (int i = 0; i < r.n; ++i)
+        if (a >= r.lo[i] && e <= r.hi[i]) return true;
+    atomicCAS(&g_dev_status, 0u, (DEV_ERR_BOUNDS << 16) | (site & 0xffffu));
+    return false;
+}
+#define NC_IN_RANGE(p, bytes, site) ::nc::in_range(::nc::g_check_write, (p), (bytes), (site))
+#define NC_IN_RANGE_LOAD(p, bytes, site) ::nc::in_range(::nc::g_check_read, (p), (bytes), (site))
+#else
+#define NC_IN_RANGE(p, bytes, site) true
+#define NC_IN_RANGE_LOAD(p, bytes, site) true
+#endif
 
 // --------------------------------------------------------------- smem/bf16 --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -113,6 +149,15 @@ __device__ __forceinline__ uint4 f32x8_to_f16(const float (&x)[8]) {
                       pack_f16x2(x[6], x[7]));
 }
 
+// Eight floats -> one 16-byte store of the 16-bit type T (bf16 or IEEE fp16).
+template <typename T>
+__device__ __forceinline__ uint4 f32x8_to(const float (&x)[8]) {
+    if constexpr (std::is_same<T, __half>::value)
+        return f32x8_to_f16(x);
+    else
+        return f32x8_to_bf16(x);
+}
+
 __device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -120,6 +165,34 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
         float2 f = unpack_f16x2(w[i]);
         x[2 * i] = f.x;
         x[2 * i + 1] = f.y;
+    }
+}
+
+// 8 x 8 transpose of 16-byte chunks inside each group of 8 lanes (lanes
+// 8j .. 8j + 7): before, lane 8j + r holds chunks (r, 0..7) in c[0..7];
+// after, lane 8j + k holds chunks (0..7, k), chunk (r, k) in c[r].  Three
+// butterfly stages (xor 4, 2, 1), each trading half of the chunks with the
+// partner lane.  All 32 lanes must take part.
+__device__ __forceinline__ void transpose8_chunks(uint4 (&c)[8]) {
+    const int r = threadIdx.x & 7;
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1) {
+        const bool up = (r & d) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i & d) continue;
+            const int j = i | d;
+            const uint4 send = up ? c[i] : c[j];
+            uint4 got;
+            got.x = __shfl_xor_sync(0xffffffffu, send.x, d);
+            got.y = __shfl_xor_sync(0xffffffffu, send.y, d);
+            got.z = __shfl_xor_sync(0xffffffffu, send.z, d);
+            got.w = __shfl_xor_sync(0xffffffffu, send.w, d);
+            if (up)
+                c[i] = got;
+            else
+                c[j] = got;
+        }
     }
 }
 
@@ -204,6 +277,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm,
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 

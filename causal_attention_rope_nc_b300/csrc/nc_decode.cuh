@@ -3,8 +3,8 @@
 // Cache layout [B][Tcap][Hkv][D]: one cache slot holds all Hkv key/value
 // heads of one position contiguously (2*Hkv*D bytes).  Query head h reads
 // key/value head h / G (grouped-query attention, G = H / Hkv; G = 1 is plain
-// multi-head attention).  Keys are cached normalised and rotated, in IEEE
-// fp16 (elements bounded by sqrt(D)); values raw, in bf16.
+// multi-head attention).  Keys are cached normalised and rotated, values raw,
+// both in bf16.
 //
 // Split over the cache: one CTA per (chunk c of CH slots, stream b), grid
 // ceil(Tcap / CH) x B; a CTA whose chunk starts at or past the stream's
@@ -18,7 +18,7 @@
 // correct for any G, reading key/value head h / G with cached loads when
 // G > 1 and writing every key/value head of the new slot first): warp w
 // takes heads w, w + NW, ...  For one head it walks the chunk's slots BATCH
-// at a time: a group of D/8 lanes reads one slot's key row (fp16) and value
+// at a time: a group of D/8 lanes reads one slot's key row and value
 // row (bf16) as 16-byte pieces, 32/(D/8) slots per warp load (streaming
 // loads, evict-first).  The batches are software-pipelined over two
 // register buffers: every load of batch n+1 is issued before the arithmetic
@@ -57,10 +57,10 @@
 // take no part in the merge.
 //
 // The new token (position p = lens[b] - 1): the CTA that owns the last chunk
-// normalises and rotates k_new, writes it (fp16) and v_new into slot p (in
+// normalises and rotates k_new, writes it (bf16) and v_new into slot p (in
 // the ring kernel for every key/value head, followed by a proxy fence so the
 // TMA engine sees the writes) and then reads the slot like every other, so
-// the score at p uses exactly the stored fp16 key.
+// the score at p uses exactly the stored bf16 key.
 #pragma once
 
 #include "nc_common.cuh"
@@ -132,7 +132,9 @@ __device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, in
     const int NW = static_cast<int>(blockDim.x >> 5);
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) *s_last = atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
+    if (threadIdx.x == 0)
+        *s_last = NC_IN_RANGE(counters + b, 4, 0x503) &&
+                  atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
     __syncthreads();
     if (!*s_last) return;  // uniform
     __threadfence();
@@ -183,9 +185,10 @@ __device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, in
         __nv_bfloat16* orow = out + (static_cast<long long>(b) * H + h) * D + lane * EPL;
 #pragma unroll
         for (int e = 0; e < EPL; e += 2)
-            *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
+            if (NC_IN_RANGE(orow + e, 4, 0x501))
+                *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
     }
-    if (threadIdx.x == 0) counters[b] = 0u;  // ready for the next call
+    if (threadIdx.x == 0 && NC_IN_RANGE(counters + b, 4, 0x502)) counters[b] = 0u;  // ready for the next call
 }
 
 // Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
@@ -193,9 +196,9 @@ __device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, in
 template <int D>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
-    const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
-    unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
+    const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* kcache, __nv_bfloat16* vcache,
+    const int* __restrict__ lens, __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
+    float* __restrict__ part_ml, unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
     const __grid_constant__ Theta theta, float scale_log2, int W, int G) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
@@ -256,7 +259,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             const int s = j + g + SPW * u;
             if (s < s1) {
                 const long long at = base + static_cast<long long>(s) * slot_elems;
-                if (G == 1) {
+                if (!NC_IN_RANGE_LOAD(kcache + at, 16, 0x504) || !NC_IN_RANGE_LOAD(vcache + at, 16, 0x505)) {
+                    kr[u] = make_uint4(0u, 0u, 0u, 0u);
+                    vr[u] = kr[u];
+                } else if (G == 1) {
                     kr[u] = ld_stream16(kcache + at);
                     vr[u] = ld_stream16(vcache + at);
                 } else {
@@ -276,15 +282,16 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     if (!own_new && warp < H) load_batch(head_base(warp), s0, ka, va);
     for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
     __syncthreads();
-    // RoPE(RMSNorm(k_new)) (fp16) and v_new into slot p, key/value head hk
+    // RoPE(RMSNorm(k_new)) (bf16) and v_new into slot p, key/value head hk
     auto store_new = [&](int hk) {
         const long long row = (static_cast<long long>(b) * Hkv + hk) * D;
         float kv[8];
         norm_rope8(k_new + row, kv);
         if (g == 0) {
             const long long at = (static_cast<long long>(b) * Tcap + p_new) * slot_elems + static_cast<long long>(hk) * D + e0;
-            *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_f16(kv);
-            *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
+            if (NC_IN_RANGE(kcache + at, 16, 0x506)) *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_bf16(kv);
+            if (NC_IN_RANGE(vcache + at, 16, 0x507))
+                *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
         }
     };
     if (own_new && G > 1) {  // uniform over the CTA
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
 #pragma unroll
             for (int u = 0; u < NLD; ++u) {
                 float kf[8];
-                f16x8_to_f32(kr[u], kf);
+                bf16x8_to_f32(kr[u], kf);
                 float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
@@ -369,13 +376,17 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
                 const float inv = 1.f / l;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = acc[e] * inv;
-                *reinterpret_cast<uint4*>(out + row_bh + e0) = f32x8_to_bf16(o);
+                if (NC_IN_RANGE(out + row_bh + e0, 16, 0x50a))
+                    *reinterpret_cast<uint4*>(out + row_bh + e0) = f32x8_to_bf16(o);
             } else {
                 const long long pi = (static_cast<long long>(b) * max_parts + c) * H + h;
                 float4* po = reinterpret_cast<float4*>(part_o + pi * D + e0);
-                po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                if (sub == 0) *reinterpret_cast<float2*>(part_ml + pi * 2) = make_float2(m, l);
+                if (NC_IN_RANGE(po, 32, 0x50b)) {
+                    po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                }
+                if (sub == 0 && NC_IN_RANGE(part_ml + pi * 2, 8, 0x50c))
+                    *reinterpret_cast<float2*>(part_ml + pi * 2) = make_float2(m, l);
             }
         }
     }
@@ -391,9 +402,10 @@ template <int D, int HPW>
 __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
-    const __nv_bfloat16* __restrict__ v_new, __half* kcache, __nv_bfloat16* vcache, const int* __restrict__ lens,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml,
-    unsigned int* __restrict__ counters, int B, int H, int Hkv, int Tcap, int max_parts, float eps,
+    const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* kcache, __nv_bfloat16* vcache,
+    const int* __restrict__ lens, __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
+    float* __restrict__ part_ml, unsigned int* __restrict__ counters, int B, int H, int Hkv, int Tcap, int max_parts,
+    float eps,
     const __grid_constant__ Theta theta, float scale_log2, int W, int SB, int NST) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
@@ -463,7 +475,7 @@ __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
             o[e] = lo_half ? xv[e] * cs.x - yv[e] * cs.y : yv[e] * cs.y + xv[e] * cs.x;
         }
     };
-    // RoPE(RMSNorm(k_new)) (fp16) and v_new into slot p of every key/value
+    // RoPE(RMSNorm(k_new)) (bf16) and v_new into slot p of every key/value
     // head, before the producer's first copy
     if (own_new) {  // uniform over the CTA
         for (int hk = warp; hk < Hkv; hk += NW) {
@@ -473,8 +485,9 @@ __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
             if (g == 0) {
                 const long long at = (static_cast<long long>(b) * Tcap + p_new) * slot_elems +
                                      static_cast<long long>(hk) * D + e0;
-                *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_f16(kv);
-                *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
+                if (NC_IN_RANGE(kcache + at, 16, 0x508)) *reinterpret_cast<uint4*>(kcache + at) = f32x8_to_bf16(kv);
+                if (NC_IN_RANGE(vcache + at, 16, 0x509))
+                    *reinterpret_cast<uint4*>(vcache + at) = *reinterpret_cast<const uint4*>(v_new + row + e0);
             }
         }
         fence_proxy_async_global();
@@ -542,7 +555,7 @@ __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
 #pragma unroll
                     for (int u = 0; u < NLD; ++u) {
                         float kf[8];
-                        f16x8_to_f32(kr[u], kf);
+                        bf16x8_to_f32(kr[u], kf);
                         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                         for (int e = 0; e < 8; e += 2) {
@@ -597,13 +610,17 @@ __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
                     const float inv = 1.f / l[i];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[e] = acc[i][e] * inv;
-                    *reinterpret_cast<uint4*>(out + (static_cast<long long>(b) * H + h) * D + e0) = f32x8_to_bf16(o);
+                    __nv_bfloat16* op = out + (static_cast<long long>(b) * H + h) * D + e0;
+                    if (NC_IN_RANGE(op, 16, 0x50d)) *reinterpret_cast<uint4*>(op) = f32x8_to_bf16(o);
                 } else {
                     const long long pi = (static_cast<long long>(b) * max_parts + c) * H + h;
                     float4* po = reinterpret_cast<float4*>(part_o + pi * D + e0);
-                    po[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-                    po[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-                    if (sub == 0) *reinterpret_cast<float2*>(part_ml + pi * 2) = make_float2(m[i], l[i]);
+                    if (NC_IN_RANGE(po, 32, 0x50e)) {
+                        po[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                        po[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+                    }
+                    if (sub == 0 && NC_IN_RANGE(part_ml + pi * 2, 8, 0x50f))
+                        *reinterpret_cast<float2*>(part_ml + pi * 2) = make_float2(m[i], l[i]);
                 }
             }
         }

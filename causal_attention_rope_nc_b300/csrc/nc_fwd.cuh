@@ -14,8 +14,18 @@
 //   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: thread r owns
 //               query row r (TMEM lane r) of its tile
 // Tensor memory: S_t (128 fp32 columns) per tile, overwritten in place by the
-// bf16 probabilities P_t that the PV product reads as its A operand, and an
-// output accumulator O_t (D columns) per tile: 2 x 128 + 2 x D <= 512.
+// bf16 probabilities P_t that the PV product reads as its A operand (the 32
+// keys of chunk c in columns [32c, 32c + 16)), and an output accumulator O_t
+// (D columns) per tile: 2 x 128 + 2 x D <= 512.
+//
+// Rows that see few keys (the first 128 positions of a sequence, or every
+// row under a window shorter than 128) put large weights on few values, and
+// there rounding P to bf16 (relative 2^-8) would dominate the output's error.
+// For such query tiles P is split into P_hi = bf16(P) and P_lo = bf16(P -
+// P_hi), the latter in columns [32c + 16, 32c + 32), and the PV product runs
+// twice (O += P_hi V + P_lo V): P then carries about 16 bits.  The normaliser
+// sums P_hi + P_lo.  Causal attention over whole sequences pays this once
+// per (batch, head).
 //
 // Issue order (the tensor pipe executes one thread's MMAs in issue order):
 //   S_0(0) S_1(0) | PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) | ...
@@ -26,9 +36,10 @@
 // sm_103a sustains about 28 per clock per SM; the diagonal tile, the only
 // one with masked entries, runs its own copy of the loop.
 //
-// Operand types: qhat and khat arrive in fp16 (their elements are bounded by
-// sqrt(D), so fp16's range suffices and its finer mantissa keeps the scores
-// accurate); P and V are bf16.
+// Operand types: P and V are bf16; qhat and khat are IEEE fp16 (QK_BF16 =
+// false: the forward, whose prologue writes them in fp16 for the accuracy of
+// the scores) or bf16 (QK_BF16 = true: chunk prefill, whose keys come from
+// the bf16 key cache; tcgen05 wants A and B of one product in one type).
 //
 // Fixed softmax offset.  q and k are RMS-normalised before the product, so
 // |qhat . khat| <= |qhat| |khat| <= D (both norms are at most sqrt(D), up to
@@ -80,12 +91,16 @@ struct Smem {
 
 constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+// TMEM column (relative to S_t) of the packed P_hi pairs of K-step kk (keys
+// 16 kk .. 16 kk + 15): chunk kk / 2 of 32 keys, 8 columns per step; P_lo
+// sits 16 columns further
+__host__ __device__ constexpr uint32_t p_col(int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); }
 template <int D>
 __host__ __device__ constexpr uint32_t tm_o(int t) {
     return 256u + static_cast<uint32_t>(t) * D;
 }
 
-template <int D>
+template <int D, bool QK_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
@@ -125,6 +140,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_kv = hi1 - lo0 + 1;         // the stream: tile qt0's tiles then tile qt0+1's last
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
+    // query tiles whose rows see fewer than BN keys: P in two bf16 parts
+    auto split_tile = [&](int t) { return W < BN || qpos0 + (qt0 + t) * BM < BN; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Q_FULL), 1);
@@ -184,7 +201,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------- MMA issuer -----
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);  // qhat (K-major) x khat (K-major), fp16
+            constexpr uint32_t IDESC_S = idesc_f16kind(BM, BN, 0, 0, QK_BF16);  // qhat (K-major) x khat (K-major)
             constexpr uint32_t IDESC_O = idesc_bf16(BM, D, 0, 1);  // P (TMEM) x V (MN-major)
             auto issue_s = [&](int t, int st) {
 #pragma unroll
@@ -199,9 +216,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto issue_pv = [&](int t, int st, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + tm_o<D>(t), tmem + tm_s(t) + kk * 8,
+                    mma_ts(tmem + tm_o<D>(t), tmem + tm_s(t) + p_col(kk),
                            sdesc_sw128(sb + S::OFF_V + st * S::KBYTES + kk * (16 * 128), BN * 128, 1024), IDESC_O,
                            (!first || kk > 0) ? 1u : 0u);
+                if (split_tile(t)) {  // O += P_lo V
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(tmem + tm_o<D>(t), tmem + tm_s(t) + p_col(kk) + 16,
+                               sdesc_sw128(sb + S::OFF_V + st * S::KBYTES + kk * (16 * 128), BN * 128, 1024), IDESC_O,
+                               1u);
+                }
             };
             bool ok = mbar_wait(bar(Q_FULL), 0, 0x201) && mbar_wait(bar(K_FULL + 0), 0, 0x202);
             if (ok) {
@@ -269,13 +293,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld();
             const int kt = (t ? lo1 : lo0) + j;            // key tile
             const int d0 = qpos0 + qt * BM + row - kt * BN;  // query - key position at column 0 of the tile
-            auto exp_tile = [&](auto masked) {
+            auto exp_tile = [&](auto masked, auto split) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     // the load of chunk c+1 overlaps the exponentials of chunk c
                     if (c + 1 < BN / 32) tmem_ld32(ts + (c + 1) * 32, r[(c + 1) & 1]);
                     const uint32_t* rc = r[c & 1];
-                    uint32_t w[16];
+                    uint32_t w[16], wl[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float p0 = ex2(fmaf(__uint_as_float(rc[e]), scale_log2, -mfix_log2));
@@ -292,17 +316,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         l_lo = add_bf16_lo(l_lo, wv);
                         l_hi = add_bf16_hi(l_hi, wv);
                         w[e / 2] = wv;
+                        if constexpr (decltype(split)::value) {
+                            const float2 ph = unpack_bf16x2(wv);
+                            const uint32_t wlo = pack_bf16x2(p0 - ph.x, p1 - ph.y);
+                            l_lo = add_bf16_lo(l_lo, wlo);
+                            l_hi = add_bf16_hi(l_hi, wlo);
+                            wl[e / 2] = wlo;
+                        }
                     }
-                    // chunk c lands in packed columns [16c, 16c+16): already read
-                    tmem_st16(ts + c * 16, w);
+                    // chunk c lands in packed columns [32c, 32c+16) (P_lo in
+                    // [32c+16, 32c+32)): its own, already read
+                    tmem_st16(ts + c * 32, w);
+                    if constexpr (decltype(split)::value) tmem_st16(ts + c * 32 + 16, wl);
                     if (c + 1 < BN / 32) tmem_wait_ld();
                 }
             };
-            // every (query, key) pair of the tile visible: the plain loop
-            if (kt * BN + BN - 1 <= qpos0 + qt * BM && qpos0 + qt * BM + BM - 1 - kt * BN < W)
-                exp_tile(std::false_type{});
-            else
-                exp_tile(std::true_type{});
+            // every (query, key) pair of the tile visible: the plain loop; the
+            // split form whenever the MMA thread issues the P_lo product
+            const bool full = kt * BN + BN - 1 <= qpos0 + qt * BM && qpos0 + qt * BM + BM - 1 - kt * BN < W;
+            if (split_tile(t)) {
+                if (full)
+                    exp_tile(std::false_type{}, std::true_type{});
+                else
+                    exp_tile(std::true_type{}, std::true_type{});
+            } else if (full) {
+                exp_tile(std::false_type{}, std::false_type{});
+            } else {
+                exp_tile(std::true_type{}, std::false_type{});
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive_warp(bar(P_FULL + t));
@@ -317,7 +358,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const float l_sum = l_lo + l_hi;
             const float inv_l = 1.f / l_sum;
-            if (lse != nullptr && q_idx < T) lse[(static_cast<long long>(b) * H + h) * T + q_idx] = mfix + logf(l_sum);
+            float* lp = lse + (static_cast<long long>(b) * H + h) * T + q_idx;
+            if (lse != nullptr && q_idx < T && NC_IN_RANGE(lp, 4, 0x410)) *lp = mfix + logf(l_sum);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) stage_acc_bf16<32>(tmem + lane_base + tm_o<D>(t), inv_l, stage, row, c * 32);
             fence_proxy_async_smem();

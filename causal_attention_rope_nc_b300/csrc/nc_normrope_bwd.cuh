@@ -100,4 +100,14 @@ __device__ __forceinline__ float ds_scale_for(float bound) {
     return ldexpf(1.f, e);
 }
 
+// The backward's one dS scale for the whole call, from the row-norm maxima
+// the preprocess publishes (gmax[0] = max ||dout_i||, gmax[1] = max ||v_j||):
+//   |dS_ij| = P_ij |<dout_i, v_j> - <dout_i, out_i>| <= 2 max ||dout|| max ||v||
+// (out_i is a convex combination of the v_j, so ||out_i|| <= max ||v||), with
+// a 1/16 margin for the rounding of the factors.  Both backward kernels use
+// it: the key side stores alpha * dS, the query side sums those blocks.
+__device__ __forceinline__ float ds_scale_global(const unsigned int* gmax) {
+    return ds_scale_for(2.f * __uint_as_float(gmax[0]) * __uint_as_float(gmax[1]) * 1.0625f);
+}
+
 }  // namespace nc

@@ -7,9 +7,28 @@
 // held by the lane D/16 positions away, one xor-shuffle from it.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "nc_common.cuh"
 
 namespace nc {
+
+// Eight floats times `scale` -> one store of eight OutT values: 16 bytes
+// for bf16 or IEEE fp16 (scale 1), 8 bytes for E4M3 (round to nearest even,
+// saturating).
+template <typename OutT>
+__device__ __forceinline__ void store8(OutT* dst, const float (&o)[8], float scale) {
+    if constexpr (std::is_same<OutT, __nv_fp8_e4m3>::value) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = static_cast<uint32_t>(
+                __nv_cvt_float2_to_fp8x2(make_float2(o[2 * i] * scale, o[2 * i + 1] * scale), __NV_SATFINITE, __NV_E4M3));
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    } else {
+        *reinterpret_cast<uint4*>(dst) = f32x8_to<OutT>(o);
+    }
+}
 
 template <int D>
 struct RowLanes {
@@ -41,15 +60,16 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int t = static_cast<int>(e / half), i = static_cast<int>(e % half);
         const int p = pos ? pos[t] : t;
-        tab[e] = rope_cos_sin(p, s_theta[i]);
+        if (NC_IN_RANGE(tab + e, sizeof(float2), 0x401)) tab[e] = rope_cos_sin(p, s_theta[i]);
     }
 }
 
 // ------------------------------------------------- QK RMSNorm + RoPE (K1) --
 // qhat = RoPE(q / sqrt(mean(q^2) + eps)), same for k (k may be null: one
-// tensor only), stored as IEEE fp16: the norm bounds every element by
-// sqrt(D) <= 11.4, well inside fp16's range, and fp16 keeps 3 more mantissa
-// bits than bf16 for the score products.  rstd (optional) receives 1/r,
+// tensor only), stored as OutT: IEEE fp16 for the forward/backward operands
+// (the norm bounds every element by sqrt(D) <= 11.4, well inside fp16's
+// range, and fp16's 3 extra mantissa bits keep the score products within the
+// forward's error bound), bf16 for a key cache.  rstd (optional) receives 1/r,
 // laid out [2][B][T][H] (q then k).  (With fewer key/value heads than query
 // heads the host runs one launch per tensor, each with its own head count
 // and its own part of rstd.)
@@ -61,14 +81,14 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // tokens first, then k tokens.
 constexpr int NORM_HC = 8;
 
-template <int D>
+template <int D, typename OutT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
                                                            const __nv_bfloat16* __restrict__ k,
                                                            const float2* __restrict__ tab,
-                                                           __half* __restrict__ qhat,
-                                                           __half* __restrict__ khat,
+                                                           OutT* __restrict__ qhat,
+                                                           OutT* __restrict__ khat,
                                                            float* __restrict__ rstd, long long tokens_per_tensor,
-                                                           int T, int H, float eps) {
+                                                           int T, int H, float eps, float out_scale = 1.f) {
     using L = RowLanes<D>;
     const int sub = threadIdx.x % L::LPR;
     const long long groups = blockDim.x / L::LPR;
@@ -94,7 +114,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
             }
         }
         const __nv_bfloat16* src = (is_k ? k : q) + r * H * D + sub * 8;
-        __half* dst = (is_k ? khat : qhat) + r * H * D + sub * 8;
+        OutT* dst = (is_k ? khat : qhat) + r * H * D + sub * 8;
         for (int h0 = 0; h0 < H; h0 += NORM_HC) {
             uint4 u[NORM_HC];
 #pragma unroll
@@ -120,8 +140,10 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
                 if (valid) {
-                    *reinterpret_cast<uint4*>(dst + (h0 + j) * D) = f32x8_to_f16(o);
-                    if (rstd && sub == 0) rstd[((is_k ? tokens_per_tensor : 0) + r) * H + h0 + j] = rs;
+                    if (NC_IN_RANGE(dst + (h0 + j) * D, 8 * sizeof(OutT), 0x402))
+                        store8<OutT>(dst + (h0 + j) * D, o, out_scale);
+                    float* rp = rstd + ((is_k ? tokens_per_tensor : 0) + r) * H + h0 + j;
+                    if (rstd && sub == 0 && NC_IN_RANGE(rp, 4, 0x403)) *rp = rs;
                 }
             }
         }
@@ -130,8 +152,8 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
 
 // --------------------------------------------- chunk prefill prologue ----
 // For the C new tokens of stream b (positions start[b] + t, t < C):
-//   qhat[b][t][h] = RoPE(RMSNorm(q[b][t][h]), start[b] + t)    (fp16, workspace; h < H)
-//   kcache[b][start[b] + t][g] = RoPE(RMSNorm(k[b][t][g]), start[b] + t)  (fp16; g < Hkv)
+//   qhat[b][t][h] = RoPE(RMSNorm(q[b][t][h]), start[b] + t)    (bf16, workspace; h < H)
+//   kcache[b][start[b] + t][g] = RoPE(RMSNorm(k[b][t][g]), start[b] + t)  (bf16; g < Hkv)
 //   vcache[b][start[b] + t][g] = v[b][t][g]                     (bf16 copy)
 // One group of D/8 lanes owns one token of one stream: it forms the token's
 // rotation (cos, sin of its 8 pair indices) from the frequencies and walks
@@ -142,7 +164,8 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
                                                                 const __nv_bfloat16* __restrict__ k,
                                                                 const __nv_bfloat16* __restrict__ v,
                                                                 const int* __restrict__ start,
-                                                                __half* __restrict__ qhat, __half* kcache,
+                                                                __nv_bfloat16* __restrict__ qhat,
+                                                                __nv_bfloat16* kcache,
                                                                 __nv_bfloat16* vcache, int B, int C, int H, int Hkv,
                                                                 int Tcap, float eps,
                                                                 const __grid_constant__ Theta theta) {
@@ -199,11 +222,11 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
                 if (valid) {
-                    __half* dst = which ? kcache + slot + h * D : qhat + tok_q + h * D;
-                    *reinterpret_cast<uint4*>(dst) = f32x8_to_f16(o);
+                    __nv_bfloat16* dst = which ? kcache + slot + h * D : qhat + tok_q + h * D;
+                    if (NC_IN_RANGE(dst, 16, 0x404)) *reinterpret_cast<uint4*>(dst) = f32x8_to_bf16(o);
                 }
             }
-            if (valid && h < Hkv)
+            if (valid && h < Hkv && NC_IN_RANGE(vcache + slot + h * D, 16, 0x405))
                 *reinterpret_cast<uint4*>(vcache + slot + h * D) =
                     *reinterpret_cast<const uint4*>(v + tok_kv + h * D);
         }
@@ -213,16 +236,16 @@ __global__ void __launch_bounds__(256) prefill_norm_rope_kernel(const __nv_bfloa
 // -------------------------------------------------- backward preprocess ----
 // delta[b][h][t] = <dout_t, out_t> (fp32), lse2[b][h][t] = lse * log2(e),
 // both padded to Tpad columns (delta 0, lse2 +inf beyond T so that padded
-// query rows get probability 0).  gmax[0] and
-// gmax[1] receive the largest row norms ||dout_t|| and ||out_t|| over the
-// whole tensor (they must be zero on entry); the backward bounds dS with them.
+// query rows get probability 0).  gmax[0] and gmax[1] receive the largest row
+// norms ||dout_t|| and ||v_t|| over the whole tensors (they must be zero on
+// entry): the backward's dS scale (ds_scale_global) is formed from them.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
+                                                      const __nv_bfloat16* __restrict__ v,
                                                       const float* __restrict__ lse, float* __restrict__ delta,
                                                       float* __restrict__ lse2, unsigned int* __restrict__ gmax,
-                                                      int B, int T, int H,
-                                                      int Tpad) {
+                                                      int B, int T, int H, int Hkv, int Tpad) {
     using L = RowLanes<D>;
     constexpr int RB = 4;  // consecutive positions of one (b, h) per group and iteration
     __shared__ float s_max[2][32];
@@ -233,7 +256,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const long long stride = static_cast<long long>(gridDim.x) * groups;
     const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
     const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
-    float mx_do = 0.f, mx_o = 0.f;  // squared norms
+    float mx_do = 0.f, mx_v = 0.f;  // squared norms
     // every lane of a warp runs the same iterations (the group sums shuffle)
     for (long long base = warp_first, k = first; base < nblk; base += stride, k += stride) {
         const bool valid = k < nblk;
@@ -259,16 +282,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
             float a[8], g[8];
             bf16x8_to_f32(ua[i], a);
             bf16x8_to_f32(ug[i], g);
-            float d = 0.f, sdo = 0.f, so = 0.f;
+            float d = 0.f, sdo = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 d = fmaf(a[e], g[e], d);
                 sdo = fmaf(g[e], g[e], sdo);
-                so = fmaf(a[e], a[e], so);
             }
             acc[i] = group_sum<L::LPR>(d);
             mx_do = fmaxf(mx_do, group_sum<L::LPR>(sdo));
-            mx_o = fmaxf(mx_o, group_sum<L::LPR>(so));
         }
         if (valid && sub == 0) {
             // delta and lse2 live in the workspace: o = bh * Tpad + t0 is a
@@ -280,12 +301,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
             for (int i = 0; i < RB; ++i)
                 l2[i] = t0 + i < T ? lse[bh * T + t0 + i] * 1.4426950408889634f : 0.f;
             if (t0 + RB <= T) {
-                *reinterpret_cast<float4*>(delta + o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(lse2 + o) = make_float4(l2[0], l2[1], l2[2], l2[3]);
+                if (NC_IN_RANGE(delta + o, 16, 0x406))
+                    *reinterpret_cast<float4*>(delta + o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                if (NC_IN_RANGE(lse2 + o, 16, 0x407))
+                    *reinterpret_cast<float4*>(lse2 + o) = make_float4(l2[0], l2[1], l2[2], l2[3]);
             } else {
 #pragma unroll
                 for (int i = 0; i < RB; ++i) {
-                    if (t0 + i < T) {
+                    if (t0 + i < T && NC_IN_RANGE(delta + o + i, 4, 0x408) && NC_IN_RANGE(lse2 + o + i, 4, 0x409)) {
                         delta[o + i] = acc[i];
                         lse2[o + i] = l2[i];
                     }
@@ -293,23 +316,44 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
             }
         }
     }
-    // block maximum of the row norms, one atomic per block (non-negative
+    // v rows ([B][T][Hkv] of them), RB consecutive rows per group and iteration
+    const long long nv = static_cast<long long>(B) * T * Hkv;
+    const long long nvb = (nv + RB - 1) / RB;
+    for (long long base = warp_first, k = first; base < nvb; base += stride, k += stride) {
+        uint4 u[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const long long r = k * RB + i;
+            u[i] = (k < nvb && r < nv) ? *reinterpret_cast<const uint4*>(v + r * D + sub * 8)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            float a[8];
+            bf16x8_to_f32(u[i], a);
+            float sv = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sv = fmaf(a[e], a[e], sv);
+            mx_v = fmaxf(mx_v, group_sum<L::LPR>(sv));
+        }
+    }
+    // block maxima of the row norms, one atomic each per block (non-negative
     // floats order like their bit patterns)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         mx_do = fmaxf(mx_do, __shfl_xor_sync(0xffffffffu, mx_do, o));
-        mx_o = fmaxf(mx_o, __shfl_xor_sync(0xffffffffu, mx_o, o));
+        mx_v = fmaxf(mx_v, __shfl_xor_sync(0xffffffffu, mx_v, o));
     }
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     if ((threadIdx.x & 31) == 0) {
         s_max[0][wid] = mx_do;
-        s_max[1][wid] = mx_o;
+        s_max[1][wid] = mx_v;
     }
     __syncthreads();
     if (threadIdx.x < 2) {
         float m = 0.f;
         for (int w = 0; w < nw; ++w) m = fmaxf(m, s_max[threadIdx.x][w]);
-        atomicMax(gmax + threadIdx.x, __float_as_uint(sqrtf(m)));
+        if (NC_IN_RANGE(gmax + threadIdx.x, 4, 0x40a)) atomicMax(gmax + threadIdx.x, __float_as_uint(sqrtf(m)));
     }
     // padding columns t in [T, Tpad)
     const int padw = Tpad - T;
@@ -318,8 +362,98 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long bh = e / padw;
         const long long o = bh * Tpad + T + (e % padw);
+        if (!NC_IN_RANGE(delta + o, 4, 0x40b) || !NC_IN_RANGE(lse2 + o, 4, 0x40c)) continue;
         delta[o] = 0.f;
         lse2[o] = __int_as_float(0x7f800000);  // +inf
+    }
+}
+
+// ------------------------------------------------ FP8 value quantisation --
+// vmax[bg] = max |v[b][t][g][d]| over t, d for bg = b * Hkv + g, as float
+// bits (zero on entry; non-negative floats order like their bits).  Grid
+// (token chunks of 256, B * Hkv); one group of D/8 lanes per token.
+template <int D>
+__global__ void __launch_bounds__(256) v_absmax_kernel(const __nv_bfloat16* __restrict__ v,
+                                                       unsigned int* __restrict__ vmax, int T, int Hkv) {
+    using L = RowLanes<D>;
+    __shared__ float s_max[8];
+    const int sub = threadIdx.x % L::LPR;
+    const int bg = blockIdx.y, b = bg / Hkv, g = bg % Hkv;
+    const int t_end = min(T, static_cast<int>(blockIdx.x) * 256 + 256);
+    float a = 0.f;
+    for (int t = blockIdx.x * 256 + threadIdx.x / L::LPR; t < t_end; t += blockDim.x / L::LPR) {
+        float x[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(v + ((static_cast<long long>(b) * T + t) * Hkv + g) * D + sub * 8),
+                      x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, s_max[w]);
+        if (NC_IN_RANGE(vmax + bg, 4, 0x40d)) atomicMax(vmax + bg, __float_as_uint(m));
+    }
+}
+
+// The exponent tau of one head's value scale: the largest integer with
+// max 2^tau <= 448 (E4M3's largest finite value), clamped to [-126, 126] so
+// that 2^-tau is a normal fp32 number; 0 for an all-zero head.
+__device__ __forceinline__ int v_scale_exp(float mxf) {
+    const double mx = mxf;
+    if (!(mx > 0.0)) return 0;
+    int tau = static_cast<int>(floor(log2(448.0 / mx)));
+    while (ldexp(mx, tau) > 448.0) --tau;
+    while (ldexp(mx, tau + 1) <= 448.0) ++tau;
+    return max(-126, min(126, tau));
+}
+
+// v8t[bg][d][t] = E4M3(v[b][t][g][d] 2^tau) for t < Tpad (0 past T): the
+// values transposed, keys contiguous, so that the fp8 forward's PV product
+// reads a K-major B operand.  vscale[bg] = 2^-tau.  Grid (Tpad / 128,
+// B * Hkv), 256 threads; each block transposes 128 tokens through a 16 KB
+// shared tile [D][128].
+template <int D>
+__global__ void __launch_bounds__(256) v_quant_t_kernel(const __nv_bfloat16* __restrict__ v,
+                                                        const unsigned int* __restrict__ vmax,
+                                                        uint8_t* __restrict__ v8t, float* __restrict__ vscale, int T,
+                                                        int Tpad, int Hkv) {
+    using L = RowLanes<D>;
+    __shared__ __align__(16) uint8_t tile[D][128];
+    const int sub = threadIdx.x % L::LPR;
+    const int bg = blockIdx.y, b = bg / Hkv, g = bg % Hkv;
+    const int t0 = blockIdx.x * 128;
+    const int tau = v_scale_exp(__uint_as_float(vmax[bg]));
+    if (blockIdx.x == 0 && threadIdx.x == 0 && NC_IN_RANGE(vscale + bg, 4, 0x40e)) vscale[bg] = ldexpf(1.f, -tau);
+    for (int tl = threadIdx.x / L::LPR; tl < 128; tl += blockDim.x / L::LPR) {
+        const int t = t0 + tl;
+        float x[8];
+        if (t < T) {
+            bf16x8_to_f32(
+                *reinterpret_cast<const uint4*>(v + ((static_cast<long long>(b) * T + t) * Hkv + g) * D + sub * 8), x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const uint32_t w = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                make_float2(ldexpf(x[e], tau), ldexpf(x[e + 1], tau)), __NV_SATFINITE, __NV_E4M3));
+            tile[sub * 8 + e][tl] = static_cast<uint8_t>(w & 0xffu);
+            tile[sub * 8 + e + 1][tl] = static_cast<uint8_t>(w >> 8);
+        }
+    }
+    __syncthreads();
+    // D rows of 128 bytes, 16 bytes per thread per step
+    uint8_t* dst = v8t + static_cast<long long>(bg) * D * Tpad + t0;
+    for (int c = threadIdx.x; c < D * 8; c += blockDim.x) {
+        const int d = c >> 3, k = c & 7;
+        if (NC_IN_RANGE(dst + static_cast<long long>(d) * Tpad + 16 * k, 16, 0x40f))
+            *reinterpret_cast<uint4*>(dst + static_cast<long long>(d) * Tpad + 16 * k) =
+                *reinterpret_cast<const uint4*>(&tile[d][16 * k]);
     }
 }
 

@@ -33,10 +33,16 @@
  *    grouped-query attention, through the *_ex calls and nc_attn_prefill,
  *    the key/value-side tensors and the caches have Hkv heads instead of H.)
  *    Every 16-bit tensor must be 16-byte aligned.
- *  - Normalised, rotated queries and keys (qhat, khat, the decode key cache)
- *    are IEEE fp16 (nc_f16): RMSNorm bounds each element by sqrt(D), well
- *    inside fp16's range, and fp16 carries 3 more mantissa bits than bf16
- *    into the score products.  Everything else is bf16.
+ *  - Every 16-bit tensor is bf16 (nc_bf16), the KV caches included (the key
+ *    cache holds keys normalised and rotated at their slot position), except
+ *    qhat and khat, the normalised, rotated q and k that nc_attn_fwd writes
+ *    and nc_attn_bwd reads back: these are this library's own side outputs,
+ *    kept in IEEE fp16 (nc_f16).  RMSNorm bounds each of their elements by
+ *    sqrt(D), well inside fp16's range, and fp16 carries 3 more mantissa bits
+ *    than bf16 into the score products: with bf16 side outputs the forward's
+ *    largest error against the exact result measured 1.02e-2 on a seeded
+ *    128-head-dim-64 case, past the 1e-2 bound this library is held to, and
+ *    within it with fp16.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without synchronising.
  *  - Return value: NC_OK, or a negative code.  NC_EINVAL: a null pointer
@@ -60,8 +66,11 @@
 extern "C" {
 #endif
 
-typedef uint16_t nc_bf16;            /* raw bfloat16 bits */
-typedef uint16_t nc_f16;             /* raw IEEE binary16 bits */
+/* 16-bit element types.  Distinct struct types (one uint16_t of raw bits
+ * each), so that a compiler rejects an fp16 tensor passed where a bf16 one is
+ * expected and the reverse; pointers to them are plain data pointers. */
+typedef struct nc_bf16 { uint16_t bits; } nc_bf16; /* raw bfloat16 bits */
+typedef struct nc_f16 { uint16_t bits; } nc_f16;   /* raw IEEE binary16 bits */
 typedef struct CUstream_st *nc_stream_t; /* == cudaStream_t */
 
 #define NC_OK 0
@@ -75,10 +84,13 @@ typedef struct CUstream_st *nc_stream_t; /* == cudaStream_t */
 #define NC_OP_DECODE 2
 #define NC_OP_NORM_ROPE 3
 #define NC_OP_PREFILL 4
+#define NC_OP_FWD_FP8 5
 
 /* Library version, (major << 16) | minor.  0.2: the sliding-window calls
  * became the *_ex calls with a kv_heads argument (grouped-query attention),
- * and nc_attn_prefill gained kv_heads. */
+ * and nc_attn_prefill gained kv_heads.  0.3: the key cache (decode, prefill,
+ * nc_qk_norm_rope) is bf16 (it was IEEE fp16); nc_bf16 and nc_f16 are
+ * distinct types; the backward workspace holds the dS scratch. */
 int nc_version(void);
 
 /* Human-readable name of an NC_* code. */
@@ -116,10 +128,10 @@ size_t nc_attn_workspace_size(int op, int B, int T, int H, int D);
 
 /* QK RMSNorm + RoPE alone (prefill of a KV cache, or a check of the
  * prologue): xhat = RoPE(x / sqrt(mean(x^2) + eps), pos) for x [B][T][H][D].
- * xhat is fp16.  pos: [T] int32 positions, or NULL for 0..T-1.  rstd:
+ * xhat is bf16, the key cache's format.  pos: [T] int32 positions, or NULL for 0..T-1.  rstd:
  * optional [B][T][H] fp32 output of 1/sqrt(mean(x^2) + eps).
  * Workspace: NC_OP_NORM_ROPE. */
-int nc_qk_norm_rope(const nc_bf16 *x, const int32_t *pos, nc_f16 *xhat, float *rstd, void *workspace,
+int nc_qk_norm_rope(const nc_bf16 *x, const int32_t *pos, nc_bf16 *xhat, float *rstd, void *workspace,
                     size_t workspace_bytes, int B, int T, int H, int D, float eps, float rope_base,
                     nc_stream_t stream);
 
@@ -137,8 +149,13 @@ int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int3
  * softmax, the RoPE rotation and the RMSNorm).  Every output element is
  * computed by one CTA (a key-side kernel writes dk and dv, a query-side
  * kernel dq): no atomics, bit-identical results on repeated calls.
- * Workspace: NC_OP_BWD (RoPE table, per-row delta and lse, three norm
- * maxima; overwritten by every call). */
+ * Workspace: NC_OP_BWD, overwritten by every call: the RoPE table, per-row
+ * delta and lse, and the dS scratch.  The key-side kernel forms each
+ * visible 128 x 128 block of dS = P o (dP - delta) once and writes it there
+ * (bf16) for the query side's dq = dS khat, so the workspace grows with
+ * B * H * n(n+1)/2 blocks of 32 KB, n = ceil(T / 128) (1.4 GB at B = 32,
+ * T = 2048, H = 10).  Problems with B * H * n(n+1)/2 >= 2^24 blocks are
+ * NC_EINVAL. */
 int nc_attn_bwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
                 const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
                 nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
@@ -149,12 +166,12 @@ int nc_attn_bwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int3
  * lens[b]-1.  q [B][H][D] is the new token's raw query.  If k_new and v_new
  * ([B][H][D], raw) are given, the new key is normalised and rotated and
  * written with v_new into slot lens[b]-1 of kcache / vcache first;
- * otherwise that slot must already hold them.  kcache (fp16) holds keys
- * already normalised and rotated at their slot position (as
- * nc_qk_norm_rope writes them); vcache (bf16) holds raw values.
+ * otherwise that slot must already hold them.  kcache holds keys already
+ * normalised and rotated at their slot position (as nc_qk_norm_rope writes
+ * them); vcache holds raw values; both bf16.
  * out [B][H][D] bf16.  Up to 512 / (D/8) heads (32 at D = 128).
  * Workspace: NC_OP_DECODE with T = Tcap (zeroed once before first use). */
-int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+int nc_attn_decode(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_bf16 *kcache,
                    nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
                    int B, int H, int D, int Tcap, float eps, float rope_base, nc_stream_t stream);
 
@@ -194,29 +211,56 @@ int nc_attn_bwd_ex(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const i
                    const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
                    nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
                    float eps, float rope_base, int window, int kv_heads, nc_stream_t stream);
-int nc_attn_decode_ex(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+int nc_attn_decode_ex(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_bf16 *kcache,
                       nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, void *workspace, size_t workspace_bytes,
                       int B, int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
                       nc_stream_t stream);
+
+/* FP8 forward (head dimension 128): the forward of nc_attn_fwd_ex with its
+ * products in E4M3 on the tensor cores (fp32 accumulation).  The pages name
+ * an fp8 training path (ai.flicky.cc, "nanochat: свой ChatGPT от
+ * токенизатора до чата", section "Карта репозитория", fp8.py row; the
+ * "+fp8" leaderboard row of pigsec.cn "karpathy/nanochat") and give no
+ * scheme for attention; this library's reading:
+ *   qhat and khat (normalised and rotated as in nc_attn_fwd) are rounded to
+ *   E4M3 after scaling by 2^5 (QK-norm bounds their elements by sqrt(D), so
+ *   they stay within E4M3's 448); v by 2^tau per (batch, key/value head),
+ *   tau the largest integer keeping max |v| 2^tau <= 448 (clamped to
+ *   [-126, 126]); the probabilities p = exp(s - row max) by 2^8.
+ *   out = sum_j P8_j v8_j / sum_j P8_j (rows of quantised weights that sum
+ *   to one), lse = row max + ln sum_j p (unquantised).
+ * Same arguments as nc_attn_fwd_ex minus qhat, khat and rstd (nothing is
+ * kept for a backward); lse may be NULL.  Workspace: NC_OP_FWD_FP8 (RoPE
+ * table, the E4M3 operands, the value scales).  D != 128 is NC_EINVAL. */
+int nc_attn_fwd_fp8(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
+                    float *lse, void *workspace, size_t workspace_bytes, int B, int T, int H, int D, float eps,
+                    float rope_base, int window, int kv_heads, nc_stream_t stream);
 
 /* Chunk prefill into a KV cache.  Stream b appends C new tokens at
  * positions start[b] .. start[b] + C - 1 (start: [B] int32, device): their
  * raw q [B][C][H][D] and k, v [B][C][Hkv][D] are normalised and rotated
  * at those positions (Hkv = kv_heads, 0 meaning H, as in the *_ex calls);
- * the keys (fp16, normalised and rotated, as nc_qk_norm_rope writes them)
+ * the keys (normalised and rotated, as nc_qk_norm_rope writes them)
  * and the values go into slots start[b] .. start[b] + C - 1 of kcache /
  * vcache [B][Tcap][Hkv][D]; each new query attends causally over slots
  * 0 .. its own position (the last `window` of them when window > 0, as in
  * the *_ex calls).  out [B][C][H][D] bf16; lse [B][H][C] fp32, natural log,
  * or NULL.  The slots before start[b] must already hold the stream's keys
- * and values.  With start[b] = 0 and C = T this is nc_attn_fwd_ex over the
+ * and values, the keys normalised and rotated (as this call, nc_attn_decode
+ * or nc_qk_norm_rope write them).  The prefill's softmax relies on that: it
+ * subtracts the fixed offset sqrt(D) * 1.0079, which bounds every score
+ * only when both vectors have norm at most sqrt(D).  A slot holding anything
+ * else is not detected: its scores may exceed the offset, the row's weights
+ * are then no longer bounded by 1, and a key whose norm exceeds about
+ * sqrt(D) * 1.0079 + 88 can overflow the rows that see it to inf or NaN.
+ * (Decode keeps a running maximum and has no such precondition.)  With start[b] = 0 and C = T this is nc_attn_fwd_ex over the
  * chunk (plus the cache writes); a prompt may also be fed in several chunks,
  * each starting where the previous one ended.  The pages prefill the KV
  * cache before decoding (ai.flicky.cc, "nanochat: свой ChatGPT от
  * токенизатора до чата", section "Карта репозитория", engine.py row).
  * A stream with start[b] < 0 or start[b] + C > Tcap is skipped and recorded
  * in the device status word (2).  Workspace: NC_OP_PREFILL with T = C. */
-int nc_attn_prefill(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *start, nc_f16 *kcache,
+int nc_attn_prefill(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *start, nc_bf16 *kcache,
                     nc_bf16 *vcache, nc_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, int B,
                     int C, int H, int D, int Tcap, float eps, float rope_base, int window, int kv_heads,
                     nc_stream_t stream);
@@ -243,7 +287,7 @@ int nc_attn_prefill(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const 
 #define NC_ETOOLARGE (-5)
 #define NC_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 
-int nc_attn_decode_noalloc(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_f16 *kcache,
+int nc_attn_decode_noalloc(const nc_bf16 *q, const nc_bf16 *k_new, const nc_bf16 *v_new, nc_bf16 *kcache,
                            nc_bf16 *vcache, const int32_t *lens, nc_bf16 *out, int B, int H, int D, int Tcap,
                            float eps, float rope_base, nc_stream_t stream);
 

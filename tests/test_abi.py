@@ -36,6 +36,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_checked_build_exports_every_declared_symbol():
+    """The bounds-checked debug build (-DNC_CHECK) has the same ABI."""
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    chk = ctypes.CDLL(b.build(checked=True))
+    for name in _declared():
+        assert hasattr(chk, name), name
+
+
 def test_binding_lists_every_declared_symbol():
     import causal_attention_rope_nc_b300 as nc
     assert sorted(nc.EXPORTED) == _declared()
@@ -48,7 +57,8 @@ def test_workspace_sizes(lib):
     B, T, H, D = 32, 2048, 10, 128
     tab = T * (D // 2) * 8
     assert f(0, B, T, H, D) == tab
-    assert f(1, B, T, H, D) == tab + 2 * B * H * T * 4 + 256
+    n_t = T // 128
+    assert f(1, B, T, H, D) == tab + 2 * B * H * T * 4 + 256 + B * H * (n_t * (n_t + 1) // 2) * 128 * 128 * 2
     assert f(2, B, T, H, D) > 0
     assert f(0, B, T, H, 96) == 0  # unsupported head dim
 
@@ -163,6 +173,20 @@ def test_binding_checks_grouped_heads_on_the_host():
     nc._shape(None, "k_new", (1, 3, 64))  # an absent optional tensor passes
 
 
-def test_version_names_the_grouped_query_api(lib):
+def test_version_names_the_bf16_key_cache(lib):
+    """0.3: the key cache is bf16 and the backward keeps a dS scratch (0.2
+    added kv_heads)."""
     lib.nc_version.restype = ctypes.c_int
-    assert lib.nc_version() == (0 << 16) | 2
+    assert lib.nc_version() == (0 << 16) | 3
+
+
+def test_binding_rejects_wrong_16bit_types():
+    """The binding refuses a key cache that is not bf16, and qhat or khat
+    that are not fp16, before the C call."""
+    import torch
+    import causal_attention_rope_nc_b300 as nc
+    with pytest.raises(ValueError, match="bfloat16"):
+        nc._bf16(torch.empty((1, 4, 2, 64), dtype=torch.float16), "kcache")
+    with pytest.raises(ValueError, match="float16"):
+        nc._f16(torch.empty((1, 4, 2, 64), dtype=torch.bfloat16), "qhat")
+

@@ -249,3 +249,21 @@ def test_full_size_sampled(nc, name):
     # properties that hold everywhere: finite outputs, softmax normaliser sane
     for t in (out, dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())
+
+
+def test_full_size_forward_first_and_last_batch(nc):
+    """d20 forward at full size: every head of the first and of the last batch
+    element against the oracle.  The grouped CTA order puts the last (b, h)
+    pairs into the grid's tail group, whose tiles run at other group
+    positions than the sampled slices above."""
+    w = workloads.D20
+    q, k, v, _ = workloads.workload_inputs(w, with_dout=False)
+    out, lse, *_ = nc.attn_fwd(q.cuda(), k.cuda(), v.cuda(), eps=EPS, rope_base=BASE)
+    torch.cuda.synchronize()
+    assert nc.device_status() == 0
+    for b in (0, w.B - 1):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+            qs, ks, vs = (x[sl].contiguous() for x in (q, k, v))
+            o_ref, l_ref = oracle.attn_fwd(qs, ks, vs, eps=EPS, base=BASE)
+            check_fwd(out[sl], lse[b:b + 1, h:h + 1], o_ref, l_ref)

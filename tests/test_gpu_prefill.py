@@ -66,21 +66,24 @@ def test_prefill_matches_oracle(nc, B, C, H, D, Tcap, start, W, seed):
     assert np.max(np.abs(o - o_ref)) <= FWD_MAX_ABS
     assert rel_frob(o, o_ref) <= FWD_REL
     assert np.max(np.abs(f64(lse) - lse_ref)) <= 1e-2
-    # the chunk's keys (normalised, rotated at their positions) and values are in the cache
+    # the chunk's keys (normalised, rotated at their positions, rounded to the
+    # bf16 cache: half a bf16 ulp, 2^-8 relative) and values are in the cache
     kc, vc = kcache.cpu(), vcache.cpu()
     for b, s in enumerate(start):
         kr, _ = oracle.norm_rope(k_raw[b:b + 1, s:s + C], pos=list(range(s, s + C)), eps=EPS, base=BASE)
         got = f64(kc[b, s:s + C])
-        assert np.all(np.abs(got - kr[0]) <= np.abs(kr[0]) * 2.0 ** -10 + 1e-3)
+        assert np.all(np.abs(got - kr[0]) <= np.abs(kr[0]) * 2.0 ** -8 + 1e-4)
         assert torch.equal(vc[b, s:s + C], v[b, s:s + C])
 
 
 def test_two_chunks_equal_one_forward(nc):
-    """A prompt fed in two chunks gives the forward's rows."""
+    """A prompt fed in two chunks gives the rows of one forward over the whole
+    prompt: both chunks' outputs against the oracle's forward, at the
+    forward's tolerances."""
     B, H, D, T, a = 2, 3, 128, 333, 150
     start_t, q, k_raw, v = prefill_inputs(B, T, H, D, T, seed=94, start=[0, 0])
-    out_f, *_ = nc.attn_fwd(q.cuda(), k_raw.cuda(), v.cuda(), eps=EPS, rope_base=BASE)
-    kcache = torch.zeros((B, T, H, D), dtype=torch.float16, device="cuda")
+    o_ref, _ = oracle.attn_fwd(q, k_raw, v, eps=EPS, base=BASE)
+    kcache = torch.zeros((B, T, H, D), dtype=torch.bfloat16, device="cuda")
     vcache = torch.zeros((B, T, H, D), dtype=torch.bfloat16, device="cuda")
     o1, _ = nc.attn_prefill(q[:, :a].contiguous().cuda(), k_raw[:, :a].contiguous().cuda(),
                             v[:, :a].contiguous().cuda(), torch.zeros(B, dtype=torch.int32, device="cuda"),
@@ -90,15 +93,16 @@ def test_two_chunks_equal_one_forward(nc):
                             kcache, vcache, eps=EPS, rope_base=BASE)
     torch.cuda.synchronize()
     assert nc.device_status() == 0
-    both = torch.cat([o1, o2], dim=1).float()
-    assert float((both - out_f.float()).abs().max()) <= 1e-2
+    both = f64(torch.cat([o1, o2], dim=1))
+    assert np.max(np.abs(both - o_ref)) <= FWD_MAX_ABS
+    assert rel_frob(both, o_ref) <= FWD_REL
 
 
 def test_decode_after_prefill(nc):
     """Prefill a prompt, then decode the next token on the cache it wrote."""
     B, H, D, Tcap, C = 2, 4, 128, 512, 300
     start_t, q, k_raw, v = prefill_inputs(B, C, H, D, Tcap, seed=95, start=[0, 100])
-    kcache = torch.zeros((B, Tcap, H, D), dtype=torch.float16, device="cuda")
+    kcache = torch.zeros((B, Tcap, H, D), dtype=torch.bfloat16, device="cuda")
     vcache = torch.zeros((B, Tcap, H, D), dtype=torch.bfloat16, device="cuda")
     # history before the chunk of stream 1 through the library's prologue
     kcache[1, :100] = nc.qk_norm_rope(k_raw[1:2, :100].contiguous().cuda(), eps=EPS, rope_base=BASE)[0]

@@ -50,6 +50,9 @@ def test_oversize_problem_is_refused(nc):
 
 @pytest.mark.gpu
 def test_two_calls_match_the_workspace_decode(nc):
+    """Each path gets its own copy of the caches, so the slot that the second
+    call writes (the new token's normalised, rotated key and its value) is
+    compared too, not only the outputs."""
     w = workloads.D20_DECODE
     assert nc.workspace_size(nc.NC_OP_DECODE, w.B, w.Tcap, w.H, w.D) <= 16 << 20
     lens, q, k_raw, v = workloads.decode_workload_inputs(w)
@@ -61,13 +64,24 @@ def test_two_calls_match_the_workspace_decode(nc):
     idx = (lens2 - 1).long()
     k_new = k_raw[torch.arange(w.B), idx].contiguous().cuda()
     v_new = v[torch.arange(w.B), idx].contiguous().cuda()
+    bi, pi = torch.arange(w.B, device="cuda"), idx.cuda()
     for ln, kn, vn in ((lens, None, None), (lens2, k_new, v_new)):
         ld = ln.cuda()
-        ref = nc.attn_decode(qd, kcache, vcache, ld, k_new=kn, v_new=vn, eps=EPS, rope_base=BASE)
+        kc_ws, vc_ws = kcache.clone(), vcache.clone()
+        kc_na, vc_na = kcache.clone(), vcache.clone()
+        if kn is not None:  # the slot to be written holds zeros in both copies
+            for t in (kc_ws, vc_ws, kc_na, vc_na):
+                t[bi, pi] = 0
+        ref = nc.attn_decode(qd, kc_ws, vc_ws, ld, k_new=kn, v_new=vn, eps=EPS, rope_base=BASE)
         out = torch.empty_like(ref)
-        _call_noalloc(nc, qd, kn, vn, kcache, vcache, ld, out)
+        _call_noalloc(nc, qd, kn, vn, kc_na, vc_na, ld, out)
         torch.cuda.synchronize()
         assert nc.device_status() == 0
         err = float((out.float() - ref.float()).abs().max())
         assert err <= MAX_ABS, err
         assert bool(torch.isfinite(out.float()).all())
+        if kn is not None:
+            assert torch.equal(kc_na[bi, pi], kc_ws[bi, pi])
+            assert torch.equal(vc_na[bi, pi], vc_ws[bi, pi])
+            assert bool((vc_na[bi, pi] == v_new).all())
+        assert torch.equal(kc_na, kc_ws) and torch.equal(vc_na, vc_ws)
