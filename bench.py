@@ -213,6 +213,7 @@ def bench_ours(args, ws_n, rank, local):
     nc.nc_profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
     kern = nc.nc_profile_read()
+    kern_kernels = dict(nc.last_profile_kernels)  # kernel launches per step name
     if nc.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
 
@@ -241,7 +242,7 @@ def bench_ours(args, ws_n, rank, local):
     if rank != 0:
         return None
     pk, pk_kind = peaks()
-    launches = sum(n for n, _ in kern.values())
+    launches = sum(kern_kernels.get(k_, n) for k_, (n, _) in kern.items())
     # dominant kernel by total time
     name, (n_l, tot) = max(kern.items(), key=lambda kv: kv[1][1])
     per_launch_ms = tot / max(n_l, 1)

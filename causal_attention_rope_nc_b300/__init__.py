@@ -51,7 +51,8 @@ class NcError(RuntimeError):
 
 
 class KernelTime(ctypes.Structure):
-    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("kernels", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
 
 
 LIB_CHECK_PATH = os.path.join(_HERE, "libncattn_check.so")
@@ -150,12 +151,19 @@ def nc_profile_enable(on: bool):
     _check(lib.nc_profile_enable(1 if on else 0), "nc_profile_enable")
 
 
+last_profile_kernels: dict = {}
+
+
 def nc_profile_read() -> dict:
-    """{kernel name: (launches, total ms)} since the last read."""
+    """{step name: (timed steps, total ms)} since the last read; the kernel
+    launches inside each name's steps go to ``last_profile_kernels``."""
+    global last_profile_kernels
     buf = (KernelTime * 64)()
     n = ctypes.c_int(0)
     _check(lib.nc_profile_read(buf, 64, ctypes.byref(n)), "nc_profile_read")
-    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, 64))}
+    m = min(n.value, 64)
+    last_profile_kernels = {buf[i].name.decode(): buf[i].kernels for i in range(m)}
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(m)}
 
 
 # ------------------------------------------------------ C entry points 1:1 --

@@ -43,6 +43,7 @@ EncodeTiledFn encode_fn() {
 }
 
 constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];  // multiprocessors per device (set by device_ready)
 
 // Per-device one-time set-up: architecture check and shared-memory opt-in.
 int device_ready() {
@@ -67,6 +68,9 @@ int device_ready() {
         state[dev] = NC_EDEVICE;
         return NC_EDEVICE;
     }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = sms > 0 ? sms : 148;
     cudaError_t r = cudaSuccess;
     auto optin = [&](const void* f, int bytes) {
         cudaError_t x = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -144,6 +148,7 @@ int launch_status() {
 struct ProfRec {
     const char* name;
     cudaEvent_t a, b;
+    int kernels;
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -161,12 +166,14 @@ cudaEvent_t prof_event() {
     return e;
 }
 
-// Brackets one kernel launch on `s` when timing is enabled.
+// Brackets the `kernels` kernel launches of one library step on `s` when
+// timing is enabled.
 struct ProfScope {
     const char* name;
     cudaStream_t s;
+    int kernels;
     cudaEvent_t a = nullptr;
-    ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
+    ProfScope(const char* n, cudaStream_t st, int k = 1) : name(n), s(st), kernels(k) {
         if (!g_prof_on) return;
         std::lock_guard<std::mutex> lock(g_prof_mu);
         a = prof_event();
@@ -177,7 +184,7 @@ struct ProfScope {
         std::lock_guard<std::mutex> lock(g_prof_mu);
         cudaEvent_t b = prof_event();
         cudaEventRecord(b, s);
-        g_prof_recs.push_back({name, a, b});
+        g_prof_recs.push_back({name, a, b, kernels});
     }
 };
 
@@ -202,13 +209,13 @@ int make_tmap(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D, int 
 
 // The backward's dS^T scratch (fp16) as rows of 64 values: each block is
 // two [128 keys][64 queries] halves (bwdq::ds_offset); boxes of 64 values x
-// 128 rows (one half), 128-byte swizzled.
+// 64 rows (64 keys of one half), 128-byte swizzled.
 int make_ds_tmap(CUtensorMap* tm, const void* ds, long long rows) {
     const long long rows64 = 2 * rows;  // rows of 64 values
     if (rows <= 0 || rows64 >= (1LL << 31)) return NC_EINVAL;  // TMA row coordinates are int32
     const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows64)};
     const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, nc::bwdq::KS};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = encode_fn()(tm, kF16, 2, const_cast<void*>(ds), dims, strides, box, estr,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -296,7 +303,7 @@ template <int D, typename OutT>
 int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, void* qh, void* kh, float* rstd,
                      int B, int T, int H, int Hkv, float eps, cudaStream_t s, float out_scale = 1.f) {
     const long long toks = static_cast<long long>(B) * T;
-    ProfScope ps("qk_norm_rope", s);
+    ProfScope ps("qk_norm_rope", s, (!k || Hkv == H) ? 1 : 2);
     if (!k || Hkv == H) {
         nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks * (k ? 2 : 1), D), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
@@ -326,6 +333,28 @@ int kv_heads_of(int kv_heads, int H) {
     return kv_heads;
 }
 
+// The forward kernel over all pairs of query tiles, one CTA per pair in the
+// grouped order.  (Measured: launching the first pair of each (batch, head),
+// whose first tile's rows need the split-P path, separately from the rest
+// through an instantiation without that path, was 6% slower in total.)
+template <int D, bool QK_BF16>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, float* lse,
+               int T, int H, int B, int Hkv, int W, const int* qoff, int Tk, const char* name, cudaStream_t s) {
+    const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
+    const int n_pairs = (n_qt + 1) / 2;
+    const double scale = 1.0 / std::sqrt(double(D));
+    const double log2e = 1.4426950408889634;
+    const double mfix = std::sqrt(double(D)) * 1.0079;
+    const long long nblk = static_cast<long long>(n_pairs) * B * H;
+    if (nblk > 0x7fffffffLL) return NC_EINVAL;
+    ProfScope ps(name, s);
+    nc::fwd::attn_fwd_kernel<D, QK_BF16><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS,
+                                           nc::fwd::Smem<D>::ALLOC, s>>>(
+        tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H), float(scale * log2e), float(mfix * log2e),
+        float(mfix), W, qoff, Tk, H / Hkv);
+    return launch_status();
+}
+
 template <int D>
 int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* pos, nc_bf16* out, float* lse,
              nc_f16* qhat, nc_f16* khat, float* rstd, void* ws, int B, int T, int H, int Hkv, float eps, float base,
@@ -340,20 +369,8 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         make_tmap(&tk, khat, B, T, Hkv, D, nc::fwd::BN, kF16) || make_tmap(&tv, v, B, T, Hkv, D, nc::fwd::BN) ||
         make_tmap(&to, out, B, T, H, D, nc::fwd::BM))
         return NC_EINVAL;
-    const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
-    const double scale = 1.0 / std::sqrt(double(D));
-    const double log2e = 1.4426950408889634;
-    const double mfix = std::sqrt(double(D)) * 1.0079;
     // one CTA per pair of query tiles
-    const int n_pairs = (n_qt + 1) / 2;
-    const long long nblk = static_cast<long long>(n_pairs) * B * H;
-    if (nblk > 0x7fffffffLL) return NC_EINVAL;
-    ProfScope ps("attn_fwd", s);
-    nc::fwd::attn_fwd_kernel<D, false><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
-        tq, tk, tv, to, lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
-        float(scale * log2e),
-        float(mfix * log2e), float(mfix), W, nullptr, T, H / Hkv);
-    return launch_status();
+    return launch_fwd<D, false>(tq, tk, tv, to, lse, T, H, B, Hkv, W, nullptr, T, "attn_fwd", s);
 }
 
 // Chunk prefill: the prologue writes qhat (workspace) and the chunk's keys
@@ -380,18 +397,7 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
         make_tmap(&tk, kcache, B, Tcap, Hkv, D, nc::fwd::BN) ||
         make_tmap(&tv, vcache, B, Tcap, Hkv, D, nc::fwd::BN) || make_tmap(&to, out, B, C, H, D, nc::fwd::BM))
         return NC_EINVAL;
-    const int n_qt = (C + nc::fwd::BM - 1) / nc::fwd::BM;
-    const double scale = 1.0 / std::sqrt(double(D));
-    const double log2e = 1.4426950408889634;
-    const double mfix = std::sqrt(double(D)) * 1.0079;
-    const int n_pairs = (n_qt + 1) / 2;
-    const long long nblk = static_cast<long long>(n_pairs) * B * H;
-    if (nblk > 0x7fffffffLL) return NC_EINVAL;
-    ProfScope ps("attn_prefill", s);
-    nc::fwd::attn_fwd_kernel<D, true><<<static_cast<unsigned>(nblk), nc::fwd::NUM_THREADS, nc::fwd::Smem<D>::ALLOC, s>>>(
-        tq, tk, tv, to, lse, C, H, B, n_qt, tile_group(n_pairs, B * H), float(scale * log2e), float(mfix * log2e),
-        float(mfix), W, start, Tcap, H / Hkv);
-    return launch_status();
+    return launch_fwd<D, true>(tq, tk, tv, to, lse, C, H, B, Hkv, W, start, Tcap, "attn_prefill", s);
 }
 
 template <int D>
@@ -407,12 +413,12 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
     float* lse2 = reinterpret_cast<float*>(w);
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
-    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||v_t||
+    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||v_t||, dq tile counter
     w += 256;
     nc_f16* ds = reinterpret_cast<nc_f16*>(w);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    if (cudaMemsetAsync(gmax, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    if (cudaMemsetAsync(gmax, 0, 3 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
     const long long rows = static_cast<long long>(B) * T * H;
     {
         ProfScope ps("attn_bwd_pre", s);
@@ -421,13 +427,13 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
             reinterpret_cast<const __nv_bfloat16*>(v), lse, delta, lse2, gmax, B, T, H, Hkv, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tds;
+    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tds, tk64;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, Hkv, D, 128, kF16) ||
         make_tmap(&tv, v, B, T, Hkv, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
         make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, Hkv, D, 128) ||
         make_tab_tmap(&ttab, tab, T, D) || make_tmap(&tdq, dq, B, T, H, D, 128) ||
         make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128) ||
-        make_ds_tmap(&tds, ds, ds_rows(B, T, H)))
+        make_ds_tmap(&tds, ds, ds_rows(B, T, H)) || make_tmap(&tk64, khat, B, T, Hkv, D, nc::bwdq::KS, kF16))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -447,12 +453,16 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     }
     if ((rc = launch_status())) return rc;
     {
-        // query side: dq = dS khat from the key side's dS^T scratch (one CTA
-        // per query tile)
+        // query side: dq = dS khat from the key side's dS^T scratch, one
+        // persistent CTA per SM over all query tiles
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const long long n_tiles = n_t * B * H;
+        const int grid = static_cast<int>(n_tiles < g_sm_count[dev] ? n_tiles : g_sm_count[dev]);
         ProfScope ps("attn_bwd_dq", s);
-        nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(nblk), nc::bwdq::NUM_THREADS,
-                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk, tqr, ttab, tdq, gmax, T, H, B,
-                                                                         group, float(scale), eps, W, G);
+        nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid), nc::bwdq::NUM_THREADS,
+                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk64, tqr, ttab, tdq, gmax, gmax + 2, T,
+                                                                         H, B, group, float(scale), eps, W, G);
     }
     return launch_status();
 }
@@ -525,7 +535,7 @@ int fwd_fp8_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
     if (rc) return rc;
     if (cudaMemsetAsync(w.vmax, 0, static_cast<size_t>(B) * Hkv * 4, s) != cudaSuccess) return launch_status();
     {
-        ProfScope ps("v_quant", s);
+        ProfScope ps("v_quant", s, 2);
         nc::v_absmax_kernel<D><<<dim3((T + 255) / 256, B * Hkv), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(v), w.vmax, T, Hkv);
         if ((rc = launch_status())) return rc;
@@ -697,6 +707,7 @@ int nc_profile_read(nc_kernel_time* out, int max_entries, int* n_entries) {
             acc.push_back(z);
         }
         acc[i].launches += 1;
+        acc[i].kernels += r.kernels;
         acc[i].total_ms += ms;
     }
     {

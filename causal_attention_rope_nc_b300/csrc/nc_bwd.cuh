@@ -18,20 +18,22 @@
 //   dK_j += dS^T qhat_i                      (same shape)
 // and every dS^T block goes, in fp16, to a scratch buffer in HBM too, for
 // the query-side kernel's dQ = dS khat (nc_bwd_dq.cuh): dS is formed once.
-// Tensor memory (512 columns): S^T (128), dP^T (128, overwritten in place by
-// the fp16 dS^T that the dK product reads as its A operand), dV and dK (D
-// each).  P^T (bf16) goes to a shared-memory tile, the A operand of dV, so
-// the S^T columns are free as soon as the softmax warps have loaded them.
+// Tensor memory (512 columns): S^T (128) is overwritten in place by the
+// bf16 P^T and dP^T (128) by the fp16 dS^T; both are then read from TMEM as
+// the A operands of the dV and dK products.  dV and dK take D columns each.
+// Only tensor memory and registers hold the per-block intermediates: the
+// shared-memory traffic per block is the operand tiles and the SS products'
+// reads (about 260 KB against 2048 cycles of tensor work), close to what
+// shared memory delivers, so nothing else goes through it.  (Measured: P^T
+// through a shared-memory tile, which would let S^T(i+1) start before dV(i),
+// made the kernel 11% slower.)
 //
 // Issue order of the MMA thread for block i (one thread's MMAs execute in
 // issue order, so a product that overwrites TMEM another one reads may
 // follow it directly):
-//   [S^T(i) in registers]  S^T(i+1)
-//   [P^T(i) in smem]       dV(i)
-//   [dS^T(i) in TMEM]      dK(i), dP^T(i+1)
-// S^T(i+1) runs while the softmax warps make P(i); dV(i), dK(i) and dP^T(i+1)
-// while they make dS(i) and start on P(i+1): the tensor pipe does not wait
-// for the exponentials of the block it has just finished.
+//   [P^T(i) in TMEM]   dV(i), S^T(i+1)      while the softmax warps make dS(i)
+//   [dS^T(i) in TMEM]  dK(i), dP^T(i+1)     while they make P(i+1)
+// so each softmax phase overlaps two products.
 //
 // Roles: warps 0-7 P and dS (warp w: TMEM lane quarter w%4 = 32 key rows,
 // query half w/4 = 64 columns), warp 8 TMA, warp 9 MMA.  At the end the same
@@ -70,16 +72,14 @@ enum Bar {
     QF = 1,       // +stage: qhat_i, dout_i, lse2_i, delta_i landed
     QE = 3,       // +stage: stage free again
     S_FULL = 5,   // S^T in TMEM
-    P_FULL = 6,   // softmax wrote P^T to the shared-memory tile
+    P_FULL = 6,   // softmax wrote P^T over S^T
     DP_FULL = 7,  // dP^T in TMEM
     DS_FULL = 8,  // softmax wrote dS^T over dP^T
     DKV_FULL = 9,
     MMA_DONE = 10,
     EPI_FULL = 11,  // raw k tile and RoPE table tile staged for the dk epilogue
     KV_FREE = 12,   // the last products reading khat and v are done
-    S_READ = 13,    // softmax holds S^T in registers: the next S^T may overwrite it
-    P_FREE = 14,    // dV has read the P^T tile: the next block's P^T may overwrite it
-    NUM_BARS = 15
+    NUM_BARS = 13
 };
 
 template <int D>
@@ -90,15 +90,11 @@ struct Smem {
     static constexpr int OFF_V = OFF_K + KBYTES;
     static constexpr int OFF_Q = OFF_V + KBYTES;        // 2 stages
     static constexpr int OFF_DO = OFF_Q + 2 * QBYTES;   // 2 stages
-    static constexpr int OFF_P = OFF_DO + 2 * QBYTES;   // P^T [128 keys][128 queries] bf16, K-major
-    static constexpr int PBYTES = BN * BM * 2;
-    static constexpr int OFF_L = OFF_P + PBYTES;        // 2 stages x BM fp32 (lse * log2e)
+    static constexpr int OFF_L = OFF_DO + 2 * QBYTES;   // 2 stages x BM fp32 (lse * log2e)
     static constexpr int OFF_DL = OFF_L + 2 * BM * 4;   // 2 stages x BM fp32 (delta)
     static constexpr int OFF_BAR = OFF_DL + 2 * BM * 4;
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_TSLOT + 16;
-    // the base is 1024-aligned (the declaration asks for it); any slack left
-    // below the limit is kept for smem_align1024
     static constexpr int ALLOC = (BYTES + 1024 < SMEM_LIMIT) ? BYTES + 1024 : SMEM_LIMIT;
     // epilogue: the raw k tile over the khat tile, the RoPE table tile (fp32
     // [128][D]) over the qhat and dout halves of the stage the last block
@@ -170,8 +166,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(bar(MMA_DONE), 1);
         mbar_init(bar(EPI_FULL), 1);
         mbar_init(bar(KV_FREE), 1);
-        mbar_init(bar(S_READ), 8);
-        mbar_init(bar(P_FREE), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -238,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_f16(BN, BM, 0, 0);   // khat x qhat^T
             constexpr uint32_t IDESC_DP = idesc_bf16(BN, BM, 0, 0);  // v x dout^T
-            constexpr uint32_t IDESC_DV = idesc_bf16(BN, D, 0, 1);   // P^T (smem, K-major) x dout (MN-major)
+            constexpr uint32_t IDESC_DV = idesc_bf16(BN, D, 0, 1);   // P^T (TMEM) x dout (MN-major)
             constexpr uint32_t IDESC_DK = idesc_f16(BN, D, 0, 1);    // dS^T (TMEM) x qhat (MN-major)
             auto issue_s = [&](int st) {
                 const uint32_t q_s = sb + S::OFF_Q + st * S::QBYTES;
@@ -272,27 +266,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int it = 0; ok && it < n_tot; ++it) {
                 const int st = it & 1;
                 const bool more = it + 1 < n_tot;
-                // S^T of the next block as soon as the softmax warps hold S^T(it)
-                if (more) {
-                    if (!mbar_wait(bar(S_READ), it & 1, 0x217) ||
-                        !mbar_wait(bar(QF + (st ^ 1)), ((it + 1) >> 1) & 1, 0x214)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_s(st ^ 1);
-                }
-                // dV += P^T dout, P^T from the shared-memory tile
                 if (!mbar_wait(bar(P_FULL), it & 1, 0x213)) { ok = false; break; }
                 tc_fence_after();
                 {
                     const uint32_t do_s = sb + S::OFF_DO + st * S::QBYTES;
 #pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_bf16(tmem + TM_DV, sdesc_sw128(sb + S::OFF_P + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(do_s + kk * (16 * 128), BM * 128, 1024), IDESC_DV,
-                                 (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(P_FREE));
+                        mma_ts(tmem + TM_DV, tmem + TM_S + packed_col(kk),
+                               sdesc_sw128(do_s + kk * (16 * 128), BM * 128, 1024), IDESC_DV,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (more) {
+                    if (!mbar_wait(bar(QF + (st ^ 1)), ((it + 1) >> 1) & 1, 0x214)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_s(st ^ 1);
                 }
                 // dK += dS^T qhat, then dP^T of the next block over dS^T
                 if (!mbar_wait(bar(DS_FULL), it & 1, 0x215)) { ok = false; break; }
@@ -345,8 +332,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld32(ts + cbase, r[0]);
                 tmem_ld32(ts + cbase + 32, r[1]);
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive_warp(bar(S_READ));  // S^T is in registers: the next S^T may overwrite it
                 auto exp_block = [&](auto masked) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -375,12 +360,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             // P^T into the shared-memory tile (K-major, 128-byte swizzled: this
             // thread's 64 queries of key row `row`) once dV(it-1) has read it
-            if (it > 0 && !mbar_wait_warp(bar(P_FREE), (it - 1) & 1, 0x314)) { ok = false; break; }
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                *reinterpret_cast<uint4*>(smem + S::OFF_P + tile16_off(row, cbase + 8 * g)) =
-                    make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-            fence_proxy_async_smem();
+            tmem_st16(ts + cbase, pk);
+            tmem_st16(ts + cbase + 16, pk + 16);
+            tmem_wait_st();
+            tc_fence_before();
             mbar_arrive_warp(bar(P_FULL));
             // dS^T = P^T o (dP^T - delta) * alpha as fp16 pairs over this half's dP^T columns
             if (!mbar_wait_warp(bar(DP_FULL), it & 1, 0x313)) { ok = false; break; }
@@ -411,20 +394,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_st16(tdp + cbase, w);
                 tmem_st16(tdp + cbase + 16, w + 16);
                 // the same fp16 alpha dS^T row half into the scratch block
-                // (query tile qb, key tile kt) of query head h.  Transposed
-                // in 16-byte chunks across each 8-lane group first, so that
-                // each warp store writes four whole 128-byte rows (one per
-                // 8-lane group) instead of 16 bytes of 32 different rows.
+                // (query tile qb, key tile kt) of query head h.  Transposed in
+                // 16-byte chunks across each 4-lane group first, so that each
+                // warp store writes 64 contiguous bytes of each of 8 rows
+                // instead of 16 bytes of 32 rows.  (A full 8 x 8 transpose,
+                // whole 128-byte rows per store, measured slower: its extra
+                // shuffle stage costs more than the half-line stores save.)
                 uint4 ch[8];
 #pragma unroll
                 for (int g = 0; g < 8; ++g) ch[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-                transpose8_chunks(ch);
+                transpose4_chunks(ch);
                 const int h = hk * G + it / n_it;
                 __half* blk = ds_out + bwdq::ds_block(static_cast<long long>(b) * H + h, nqb, qb, kt) * (BN * BM);
-                const int key0 = quarter * 32 + 8 * (lane >> 3);  // + k: the row this lane stores at step k
+                const int key0 = quarter * 32 + 4 * (lane >> 2);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    __half* p = blk + bwdq::ds_offset(key0 + k, cbase + 8 * (lane & 7));
+                    // lane 4j + c now holds (row 4j + (k & 3), chunk c + 4 (k >> 2)) in ch[k]
+                    __half* p = blk + bwdq::ds_offset(key0 + (k & 3), cbase + 8 * ((lane & 3) + 4 * (k >> 2)));
                     if (NC_IN_RANGE(p, 16, 0x412)) *reinterpret_cast<uint4*>(p) = ch[k];
                 }
             }

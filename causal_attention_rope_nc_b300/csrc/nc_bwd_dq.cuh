@@ -8,24 +8,35 @@
 // scratch buffer in HBM: the dS^T block of (query tile i, key tile j) of one
 // (batch, query head) is a [128 keys][128 queries] fp16 tile holding
 // alpha * dS (alpha: the call's one power-of-two scale, ds_scale_global,
-// undone in the epilogue).  This kernel
-// is then a streaming GEMM per query tile,
-//   dQhat_i = sum_j dS_ij khat_j          (M=128 queries, N=D, K=128 keys per tile),
+// undone in the epilogue).  This kernel is then a streaming GEMM per query
+// tile,
+//   dQhat_i = sum_j dS_ij khat_j          (M=128 queries, N=D, K=64 keys per stage),
 // that reads each dS block once (32 KB per 128 x D x 128 product: it is HBM
 // bound), recomputes nothing and uses no atomics: each dQ element is
 // produced by exactly one CTA.
 //
-// One CTA per 128-query tile i of one (batch, head), walking the key tiles
-// j it can see (j <= i; with a sliding window W -- query q sees key k when
-// 0 <= q - k < W -- from the tile of the first query's oldest visible key):
-//   warp 8      TMA producer: (dS^T block, khat tile) pairs into an NST-stage ring
+// Persistent: one CTA per SM takes query tiles until none are left, so that a
+// tile's epilogue overlaps the next tile's loads and products:
+//   warp 8      TMA producer: (dS^T half-block, khat half-tile) pairs of 64
+//               keys into an NST-stage ring, tile after tile
+//   warp 10     TMA producer of the epilogue tiles: the tile's raw q rows and
+//               RoPE table rows, once the previous tile's epilogue is done
 //   warp 9      MMA issuer (one thread): A = alpha dS (the MN-major view of
-//               the dS^T tile), B = khat (MN-major), both fp16, fp32
-//               accumulator in TMEM
+//               the dS^T stage), B = khat (MN-major), both fp16; the fp32
+//               accumulator alternates between two TMEM buffers
 //   warps 0-7   epilogue: two threads per query row apply RoPE^T and the
-//               RMSNorm backward to dQhat, stage dq, TMA store
-// The raw q rows and the RoPE table rows that the epilogue needs are loaded
-// into ring stages as the last tiles free them.
+//               RMSNorm backward to dQhat, overwrite the raw q rows with dq
+//               (each thread only the columns it read) and store them by TMA
+// Tile order: the grouped order of the other kernels ((batch, head) pairs
+// in groups of about one wave, the longest walks first inside a group, so
+// that a group's khat tiles stay in L2), handed out dynamically: the ring
+// producer takes the next tile from a global counter and passes its index
+// to the other roles through a 4-slot queue in shared memory, so every CTA
+// keeps streaming until the list runs out.  (A static deal of the tiles
+// sorted by length balanced the CTAs but spread them over 148 heads at a
+// time and doubled the HBM traffic.)  With a sliding window
+// (query q sees key k when 0 <= q - k < W) a tile walks the key tiles from
+// the one holding its first query's oldest visible key.
 #pragma once
 
 #include "nc_common.cuh"
@@ -34,21 +45,30 @@
 namespace nc {
 namespace bwdq {
 
-constexpr int BM = 128;  // queries per CTA
-constexpr int BN = 128;  // keys per tile
-constexpr int NST = 3;   // ring stages
+constexpr int BM = 128;    // queries per tile
+constexpr int BN = 128;    // keys per dS block
+constexpr int KS = 64;     // keys per ring stage (half a block)
+constexpr int NST = 4;     // ring stages
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
-constexpr int NUM_THREADS = 10 * 32;
+constexpr int WARP_EPI_TMA = 10;
+constexpr int NUM_THREADS = 11 * 32;
+
+constexpr int NQ = 4;      // tile-index queue slots
 
 enum Bar {
-    FULL = 0,      // +stage
-    EMPTY = 3,     // +stage
-    DQ_FULL = 6,
-    EPI_FULL = 7,  // raw q tile and RoPE table tile staged for the epilogue
-    MMA_DONE = 8,
-    NUM_BARS = 9
+    FULL = 0,        // +stage
+    EMPTY = 4,       // +stage
+    DQ_FULL = 8,     // +buffer: the tile's dQhat is in TMEM
+    DQ_EMPTY = 10,   // +buffer: the epilogue has read it
+    EPI_FULL = 12,   // raw q tile and RoPE table tile of the tile staged
+    EPI_EMPTY = 13,  // the previous tile's epilogue is done with them
+    MMA_DONE = 14,
+    TQ_FULL = 15,    // +slot: a tile index (or -1: no more) in the queue
+    TQ_EMPTY = 19,   // +slot: every consumer has read it
+    NUM_BARS = 23
 };
+constexpr int TQ_READERS = 10;  // the MMA thread, the epilogue producer, 8 epilogue warps
 
 // Index of the dS^T block (query tile i, key tile j <= i) of one (batch,
 // query head) bh in the scratch: the causal triangle of each (b, h), in
@@ -66,36 +86,50 @@ __host__ __device__ __forceinline__ int ds_offset(int key, int query) {
 
 template <int D>
 struct Smem {
-    static constexpr int DSBYTES = BN * BM * 2;  // one dS^T block
-    static constexpr int KBYTES = BN * D * 2;    // one khat tile
+    static constexpr int DSBYTES = KS * BM * 2;  // 64 keys x 128 queries of dS^T (two 8 KB query halves)
+    static constexpr int KBYTES = KS * D * 2;    // 64 keys of khat (D/64 halves of 8 KB)
     static constexpr int STAGE = DSBYTES + KBYTES;
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_BAR = OFF_RING + NST * STAGE;
-    static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
-    static constexpr int BYTES = OFF_TSLOT + 16;
-    static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
-    // epilogue (over the ring once its stages are free): raw q [128][D] bf16
-    // and the first half of the RoPE table [128][D] fp32 in stage s_a, the
-    // second half of the table in stage s_b (the stages of tiles n_kv - 2 and
-    // n_kv - 3), the dq staging tile and the row-half exchange in the last
-    // tile's stage
+    static constexpr int OFF_X = OFF_RING + NST * STAGE;  // raw q [128][D] bf16 (TMA box layout), then dq
     static constexpr int XBYTES = BM * D * 2;
-    static constexpr int CBYTES = BM * D * 4;
-    static_assert(XBYTES + CBYTES / 2 <= STAGE && XBYTES + 2 * BM * 8 <= STAGE, "epilogue tiles exceed the stages");
-    static_assert(ALLOC <= 232448, "dQ ring exceeds shared memory");
+    static constexpr int OFF_TAB = OFF_X + XBYTES;  // RoPE table rows [128][D] fp32: D/32 boxes of 32 floats
+    static constexpr int TBYTES = BM * D * 4;
+    static constexpr int OFF_XCH = OFF_TAB + TBYTES;  // row-half exchange, 2 x 128 float2
+    static constexpr int OFF_BAR = OFF_XCH + 2 * BM * 8;
+    static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_TQ = OFF_TSLOT + 16;  // NQ tile indices
+    static constexpr int BYTES = OFF_TQ + NQ * 4;
+    // the base is 1024-aligned (the declaration asks for it); whatever slack
+    // is left below the opt-in limit stays for smem_align1024
+    static constexpr int ALLOC = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
+    static_assert(BYTES <= 232448, "dQ buffers exceed shared memory");
 };
 
-constexpr uint32_t TMEM_COLS = 128;  // the dQ accumulator (D <= 128 columns)
+constexpr uint32_t TMEM_COLS = 256;  // two dQ accumulators of D <= 128 columns
+
+// Tile idx of the grouped order: (query tile, (b, h)).
+struct DqTile {
+    int qt;  // query tile
+    int bh;  // b * H + h
+};
+__device__ __forceinline__ DqTile dq_tile(int idx, int n_qt, int nbh, int group) {
+    const TileCoord c = grouped_tile(idx, nbh, n_qt, group);
+    DqTile t;
+    t.qt = n_qt - 1 - c.rank;
+    t.bh = c.bh;
+    return t;
+}
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
-                       const __grid_constant__ CUtensorMap tm_dq, const unsigned int* __restrict__ gmax, int T,
-                       int H, int B, int group, float scale, float eps, int W, int G) {
+                       const __grid_constant__ CUtensorMap tm_dq, const unsigned int* __restrict__ gmax,
+                       unsigned int* __restrict__ tile_counter, int T, int H, int B, int group, float scale, float eps,
+                       int W, int G) {
     using S = Smem<D>;
     constexpr int NC = D / 64;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw, S::BYTES, S::ALLOC);
     if (smem == nullptr) {  // uniform over the CTA: nothing has started yet
         if (threadIdx.x == 0) flag_error(3, 0x2f0);
@@ -103,30 +137,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grouped (b, h) order, longest walks (the last query tile) first in a group
     const int n_qt = (T + BM - 1) / BM;
-    const TileCoord tc = grouped_tile(static_cast<int>(blockIdx.x), B * H, n_qt, group);
-    const int qt = n_qt - 1 - tc.rank;
-    const int b = tc.bh / H, h = tc.bh % H;
-    const int hk = h / G;  // key/value head (grouped-query attention; G = 1: hk = h)
-    const int kt_lo = max(0, qt * BM - W + 1) / BN;  // first visible key tile (W >= 2^30: none cut)
-    const int n_kv = qt - kt_lo + 1;                  // BM == BN: key tiles kt_lo..qt
+    const int nbh = B * H;
+    const int n_tiles = n_qt * nbh;
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
     auto stage = [&](int s) -> uint32_t { return sb + S::OFF_RING + s * S::STAGE; };
+    auto kt_lo_of = [&](int qt) { return max(0, qt * BM - W + 1) / BN; };  // W >= 2^30: none cut
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
-    const long long blk0 = ds_block(tc.bh, n_qt, qt, 0);  // dS^T block of key tile 0
-    // epilogue space: the stages of tiles n_kv - 2 (s_a) and n_kv - 3 (s_b),
-    // free from the start when those tiles do not exist, and the last tile's
-    const int s_last = (n_kv - 1) % NST, s_a = (n_kv + 1) % NST, s_b = n_kv % NST;
+    volatile int* tq = reinterpret_cast<volatile int*>(smem + S::OFF_TQ);
+    // the n-th tile of this CTA from the queue (every consumer reads every slot
+    // once, in order); -1: no more tiles, or a wait gave up
+    auto next_tile = [&](int n, bool warp_wide) -> int {
+        const int q = n % NQ;
+        const bool ok = warp_wide ? mbar_wait_warp(bar(TQ_FULL + q), (n / NQ) & 1, 0x230)
+                                  : mbar_wait(bar(TQ_FULL + q), (n / NQ) & 1, 0x230);
+        const int idx = ok ? tq[q] : -1;
+        if (warp_wide)
+            mbar_arrive_warp(bar(TQ_EMPTY + q));
+        else
+            mbar_arrive(bar(TQ_EMPTY + q));
+        return idx;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar(FULL + s), 1);
             mbar_init(bar(EMPTY + s), 1);
         }
-        mbar_init(bar(DQ_FULL), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(DQ_FULL + i), 1);
+            mbar_init(bar(DQ_EMPTY + i), 8);  // one arrival per epilogue warp
+        }
         mbar_init(bar(EPI_FULL), 1);
+        mbar_init(bar(EPI_EMPTY), 1);
         mbar_init(bar(MMA_DONE), 1);
+        for (int q = 0; q < NQ; ++q) {
+            mbar_init(bar(TQ_FULL + q), 1);
+            mbar_init(bar(TQ_EMPTY + q), TQ_READERS);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -139,66 +187,101 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tslot;
 
     if (warp == WARP_TMA) {
-        // ------------------------------------------------ TMA producer ----
+        // -------------------------------------------- ring producer ----
         if (lane == 0) {
-            int issued[NST] = {0, 0, 0};
+            int x = 0;  // stages filled so far (all tiles)
+            int issued[NST] = {0, 0, 0, 0};
             bool ok = true;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % NST;
-                if (j >= NST && !mbar_wait(bar(EMPTY + s), (j / NST - 1) & 1, 0x121)) {
-                    ok = false;
-                    break;
+            for (int n = 0; ok; ++n) {
+                // take the next tile and publish it to the other roles
+                const int q = n % NQ;
+                if (n >= NQ && !mbar_wait(bar(TQ_EMPTY + q), (n / NQ - 1) & 1, 0x231)) break;
+                const unsigned int got = atomicAdd(tile_counter, 1u);
+                const int idx = got < static_cast<unsigned int>(n_tiles) ? static_cast<int>(got) : -1;
+                tq[q] = idx;
+                mbar_arrive(bar(TQ_FULL + q));
+                if (idx < 0) break;
+                const DqTile tl = dq_tile(idx, n_qt, nbh, group);
+                const int b = tl.bh / H, hk = (tl.bh % H) / G;
+                const int kt_lo = kt_lo_of(tl.qt);
+                const long long blk0 = ds_block(tl.bh, n_qt, tl.qt, 0);
+                for (int kt = kt_lo; ok && kt <= tl.qt; ++kt) {
+                    for (int half = 0; half < 2; ++half, ++x) {
+                        const int s = x % NST, use = x / NST;
+                        if (x >= NST && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, 0x121)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(bar(FULL + s), S::STAGE);
+                        // keys kt*128 + 64 half .. + 63: rows of both query halves of the block
+                        const int row = static_cast<int>((blk0 + kt) * 2 * BN) + half * KS;  // < 2^31 (host check)
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d(stage(s) + c * (KS * 128), &tm_ds, 0, row + c * BN, bar(FULL + s));
+                        for (int c = 0; c < NC; ++c)
+                            tma_load_4d(stage(s) + S::DSBYTES + c * (KS * 128), &tm_k, c * 64, hk,
+                                        kt * BN + half * KS, b, bar(FULL + s));
+                        ++issued[s];
+                    }
                 }
-                const int kt = kt_lo + j;
-                mbar_expect_tx(bar(FULL + s), S::STAGE);
-                const int row = static_cast<int>((blk0 + kt) * 2 * BN);  // < 2^31 (checked by the host)
-                for (int c = 0; c < 2; ++c)
-                    tma_load_2d(stage(s) + c * (BN * 128), &tm_ds, 0, row + c * BN, bar(FULL + s));
-                for (int c = 0; c < NC; ++c)
-                    tma_load_4d(stage(s) + S::DSBYTES + c * (BN * 128), &tm_k, c * 64, hk, kt * BN, b,
-                                bar(FULL + s));
-                ++issued[s];
-            }
-            // epilogue tiles, each as soon as its stage is released
-            mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::CBYTES);
-            bool epi = ok && (n_kv < 2 || mbar_wait(bar(EMPTY + s_a), ((n_kv - 2) / NST) & 1, 0x128));
-            if (epi) {
-                for (int c = 0; c < NC; ++c)
-                    tma_load_4d(stage(s_a) + c * (BM * 128), &tm_qraw, c * 64, h, qt * BM, b, bar(EPI_FULL));
-                for (int c = 0; c < NC; ++c)
-                    tma_load_2d(stage(s_a) + S::XBYTES + c * (BM * 128), &tm_tab, c * 32, qt * BM, bar(EPI_FULL));
-            }
-            epi = epi && (n_kv < 3 || mbar_wait(bar(EMPTY + s_b), ((n_kv - 3) / NST) & 1, 0x129));
-            if (epi) {
-                for (int c = 0; c < NC; ++c)
-                    tma_load_2d(stage(s_b) + c * (BM * 128), &tm_tab, (NC + c) * 32, qt * BM, bar(EPI_FULL));
             }
             // never leave the CTA with a bulk copy still in flight
             for (int s = 0; s < NST; ++s)
                 if (issued[s]) mbar_wait(bar(FULL + s), (issued[s] - 1) & 1, 0x124);
-            if (epi) mbar_wait(bar(EPI_FULL), 0, 0x127);
+        }
+        __syncwarp();
+    } else if (warp == WARP_EPI_TMA) {
+        // ------------------------------- epilogue tile producer ----
+        if (lane == 0) {
+            int issued = 0;
+            for (int n = 0;; ++n) {
+                const int idx = next_tile(n, false);
+                if (idx < 0) break;
+                // the previous tile's epilogue has stored its dq (read the buffers)
+                if (n > 0 && !mbar_wait(bar(EPI_EMPTY), (n - 1) & 1, 0x128)) break;
+                const DqTile tl = dq_tile(idx, n_qt, nbh, group);
+                const int b = tl.bh / H, h = tl.bh % H;
+                mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::TBYTES);
+                for (int c = 0; c < NC; ++c)
+                    tma_load_4d(sb + S::OFF_X + c * (BM * 128), &tm_qraw, c * 64, h, tl.qt * BM, b, bar(EPI_FULL));
+                for (int c = 0; c < D / 32; ++c)
+                    tma_load_2d(sb + S::OFF_TAB + c * (BM * 128), &tm_tab, c * 32, tl.qt * BM, bar(EPI_FULL));
+                ++issued;
+            }
+            if (issued) mbar_wait(bar(EPI_FULL), (issued - 1) & 1, 0x127);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------- MMA issuer -----
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_f16(BM, D, 1, 1);  // alpha dS (MN-major) x khat (MN-major), fp16
+            int x = 0;
             bool ok = true;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % NST;
-                if (!mbar_wait(bar(FULL + s), (j / NST) & 1, 0x221)) {
-                    ok = false;
-                    break;
-                }
+            for (int n = 0; ok; ++n) {
+                const int idx = next_tile(n, false);
+                if (idx < 0) break;
+                const DqTile tl = dq_tile(idx, n_qt, nbh, group);
+                const int buf = n & 1;
+                // the epilogue of tile n - 2 has read this accumulator
+                if (n >= 2 && !mbar_wait(bar(DQ_EMPTY + buf), ((n - 2) >> 1) & 1, 0x225)) break;
                 tc_fence_after();
+                const uint32_t acc = tmem + buf * 128;
+                const int steps = 2 * (tl.qt - kt_lo_of(tl.qt) + 1);
+                for (int j = 0; j < steps; ++j, ++x) {
+                    const int s = x % NST;
+                    if (!mbar_wait(bar(FULL + s), (x / NST) & 1, 0x221)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16(tmem, sdesc_sw128(stage(s) + kk * (16 * 128), BN * 128, 1024),
-                             sdesc_sw128(stage(s) + S::DSBYTES + kk * (16 * 128), BN * 128, 1024), IDESC,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(EMPTY + s));
+                    for (int kk = 0; kk < KS / 16; ++kk)
+                        mma_bf16(acc, sdesc_sw128(stage(s) + kk * (16 * 128), KS * 128, 1024),
+                                 sdesc_sw128(stage(s) + S::DSBYTES + kk * (16 * 128), KS * 128, 1024), IDESC,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(EMPTY + s));
+                }
+                if (ok) mma_commit(bar(DQ_FULL + buf));
             }
-            if (ok) mma_commit(bar(DQ_FULL));
             // all MMAs issued by this thread complete before teardown
             mma_commit(bar(MMA_DONE));
             mbar_wait(bar(MMA_DONE), 0, 0x224);
@@ -211,21 +294,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        bool epi = named_bar_and(1, 256, mbar_wait_warp(bar(DQ_FULL), 0, 0x323));
-        epi = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), 0, 0x324));
-        if (epi) tc_fence_after();
-        uint8_t* last = smem + S::OFF_RING + s_last * S::STAGE;
-        uint8_t* sa = smem + S::OFF_RING + s_a * S::STAGE;
-        // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha))
         const float alpha = ds_scale_global(gmax);
-        norm_rope_bwd_stage<D>(epi, tmem + lane_base, scale / alpha, sa, sa + S::XBYTES, smem + S::OFF_RING + s_b * S::STAGE,
-                               row, half, eps, reinterpret_cast<float2*>(last + S::XBYTES), last, 1, 256);
-        if (epi) fence_proxy_async_smem();
-        named_bar_sync(1, 256);
-        if (epi && threadIdx.x == 0) {
-            for (int c = 0; c < NC; ++c) tma_store_4d(&tm_dq, smem_u32(last) + c * (BM * 128), c * 64, h, qt * BM, b);
-            bulk_commit();
-            bulk_wait_read_all();  // the staged tile stays valid until the stores have read it
+        uint8_t* xq = smem + S::OFF_X;
+        for (int n = 0;; ++n) {
+            const int idx = next_tile(n, true);
+            if (idx < 0) break;  // uniform over each warp (it read the slot as one)
+            const DqTile tl = dq_tile(idx, n_qt, nbh, group);
+            const int buf = n & 1;
+            bool epi = named_bar_and(1, 256, mbar_wait_warp(bar(DQ_FULL + buf), (n >> 1) & 1, 0x323));
+            epi = named_bar_and(1, 256, epi && mbar_wait_warp(bar(EPI_FULL), n & 1, 0x324));
+            if (!epi) break;  // uniform: a wait gave up (recorded)
+            tc_fence_after();
+            // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)), written over the raw q rows
+            norm_rope_bwd_stage<D>(true, tmem + lane_base + buf * 128, scale / alpha, xq, smem + S::OFF_TAB,
+                                   smem + S::OFF_TAB + NC * (BM * 128), row, half, eps,
+                                   reinterpret_cast<float2*>(smem + S::OFF_XCH), xq, 1, 256);
+            // the accumulator has been read (norm_rope_bwd_stage waits for its TMEM loads)
+            tc_fence_before();
+            mbar_arrive_warp(bar(DQ_EMPTY + buf));
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 0) {
+                const int b = tl.bh / H, h = tl.bh % H;
+                for (int c = 0; c < NC; ++c)
+                    tma_store_4d(&tm_dq, smem_u32(xq) + c * (BM * 128), c * 64, h, tl.qt * BM, b);
+                bulk_commit();
+                bulk_wait_read_all();  // the staged rows stay valid until the stores have read them
+                mbar_arrive(bar(EPI_EMPTY));
+            }
         }
     }
     tc_fence_before();

@@ -168,15 +168,16 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
     }
 }
 
-// 8 x 8 transpose of 16-byte chunks inside each group of 8 lanes (lanes
-// 8j .. 8j + 7): before, lane 8j + r holds chunks (r, 0..7) in c[0..7];
-// after, lane 8j + k holds chunks (0..7, k), chunk (r, k) in c[r].  Three
-// butterfly stages (xor 4, 2, 1), each trading half of the chunks with the
-// partner lane.  All 32 lanes must take part.
-__device__ __forceinline__ void transpose8_chunks(uint4 (&c)[8]) {
-    const int r = threadIdx.x & 7;
+// Two 4 x 4 transposes of 16-byte chunks inside each group of 4 lanes
+// (lanes 4j .. 4j + 3), one over chunks 0-3 and one over chunks 4-7: before,
+// lane 4j + r holds chunks (r, 0..7) in c[0..7]; after, lane 4j + k holds
+// chunks (r, k) in c[r] and (r, 4 + k) in c[4 + r], r = 0..3.  Two butterfly
+// stages (xor 2, 1), each trading half of the chunks with the partner lane.
+// All 32 lanes must take part.
+__device__ __forceinline__ void transpose4_chunks(uint4 (&c)[8]) {
+    const int r = threadIdx.x & 3;
 #pragma unroll
-    for (int d = 4; d > 0; d >>= 1) {
+    for (int d = 2; d > 0; d >>= 1) {
         const bool up = (r & d) != 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {

@@ -105,15 +105,18 @@ int nc_last_cuda_error(void);
  * 2 = a decode length outside [1, Tcap] or a prefill chunk outside its cache.  Returns NC_OK or NC_ELAUNCH. */
 int nc_device_status(nc_stream_t stream, unsigned int *status);
 
-/* Optional per-kernel timing.  While enabled (on != 0), every kernel the
- * library launches is bracketed by two CUDA events recorded on the launch
- * stream.  nc_profile_read() waits for the recorded events, writes up to
- * max_entries per-kernel sums (launch count, total milliseconds) to `out`,
- * sets *n_entries to the number of distinct kernels, and clears the
+/* Optional per-kernel timing.  While enabled (on != 0), every step of a
+ * call (one kernel, or a few launched back to back under one name: the
+ * forward's two launches, the prologue's q and k launches with grouped-query
+ * attention) is bracketed by two CUDA events recorded on the launch stream.
+ * nc_profile_read() waits for the recorded events, writes up to max_entries
+ * per-name sums (steps timed, kernels launched, total milliseconds) to
+ * `out`, sets *n_entries to the number of distinct names, and clears the
  * record.  Timing does not change what the kernels compute. */
 typedef struct {
     char name[48];
-    int launches;
+    int launches; /* timed steps */
+    int kernels;  /* kernel launches inside them */
     double total_ms;
 } nc_kernel_time;
 
