@@ -512,7 +512,7 @@ def bench_fp8(nc, dev, args, w, qd, kd, vd, stream):
         tf = flops / (t_ / n_ * 1e-3) / 1e12
         kernels["attn_fwd_fp8"]["tflops"] = round(tf, 1)
         kernels["attn_fwd_fp8"]["frac_of_fp8_peak"] = round(tf / peak8, 4)
-    return {"workload": "d20 forward with E4M3 products (qhat, khat at 2^5; v per head; P at 2^8)",
+    return {"workload": f"{w.name} forward with E4M3 products (qhat, khat at 2^5; v per head; P at 2^8)",
             "ms_per_call": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "fp8_peak_tflops": round(peak8, 1), "kernels": kernels}
 
@@ -541,7 +541,11 @@ def bench_decode(nc, dev, args, rank, window=0, kv_heads=None):
     torch.cuda.synchronize(dev)
     times = []
     for _ in range(max(args.steps, 5)):
+        # evict the cache and the previous call's lines from L2: write a buffer
+        # larger than L2, then read it back, so that no dirty line of the flush
+        # is still being written back to HBM while the timed call runs
         flush.zero_()
+        flush.view(torch.int32).sum()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         call()
@@ -564,7 +568,7 @@ def bench_decode(nc, dev, args, rank, window=0, kv_heads=None):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
                          "frac_of_spec": round(gbs / SPEC["hbm_gbs"], 4)},
-            "l2": "256 MB buffer written between calls", "tokens_per_s": round(w.B / (ms * 1e-3), 1)}
+            "l2": "256 MB buffer written, then read, between calls", "tokens_per_s": round(w.B / (ms * 1e-3), 1)}
 
 
 def bench_e2e(nc, dev, args, w, q, k, v, dout, ws_f, ws_b):
@@ -710,6 +714,27 @@ def bench_reference(args, ws_n, rank):
     }
 
 
+def bench_leg(args):
+    """One side leg alone (for profiling a single kernel family under ncu):
+    prints that leg's JSON object and nothing else."""
+    import causal_attention_rope_nc_b300 as nc
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.leg == "decode":
+        res = bench_decode(nc, dev, args, 0)
+    elif args.leg == "decode-gqa":
+        res = bench_decode(nc, dev, args, 0, kv_heads=GQA_KV_HEADS)
+    elif args.leg == "decode-window":
+        res = bench_decode(nc, dev, args, 0, window=workloads.D20.T // 4)
+    else:  # fp8
+        w = workloads.ATTN_WORKLOADS[args.workload]
+        q, k, v, _ = workloads.attn_inputs(w.B, w.T, w.H, w.D, w.seed)
+        qd, kd, vd = (x.to(dev) for x in (q, k, v))
+        res = bench_fp8(nc, dev, args, w, qd, kd, vd, torch.cuda.current_stream(dev))
+    res["leg"] = args.leg
+    print(json.dumps(res), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -721,9 +746,14 @@ def main():
                     help="fwd+bwd shape (the headline metric is quoted on d20; others for profiling)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the decode and end-to-end legs (short runs under a profiler)")
+    ap.add_argument("--leg", choices=["all", "decode", "decode-gqa", "decode-window", "fp8"], default="all",
+                    help="run one side leg alone and print its object (profiling); default: the full line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.leg != "all":
+        bench_leg(args)
+        return
     ws_n, rank, local = dist_env()
     if args.impl == "reference":
         line = bench_reference(args, ws_n, rank)

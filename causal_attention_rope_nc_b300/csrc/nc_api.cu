@@ -461,7 +461,7 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         const int grid = static_cast<int>(n_tiles < g_sm_count[dev] ? n_tiles : g_sm_count[dev]);
         ProfScope ps("attn_bwd_dq", s);
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid), nc::bwdq::NUM_THREADS,
-                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk64, tqr, ttab, tdq, gmax, gmax + 2, T,
+                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk64, tqr, tab, tdq, gmax, gmax + 2, T,
                                                                          H, B, group, float(scale), eps, W, G);
     }
     return launch_status();
@@ -623,17 +623,20 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
     nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
     for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
     if (Hkv == H) {
-        // multi-head attention: the register-pipelined kernel, one warp per head
+        // multi-head attention: the register-pipelined kernel, one warp per
+        // head, the heads split over head groups
         const int nparts = (Tcap + nc::dec::PART_SLOTS - 1) / nc::dec::PART_SLOTS;
-        const int nch = (Tcap + nc::dec::CH - 1) / nc::dec::CH;
-        const int warps = H < nc::dec::MAX_WARPS ? H : nc::dec::MAX_WARPS;
+        const int G = H / Hkv;
+        const nc::dec::RegSplit rs = nc::dec::reg_split(H, G);
+        const int nch = (Tcap + rs.ch - 1) / rs.ch;
         ProfScope ps("attn_decode", s);
-        nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B)), warps * 32, 0,
-                                         s>>>(
+        nc::dec::attn_decode_kernel<D><<<dim3(static_cast<unsigned>(nch), static_cast<unsigned>(B),
+                                              static_cast<unsigned>(rs.groups)),
+                                         rs.warps * 32, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
             reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(kcache),
             reinterpret_cast<__nv_bfloat16*>(vcache), lens, reinterpret_cast<__nv_bfloat16*>(out), ws.part_o,
-            ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, scale_log2, W, 1);
+            ws.part_ml, ws.counters, B, H, Tcap, nparts, eps, th, scale_log2, W, G, rs.ch, rs.hpg);
         return launch_status();
     }
     // grouped-query attention: the TMA ring kernel

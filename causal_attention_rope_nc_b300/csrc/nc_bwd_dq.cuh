@@ -19,14 +19,17 @@
 // tile's epilogue overlaps the next tile's loads and products:
 //   warp 8      TMA producer: (dS^T half-block, khat half-tile) pairs of 64
 //               keys into an NST-stage ring, tile after tile
-//   warp 10     TMA producer of the epilogue tiles: the tile's raw q rows and
-//               RoPE table rows, once the previous tile's epilogue is done
+//   warp 10     TMA producer of the epilogue tile: the tile's raw q rows,
+//               once the previous tile's epilogue is done
 //   warp 9      MMA issuer (one thread): A = alpha dS (the MN-major view of
 //               the dS^T stage), B = khat (MN-major), both fp16; the fp32
 //               accumulator alternates between two TMEM buffers
 //   warps 0-7   epilogue: two threads per query row apply RoPE^T and the
 //               RMSNorm backward to dQhat, overwrite the raw q rows with dq
-//               (each thread only the columns it read) and store them by TMA
+//               (each thread only the columns it read) and store them by TMA;
+//               the RoPE table rows come from L2 (the table is T x D floats),
+//               which leaves the shared memory to the ring: six stages of 32 KB
+//               in flight per SM keep the dS stream near the HBM rate
 // Tile order: the grouped order of the other kernels ((batch, head) pairs
 // in groups of about one wave, the longest walks first inside a group, so
 // that a group's khat tiles stay in L2), handed out dynamically: the ring
@@ -48,7 +51,7 @@ namespace bwdq {
 constexpr int BM = 128;    // queries per tile
 constexpr int BN = 128;    // keys per dS block
 constexpr int KS = 64;     // keys per ring stage (half a block)
-constexpr int NST = 4;     // ring stages
+constexpr int NST = 6;     // ring stages
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int WARP_EPI_TMA = 10;
@@ -57,16 +60,16 @@ constexpr int NUM_THREADS = 11 * 32;
 constexpr int NQ = 4;      // tile-index queue slots
 
 enum Bar {
-    FULL = 0,        // +stage
-    EMPTY = 4,       // +stage
-    DQ_FULL = 8,     // +buffer: the tile's dQhat is in TMEM
-    DQ_EMPTY = 10,   // +buffer: the epilogue has read it
-    EPI_FULL = 12,   // raw q tile and RoPE table tile of the tile staged
-    EPI_EMPTY = 13,  // the previous tile's epilogue is done with them
-    MMA_DONE = 14,
-    TQ_FULL = 15,    // +slot: a tile index (or -1: no more) in the queue
-    TQ_EMPTY = 19,   // +slot: every consumer has read it
-    NUM_BARS = 23
+    FULL = 0,                  // +stage
+    EMPTY = FULL + NST,        // +stage
+    DQ_FULL = EMPTY + NST,     // +buffer: the tile's dQhat is in TMEM
+    DQ_EMPTY = DQ_FULL + 2,    // +buffer: the epilogue has read it
+    EPI_FULL = DQ_EMPTY + 2,   // raw q tile of the tile staged
+    EPI_EMPTY = EPI_FULL + 1,  // the previous tile's epilogue is done with it
+    MMA_DONE = EPI_EMPTY + 1,
+    TQ_FULL = MMA_DONE + 1,    // +slot: a tile index (or -1: no more) in the queue
+    TQ_EMPTY = TQ_FULL + NQ,   // +slot: every consumer has read it
+    NUM_BARS = TQ_EMPTY + NQ
 };
 constexpr int TQ_READERS = 10;  // the MMA thread, the epilogue producer, 8 epilogue warps
 
@@ -92,9 +95,7 @@ struct Smem {
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_X = OFF_RING + NST * STAGE;  // raw q [128][D] bf16 (TMA box layout), then dq
     static constexpr int XBYTES = BM * D * 2;
-    static constexpr int OFF_TAB = OFF_X + XBYTES;  // RoPE table rows [128][D] fp32: D/32 boxes of 32 floats
-    static constexpr int TBYTES = BM * D * 4;
-    static constexpr int OFF_XCH = OFF_TAB + TBYTES;  // row-half exchange, 2 x 128 float2
+    static constexpr int OFF_XCH = OFF_X + XBYTES;  // row-half exchange, 2 x 128 float2
     static constexpr int OFF_BAR = OFF_XCH + 2 * BM * 8;
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TQ = OFF_TSLOT + 16;  // NQ tile indices
@@ -123,7 +124,7 @@ __device__ __forceinline__ DqTile dq_tile(int idx, int n_qt, int nbh, int group)
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_qraw, const __grid_constant__ CUtensorMap tm_tab,
+                       const __grid_constant__ CUtensorMap tm_qraw, const float2* __restrict__ tab,
                        const __grid_constant__ CUtensorMap tm_dq, const unsigned int* __restrict__ gmax,
                        unsigned int* __restrict__ tile_counter, int T, int H, int B, int group, float scale, float eps,
                        int W, int G) {
@@ -190,7 +191,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // -------------------------------------------- ring producer ----
         if (lane == 0) {
             int x = 0;  // stages filled so far (all tiles)
-            int issued[NST] = {0, 0, 0, 0};
+            int issued[NST];
+            for (int s = 0; s < NST; ++s) issued[s] = 0;
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 // take the next tile and publish it to the other roles
@@ -240,11 +242,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (n > 0 && !mbar_wait(bar(EPI_EMPTY), (n - 1) & 1, 0x128)) break;
                 const DqTile tl = dq_tile(idx, n_qt, nbh, group);
                 const int b = tl.bh / H, h = tl.bh % H;
-                mbar_expect_tx(bar(EPI_FULL), S::XBYTES + S::TBYTES);
+                mbar_expect_tx(bar(EPI_FULL), S::XBYTES);
                 for (int c = 0; c < NC; ++c)
                     tma_load_4d(sb + S::OFF_X + c * (BM * 128), &tm_qraw, c * 64, h, tl.qt * BM, b, bar(EPI_FULL));
-                for (int c = 0; c < D / 32; ++c)
-                    tma_load_2d(sb + S::OFF_TAB + c * (BM * 128), &tm_tab, c * 32, tl.qt * BM, bar(EPI_FULL));
                 ++issued;
             }
             if (issued) mbar_wait(bar(EPI_FULL), (issued - 1) & 1, 0x127);
@@ -306,9 +306,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!epi) break;  // uniform: a wait gave up (recorded)
             tc_fence_after();
             // dq = RMSNorm^T(RoPE^T(dQhat * scale / alpha)), written over the raw q rows
-            norm_rope_bwd_stage<D>(true, tmem + lane_base + buf * 128, scale / alpha, xq, smem + S::OFF_TAB,
-                                   smem + S::OFF_TAB + NC * (BM * 128), row, half, eps,
-                                   reinterpret_cast<float2*>(smem + S::OFF_XCH), xq, 1, 256);
+            // (rows past T read the last table row; the TMA store clips them)
+            const int t_row = min(tl.qt * BM + row, T - 1);
+            const uint8_t* trow = reinterpret_cast<const uint8_t*>(tab + static_cast<long long>(t_row) * (D / 2));
+            (void)NC_IN_RANGE_LOAD(trow, D * 4, 0x2f1);  // recorded only: t_row is clamped into the table
+            norm_rope_bwd_stage<D, true>(true, tmem + lane_base + buf * 128, scale / alpha, xq, trow, nullptr, row,
+                                         half, eps, reinterpret_cast<float2*>(smem + S::OFF_XCH), xq, 1, 256);
             // the accumulator has been read (norm_rope_bwd_stage waits for its TMEM loads)
             tc_fence_before();
             mbar_arrive_warp(bar(DQ_EMPTY + buf));

@@ -10,14 +10,19 @@
 // ceil(Tcap / CH) x B; a CTA whose chunk starts at or past the stream's
 // length lens[b] exits at once, so the hardware block scheduler hands the
 // real chunks to SMs as they free up and every SM streams about the same
-// number of bytes whatever the length mix.
+// number of bytes whatever the length mix.  The register kernel also splits
+// the heads over gridDim.z CTAs (head groups of whole key/value heads) and
+// takes its chunk length as an argument, so that a call has enough small
+// CTAs (several resident per SM) to keep every SM's loads in flight to the
+// end.
 //
 // Two kernels share this split and the merge below.
 //
 // attn_decode_kernel (launched for plain multi-head attention, G = 1; it is
 // correct for any G, reading key/value head h / G with cached loads when
-// G > 1 and writing every key/value head of the new slot first): warp w
-// takes heads w, w + NW, ...  For one head it walks the chunk's slots BATCH
+// G > 1 and writing the key/value heads of its head group into the new slot
+// first): warp w of head group z takes heads z HPG + w, z HPG + w + NW, ...
+// below (z + 1) HPG.  For one head it walks the chunk's slots BATCH
 // at a time: a group of D/8 lanes reads one slot's key row and value
 // row (bf16) as 16-byte pieces, 32/(D/8) slots per warp load (streaming
 // loads, evict-first).  The batches are software-pipelined over two
@@ -47,8 +52,8 @@
 //
 // A stream with one chunk writes its output directly.  Otherwise each chunk
 // stores (m, l, o) per head in the workspace, and the last CTA of the stream
-// to finish (per-stream arrival counter) merges the chunks and resets the
-// counter for the next call: per head, lanes read the chunks' (m, l) side by
+// to finish (per-stream arrival counter over every chunk and head group)
+// merges the chunks of every head and resets the counter for the next call: per head, lanes read the chunks' (m, l) side by
 // side, and the weighted partial outputs are added in chunk order
 // (deterministic), their loads issued back to back.
 //
@@ -69,8 +74,8 @@
 namespace nc {
 namespace dec {
 
-constexpr int CH = 128;          // cache slots per CTA (one partial result)
-constexpr int PART_SLOTS = 32;   // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / CH) partials
+constexpr int CH = 128;          // cache slots per CTA of the ring kernel (one partial result)
+constexpr int PART_SLOTS = 32;   // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / chunk) partials
 constexpr int MAX_WARPS = 16;    // warps per CTA of the register kernel (heads beyond this many loop)
 constexpr int MAX_CWARPS = 16;   // compute warps per CTA of the ring kernel
 constexpr int BATCH = 8;         // slots per online-softmax step
@@ -95,6 +100,34 @@ inline int ring_stages(int Hkv, int D, int sb) {
 inline size_t smem_bytes(int Hkv, int D, int sb, int nst) {
     return static_cast<size_t>(nst) * sb * Hkv * D * 4 + 2 * nst * 8;
 }
+// Launch shape of the register kernel: head groups of whole key/value heads
+// of at most REG_WARPS warps, and REG_CH slots per chunk.  (Measured on the
+// d20 decode: groups of 5 warps, three CTAs per SM, and 64-slot chunks both
+// ran within one event tick (2 us) of one 10-warp CTA per 128-slot chunk,
+// or slower with a 512-slot window; so heads are split only past 16.)
+constexpr int REG_WARPS = 16;
+constexpr int REG_CH = 128;
+struct RegSplit {
+    int hpg;     // query heads per group (a multiple of G)
+    int groups;  // head groups: gridDim.z
+    int warps;   // warps per CTA
+    int ch;      // slots per chunk
+};
+inline RegSplit reg_split(int H, int G) {
+    RegSplit r;
+    if (G == 1) {
+        r.groups = (H + REG_WARPS - 1) / REG_WARPS;
+        r.hpg = (H + r.groups - 1) / r.groups;
+    } else {
+        r.hpg = G * (REG_WARPS / G > 1 ? REG_WARPS / G : 1);
+    }
+    r.groups = (H + r.hpg - 1) / r.hpg;  // every group holds at least one head
+    r.warps = r.hpg < MAX_WARPS ? r.hpg : MAX_WARPS;
+    r.ch = REG_CH;
+    return r;
+}
+static_assert(REG_CH % (2 * BATCH) == 0 && REG_CH >= PART_SLOTS, "register kernel chunking");
+
 // Query heads per compute warp: enough that at most MAX_CWARPS warps cover H.
 inline int heads_per_warp(int H) {
     int hpw = 1;
@@ -120,63 +153,84 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // load, so a slot written earlier by the same warp is seen after __syncwarp.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
 
-// The last CTA of stream b to finish (per-stream arrival counter) merges the
-// partial results of chunks c_lo .. nch - 1 into out and resets the counter.
-// Called by every thread of a CTA that stored a partial.
-template <int D>
+// The last of the n_arrive CTAs of stream b to finish (per-stream arrival
+// counter) merges the partial results of chunks c_lo .. nch - 1 of every head
+// into out and resets the counter.  Called by every thread of a CTA that
+// stored a partial.
+template <int D, int MGRP>
 __device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, int max_parts,
                                              const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                              __nv_bfloat16* __restrict__ out, unsigned int* __restrict__ counters,
-                                             int n_parts, int* s_last) {
+                                             int n_arrive, int* s_last) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NW = static_cast<int>(blockDim.x >> 5);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0)
         *s_last = NC_IN_RANGE(counters + b, 4, 0x503) &&
-                  atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_parts - 1);
+                  atomicAdd(&counters[b], 1u) == static_cast<unsigned>(n_arrive - 1);
     __syncthreads();
     if (!*s_last) return;  // uniform
     __threadfence();
     for (int h = warp; h < H; h += NW) {
-        // lanes take the partials 32 at a time for (m, l) and the weights;
-        // lane: D/32 consecutive elements of the output
+        // lane: D/32 consecutive elements of the output.  The (m, l) pairs
+        // of the first 32 chunks (one per lane) and the partial outputs of
+        // the first MGRP chunks do not depend on one another, so they are
+        // loaded together: one L2 round trip for a stream of up to MGRP
+        // chunks, one more per further MGRP.  The outputs are added in chunk
+        // order (deterministic).
         constexpr int EPL = D / 32;
         const long long pstride = static_cast<long long>(H) * 2;  // between one chunk's (m, l) and the next's
         const float* pmb = part_ml + (static_cast<long long>(b) * max_parts * H + h) * 2;
         const float* pob = part_o + (static_cast<long long>(b) * max_parts * H + h) * D + lane * EPL;
-        float M = -INFINITY;
-        for (int cc = c_lo + lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(pmb + cc * pstride));
+        const int n = nch - c_lo;
+        float pre[MGRP][EPL];
+        auto load_group = [&](int g0) {
+#pragma unroll
+            for (int i = 0; i < MGRP; ++i) {
+                if (g0 + i < n) {
+                    const float* po = pob + static_cast<long long>(c_lo + g0 + i) * H * D;
+                    if constexpr (EPL == 4) {
+                        const float4 a = __ldcg(reinterpret_cast<const float4*>(po));
+                        pre[i][0] = a.x, pre[i][1] = a.y, pre[i][2] = a.z, pre[i][3] = a.w;
+                    } else {
+                        const float2 a = __ldcg(reinterpret_cast<const float2*>(po));
+                        pre[i][0] = a.x, pre[i][1] = a.y;
+                    }
+                }
+            }
+        };
+        float2 mlv = make_float2(-INFINITY, 0.f);
+        if (lane < n) mlv = __ldcg(reinterpret_cast<const float2*>(pmb + (c_lo + lane) * pstride));
+        load_group(0);
+        float M = mlv.x;
+        for (int cc = c_lo + 32 + lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(pmb + cc * pstride));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float Ls = 0.f, o[EPL];
+        const float w_own = lane < n ? ex2(mlv.x - M) : 0.f;  // weight of chunk c_lo + lane
+        float Ls = lane < n ? mlv.y * w_own : 0.f;
+        for (int cc = c_lo + 32 + lane; cc < nch; cc += 32) {
+            const float2 a = __ldcg(reinterpret_cast<const float2*>(pmb + cc * pstride));
+            Ls = fmaf(a.y, ex2(a.x - M), Ls);
+        }
+        float o[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-        for (int c0 = c_lo; c0 < nch; c0 += 32) {
-            float w = 0.f;
-            if (c0 + lane < nch) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(pmb + (c0 + lane) * pstride));
-                w = ex2(ml.x - M);
-                Ls = fmaf(ml.y, w, Ls);
-            }
-            const int n = min(32, nch - c0);
-            // chunk order, as the partials were written; the loads do not
-            // depend on one another, so they overlap
-#pragma unroll 8
-            for (int i = 0; i < n; ++i) {
-                const float wi = __shfl_sync(0xffffffffu, w, i);
-                const float* po = pob + static_cast<long long>(c0 + i) * H * D;
-                if constexpr (EPL == 4) {
-                    const float4 a = __ldcg(reinterpret_cast<const float4*>(po));
-                    o[0] = fmaf(a.x, wi, o[0]);
-                    o[1] = fmaf(a.y, wi, o[1]);
-                    o[2] = fmaf(a.z, wi, o[2]);
-                    o[3] = fmaf(a.w, wi, o[3]);
+        for (int g0 = 0; g0 < n; g0 += MGRP) {
+            if (g0 > 0) load_group(g0);
+#pragma unroll
+            for (int i = 0; i < MGRP; ++i) {
+                const int ci = g0 + i;
+                if (ci >= n) break;  // uniform over the warp
+                float wi;
+                if (ci < 32) {
+                    wi = __shfl_sync(0xffffffffu, w_own, ci);
                 } else {
-                    const float2 a = __ldcg(reinterpret_cast<const float2*>(po));
-                    o[0] = fmaf(a.x, wi, o[0]);
-                    o[1] = fmaf(a.y, wi, o[1]);
+                    const float2 a = __ldcg(reinterpret_cast<const float2*>(pmb + (c_lo + ci) * pstride));
+                    wi = ex2(a.x - M);
                 }
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[e] = fmaf(pre[i][e], wi, o[e]);
             }
         }
 #pragma unroll
@@ -192,14 +246,17 @@ __device__ __forceinline__ void merge_chunks(int b, int c_lo, int nch, int H, in
 }
 
 // Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
-// counters [B] u32 (zero between calls).
+// counters [B] u32 (zero between calls).  Grid (ceil(Tcap / ch), B, groups):
+// ch slots per chunk (a multiple of 2 BATCH, at least PART_SLOTS), hpg
+// query heads per head group (a multiple of G; the last group may be
+// smaller, none is empty), at most MAX_WARPS warps.
 template <int D>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* kcache, __nv_bfloat16* vcache,
     const int* __restrict__ lens, __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
     float* __restrict__ part_ml, unsigned int* __restrict__ counters, int B, int H, int Tcap, int max_parts, float eps,
-    const __grid_constant__ Theta theta, float scale_log2, int W, int G) {
+    const __grid_constant__ Theta theta, float scale_log2, int W, int G, int ch, int hpg) {
     using Ln = Lanes<D>;
     constexpr int LPS = Ln::LPS, SPW = Ln::SPW, NLD = Ln::NLD;
     __shared__ float2 s_cs[D / 2];  // rotation at the new token's position
@@ -210,16 +267,17 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         if (c == 0 && threadIdx.x == 0) flag_error(2, 0x501);
         return;
     }
-    const int nch = (L + CH - 1) / CH;
+    const int nch = (L + ch - 1) / ch;
     const int s_vis = max(0, L - W);  // first visible slot (W >= 2^30: slot 0)
-    const int c_lo = s_vis / CH;      // first chunk holding a visible slot
+    const int c_lo = s_vis / ch;      // first chunk holding a visible slot
     if (c >= nch || c < c_lo) return;  // uniform over the CTA
     const int n_parts = nch - c_lo;    // chunks that produce a partial
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NW = static_cast<int>(blockDim.x >> 5);
+    const int h_lo = static_cast<int>(blockIdx.z) * hpg, h_hi = min(H, h_lo + hpg);  // this CTA's heads
     const int p_new = L - 1;
     const bool own_new = (k_new != nullptr) && (c == nch - 1);
-    const int s0 = max(c * CH, s_vis), s1 = min(L, c * CH + CH);
+    const int s0 = max(c * ch, s_vis), s1 = min(L, c * ch + ch);
     const int g = lane / LPS;    // slot of this lane group within a warp load
     const int sub = lane % LPS;  // 16-byte piece of the row
     const int e0 = sub * 8;      // first head-dim element of this lane
@@ -279,7 +337,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     // else: its loads do not depend on qhat.  (When k_new is given, the
     // chunk that holds the new slot waits for the slot's store below.)
     uint4 ka[NLD], va[NLD], kb[NLD], vb[NLD];
-    if (!own_new && warp < H) load_batch(head_base(warp), s0, ka, va);
+    if (!own_new && h_lo + warp < h_hi) load_batch(head_base(h_lo + warp), s0, ka, va);
     for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
     __syncthreads();
     // RoPE(RMSNorm(k_new)) (bf16) and v_new into slot p, key/value head hk
@@ -295,11 +353,12 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         }
     };
     if (own_new && G > 1) {  // uniform over the CTA
-        for (int hk = warp; hk < Hkv; hk += NW) store_new(hk);
+        // the group's key/value heads (no other group reads them)
+        for (int hk = h_lo / G + warp; hk < h_hi / G; hk += NW) store_new(hk);
         __syncthreads();  // every head of the slot is stored before any warp reads it
     }
 
-    for (int h = warp; h < H; h += NW) {
+    for (int h = h_lo + warp; h < h_hi; h += NW) {
         const long long row_bh = (static_cast<long long>(b) * H + h) * D;
         float qv[8];
         norm_rope8(q + row_bh, qv);
@@ -310,7 +369,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             store_new(h);
             __syncwarp();  // orders the slot's stores before the warp's loads below
         }
-        if (own_new || h != warp) load_batch(base, s0, ka, va);
+        if (own_new || h != h_lo + warp) load_batch(base, s0, ka, va);
         float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -391,7 +450,8 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
         }
     }
     if (n_parts == 1) return;  // uniform
-    merge_chunks<D>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts, &s_last);
+    merge_chunks<D, 16>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts * static_cast<int>(gridDim.z),
+                    &s_last);
 }
 
 // Partials: o [B][max_parts][H][D] fp32, ml [B][max_parts][H][2] fp32,
@@ -626,7 +686,8 @@ __global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
         }
     }
     if (n_parts == 1) return;  // uniform
-    merge_chunks<D>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts, &s_last);
+    // (8 partial outputs at a time: the ring kernel runs at 96 registers)
+    merge_chunks<D, 8>(b, c_lo, nch, H, max_parts, part_o, part_ml, out, counters, n_parts, &s_last);
 }
 
 }  // namespace dec

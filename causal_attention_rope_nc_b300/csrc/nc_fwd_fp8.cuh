@@ -55,11 +55,17 @@ enum Bar {
     V_EMPTY = 7,   // +stage (2)
     S_FULL = 9,    // +tile
     S_READ = 11,   // +tile: the softmax warps hold S_t in registers
-    P_FULL = 13,   // +tile: P8 of the tile's current key tile in its smem buffer
-    O_FULL = 15,   // +tile
-    MMA_DONE = 17,
-    NUM_BARS = 18
+    P_FULL = 13,   // +2 tile + buffer: P8 of a key tile in that smem buffer
+    O_FULL = 17,   // +tile
+    MMA_DONE = 19,
+    NUM_BARS = 20
 };
+// One P_FULL barrier per (tile, buffer), not per tile: the softmax warps may
+// finish P8 of step j + 1 before the MMA thread has waited for P8 of step j
+// (S of step j + 1 is issued before the PV product of step j), and a single
+// barrier would then complete two phases under one parity wait.  P8 of step
+// j + 2 (the next arrival on the same buffer's barrier) needs S of step
+// j + 2, which the MMA thread issues only after it has consumed step j.
 
 struct Smem {
     static constexpr int TILE = 128 * 128;      // one 128 x 128 E4M3 tile (16 KB)
@@ -147,7 +153,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(V_EMPTY + s), 1);
             mbar_init(bar(S_FULL + s), 1);
             mbar_init(bar(S_READ + s), 4);  // one arrival per softmax warp of the tile
-            mbar_init(bar(P_FULL + s), 4);
+            mbar_init(bar(P_FULL + 2 * s), 4);
+            mbar_init(bar(P_FULL + 2 * s + 1), 4);
             mbar_init(bar(O_FULL + s), 1);
         }
         mbar_init(bar(MMA_DONE), 1);
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // PV of stream step j for tile t (second pass)
             auto issue_pv = [&](int t, int j) -> bool {
                 const int vs = j & 1;
-                if (!mbar_wait(bar(P_FULL + t), np[t] & 1, 0x711)) return false;
+                if (!mbar_wait(bar(P_FULL + 2 * t + (np[t] & 1)), (np[t] >> 1) & 1, 0x711)) return false;
                 tc_fence_after();
                 const uint32_t p_s = sb + S::OFF_P + (2 * t + (np[t] & 1)) * S::TILE;
 #pragma unroll
@@ -295,31 +302,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int kt = lo_t + jt;
                 const int d0 = q_idx - kt * BN;  // query - key at column 0
                 const bool full = kt * BN + BN - 1 <= qt * BM && qt * BM + BM - 1 - kt * BN < W;
+                // column e visible: 0 <= query - key < W (only the diagonal and
+                // band-edge tiles test it: the loops below come in a masked and
+                // an unmasked copy)
+                auto vis = [&](int e) { return d0 - e >= 0 && d0 - e < W; };
                 if (pass == 0) {
+                    // eight independent maxima, so the reduction is not one
+                    // 128-long dependency chain
+                    float mm[8];
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) {
-                        const int dd = d0 - e;
-                        if (full || (dd >= 0 && dd < W)) m = fmaxf(m, __uint_as_float(r[e]));
-                    }
+                    for (int i = 0; i < 8; ++i) mm[i] = -INFINITY;
+                    auto max_tile = [&](auto masked) {
+#pragma unroll
+                        for (int e = 0; e < 128; ++e) {
+                            const float x = __uint_as_float(r[e]);
+                            if (!decltype(masked)::value || vis(e)) mm[e & 7] = fmaxf(mm[e & 7], x);
+                        }
+                    };
+                    if (full)
+                        max_tile(std::false_type{});
+                    else
+                        max_tile(std::true_type{});
+                    m = fmaxf(m, fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                                       fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))));
                     continue;
                 }
-                // second pass: P8 = E4M3(exp2((s - m) c_log2 + 8)) into buffer jt % 2
+                // second pass: P8 = E4M3(exp2((s - m) c_log2 + 8)) into buffer jt % 2;
+                // the sums of p and of P8 in four independent partials each
                 const float off = 8.f - m * c_log2;
                 uint32_t pw[32];
+                float lx[4] = {0.f, 0.f, 0.f, 0.f}, lq[4] = {0.f, 0.f, 0.f, 0.f};
+                auto p_tile = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 128; e += 4) {
-                    float p[4];
+                    for (int e = 0; e < 128; e += 4) {
+                        float p[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int dd = d0 - (e + i);
-                        p[i] = (full || (dd >= 0 && dd < W)) ? ex2(fmaf(__uint_as_float(r[e + i]), c_log2, off)) : 0.f;
-                        l_x += p[i];
+                        for (int i = 0; i < 4; ++i) {
+                            p[i] = ex2(fmaf(__uint_as_float(r[e + i]), c_log2, off));
+                            if (decltype(masked)::value && !vis(e + i)) p[i] = 0.f;
+                        }
+                        const int a = (e >> 2) & 3;
+                        lx[a] += (p[0] + p[1]) + (p[2] + p[3]);
+                        const uint32_t lo2 = e4m3x2(p[0], p[1]), hi2 = e4m3x2(p[2], p[3]);
+                        const float2 va = e4m3x2_value(lo2), vb = e4m3x2_value(hi2);
+                        lq[a] += (va.x + va.y) + (vb.x + vb.y);
+                        pw[e / 4] = lo2 | (hi2 << 16);
                     }
-                    const uint32_t lo2 = e4m3x2(p[0], p[1]), hi2 = e4m3x2(p[2], p[3]);
-                    const float2 a = e4m3x2_value(lo2), bq = e4m3x2_value(hi2);
-                    l_q += (a.x + a.y) + (bq.x + bq.y);
-                    pw[e / 4] = lo2 | (hi2 << 16);
-                }
+                };
+                if (full)
+                    p_tile(std::false_type{});
+                else
+                    p_tile(std::true_type{});
+                l_x += (lx[0] + lx[1]) + (lx[2] + lx[3]);
+                l_q += (lq[0] + lq[1]) + (lq[2] + lq[3]);
                 uint8_t* pb = smem + S::OFF_P + (2 * t + (jt & 1)) * S::TILE;
                 // buffer jt % 2 was last read by the PV product of step jt - 2,
                 // which the MMA thread issued before the S product of step jt
@@ -329,7 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     *reinterpret_cast<uint4*>(pb + sw128_offset(row, c)) =
                         make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
                 fence_proxy_async_smem();
-                mbar_arrive_warp(bar(P_FULL + t));
+                mbar_arrive_warp(bar(P_FULL + 2 * t + (jt & 1)));
             }
         }
         // ---- epilogue: O / (l_q 2^tau) through the tile's P buffers (free:

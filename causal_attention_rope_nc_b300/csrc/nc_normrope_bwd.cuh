@@ -24,7 +24,9 @@ namespace nc {
 // named barrier `bar_id` over `nthreads` threads, which every participating
 // thread reaches exactly once whether or not it is `active`.  The bf16 dx
 // goes into `stage` (layout of tile16_off).
-template <int D>
+// With GTAB the table is read from global memory (L2) instead: ct0 is then
+// the row's own D floats of the [T][D/2] (cos, sin) table and ct1 is unused.
+template <int D, bool GTAB = false>
 __device__ __forceinline__ void norm_rope_bwd_stage(bool active, uint32_t tm, float out_scale, const uint8_t* xt,
                                                     const uint8_t* ct0, const uint8_t* ct1, int row, int half,
                                                     float eps, float2* xch, uint8_t* stage, int bar_id,
@@ -32,6 +34,7 @@ __device__ __forceinline__ void norm_rope_bwd_stage(bool active, uint32_t tm, fl
     constexpr int HALF = D / 2, NF = D / 4;
     const int f0 = half * NF;
     const uint8_t* ct = half ? ct1 : ct0;  // this half's table floats [2 f0, 2 f0 + 2 NF)
+    const float* gt = reinterpret_cast<const float*>(ct0) + 2 * f0;
     uint32_t u[2][NF];                     // g, then u, for the lo and hi columns
     float ss = 0.f, dot = 0.f;
     if (active) {
@@ -48,7 +51,8 @@ __device__ __forceinline__ void norm_rope_bwd_stage(bool active, uint32_t tm, fl
             for (int i = 0; i < 4; ++i) {
                 const int f = 16 * ch + 4 * i;  // table float index relative to this half
                 const float4 cs =
-                    *reinterpret_cast<const float4*>(ct + (f >> 5) * (128 * 128) + sw128_offset(row, (f & 31) >> 2));
+                    GTAB ? __ldg(reinterpret_cast<const float4*>(gt + f))
+                         : *reinterpret_cast<const float4*>(ct + (f >> 5) * (128 * 128) + sw128_offset(row, (f & 31) >> 2));
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int e = ch * 8 + 2 * i + k;

@@ -78,8 +78,9 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // token's rotation row from the table once and walks the token's H heads,
 // HC heads at a time with every load of a chunk issued before any math, so
 // each lane keeps HC 16-byte loads in flight.  Tokens are enumerated q
-// tokens first, then k tokens.
-constexpr int NORM_HC = 8;
+// tokens first, then k tokens.  (d20, 671 MB: 135 us with HC = 4, 140 us
+// with 8, 196 us with 16: more loads in flight per lane cost occupancy.)
+constexpr int NORM_HC = 4;
 
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
@@ -414,46 +415,56 @@ __device__ __forceinline__ int v_scale_exp(float mxf) {
 // v8t[bg][d][t] = E4M3(v[b][t][g][d] 2^tau) for t < Tpad (0 past T): the
 // values transposed, keys contiguous, so that the fp8 forward's PV product
 // reads a K-major B operand.  vscale[bg] = 2^-tau.  Grid (Tpad / 128,
-// B * Hkv), 256 threads; each block transposes 128 tokens through a 16 KB
-// shared tile [D][128].
+// B * Hkv), 256 threads; each block transposes 128 tokens through a bf16
+// shared tile [128 tokens][D] whose 16-byte chunks are XOR-swizzled by bits
+// 4-6 of the token (chunk c of token t sits at chunk c ^ ((t >> 4) & 7)):
+// the row loads store whole chunks, and in the column pass the eight lanes
+// that read the same element of tokens 16 k + j (k = 0..7) hit eight
+// different chunks, so neither pass has bank conflicts.  Each column-pass
+// thread quantises 16 consecutive tokens of one d into one 16-byte store; a
+// warp stores four whole 128-byte rows.
 template <int D>
 __global__ void __launch_bounds__(256) v_quant_t_kernel(const __nv_bfloat16* __restrict__ v,
                                                         const unsigned int* __restrict__ vmax,
                                                         uint8_t* __restrict__ v8t, float* __restrict__ vscale, int T,
                                                         int Tpad, int Hkv) {
     using L = RowLanes<D>;
-    __shared__ __align__(16) uint8_t tile[D][128];
+    constexpr int ROW = D * 2;  // bytes per token row of the tile
+    __shared__ __align__(16) uint8_t tile[128 * ROW];
+    __shared__ int s_tau;
     const int sub = threadIdx.x % L::LPR;
     const int bg = blockIdx.y, b = bg / Hkv, g = bg % Hkv;
     const int t0 = blockIdx.x * 128;
-    const int tau = v_scale_exp(__uint_as_float(vmax[bg]));
-    if (blockIdx.x == 0 && threadIdx.x == 0 && NC_IN_RANGE(vscale + bg, 4, 0x40e)) vscale[bg] = ldexpf(1.f, -tau);
+    if (threadIdx.x == 0) {
+        s_tau = v_scale_exp(__uint_as_float(vmax[bg]));
+        if (blockIdx.x == 0 && NC_IN_RANGE(vscale + bg, 4, 0x40e)) vscale[bg] = ldexpf(1.f, -s_tau);
+    }
+    // row pass: token rows in, 16 bytes a lane
     for (int tl = threadIdx.x / L::LPR; tl < 128; tl += blockDim.x / L::LPR) {
         const int t = t0 + tl;
-        float x[8];
-        if (t < T) {
-            bf16x8_to_f32(
-                *reinterpret_cast<const uint4*>(v + ((static_cast<long long>(b) * T + t) * Hkv + g) * D + sub * 8), x);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const uint32_t w = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-                make_float2(ldexpf(x[e], tau), ldexpf(x[e + 1], tau)), __NV_SATFINITE, __NV_E4M3));
-            tile[sub * 8 + e][tl] = static_cast<uint8_t>(w & 0xffu);
-            tile[sub * 8 + e + 1][tl] = static_cast<uint8_t>(w >> 8);
-        }
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (t < T) x = *reinterpret_cast<const uint4*>(v + ((static_cast<long long>(b) * T + t) * Hkv + g) * D + sub * 8);
+        *reinterpret_cast<uint4*>(tile + tl * ROW + ((sub ^ ((tl >> 4) & 7)) << 4)) = x;
     }
     __syncthreads();
-    // D rows of 128 bytes, 16 bytes per thread per step
+    const float sc = __int_as_float((s_tau + 127) << 23);  // 2^tau, tau in [-126, 126]
+    // column pass: item = (d, k): tokens 16 k .. 16 k + 15 of element d
     uint8_t* dst = v8t + static_cast<long long>(bg) * D * Tpad + t0;
-    for (int c = threadIdx.x; c < D * 8; c += blockDim.x) {
-        const int d = c >> 3, k = c & 7;
-        if (NC_IN_RANGE(dst + static_cast<long long>(d) * Tpad + 16 * k, 16, 0x40f))
-            *reinterpret_cast<uint4*>(dst + static_cast<long long>(d) * Tpad + 16 * k) =
-                *reinterpret_cast<const uint4*>(&tile[d][16 * k]);
+    for (int it = threadIdx.x; it < D * 8; it += blockDim.x) {
+        const int k = it & 7, d = it >> 3;
+        const int cpos = ((d >> 3) ^ k) << 4, w = (d & 7) * 2;
+        uint32_t word[4];
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            float x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                x[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + (16 * k + j + i) * ROW + cpos + w)) * sc;
+            word[j / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3)) |
+                          (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x[2], x[3]), __NV_SATFINITE, __NV_E4M3)) << 16);
+        }
+        uint8_t* p = dst + static_cast<long long>(d) * Tpad + 16 * k;
+        if (NC_IN_RANGE(p, 16, 0x40f)) *reinterpret_cast<uint4*>(p) = make_uint4(word[0], word[1], word[2], word[3]);
     }
 }
 
