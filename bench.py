@@ -308,7 +308,11 @@ def bench_ours(args, ws_n, rank, local):
 # from one ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum, summarised under profiles/ with its command).
 # Must go back to None whenever that kernel's code changes.
-DRAM_TRAFFIC = {"attn_bwd_dkdv": 853.19e6 + 311.68e6}
+DRAM_TRAFFIC = {"attn_bwd_dkdv": 870.32e6 + 1.71e9, "attn_bwd_dq": 1.78e9 + 159.49e6,
+                "attn_fwd": 507.92e6 + 148.25e6}
+# The same for the decode kernels at the d20 decode workload (plain multi-head
+# attention, and 2 key/value heads).
+DECODE_TRAFFIC = {"mha": 176.36e6 + 0.38e6, "gqa2": 35.88e6 + 0.0}
 
 
 def band_pairs(T, W):
@@ -566,7 +570,9 @@ def bench_decode(nc, dev, args, rank, window=0, kv_heads=None):
     return {"workload": name,
             "bytes": byt, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": None if window else DECODE_TRAFFIC.get("gqa2" if kv_heads == 2 else
+                                                                       "mha" if not kv_heads else None),
                          "frac_of_spec": round(gbs / SPEC["hbm_gbs"], 4)},
             "l2": "256 MB buffer written, then read, between calls", "tokens_per_s": round(w.B / (ms * 1e-3), 1)}
 
