@@ -25,9 +25,12 @@
 // below (z + 1) HPG.  For one head it walks the chunk's slots BATCH
 // at a time: a group of D/8 lanes reads one slot's key row and value
 // row (bf16) as 16-byte pieces, 32/(D/8) slots per warp load (streaming
-// loads, evict-first).  The batches are software-pipelined over two
-// register buffers: every load of batch n+1 is issued before the arithmetic
-// of batch n, so the rows come straight from HBM into registers.
+// loads, evict-first).  The batches are software-pipelined over three
+// register buffers: every load of batches n+1 and n+2 is issued before the
+// arithmetic of batch n, so the rows come straight from HBM into registers
+// with two batches in flight per warp (measured on the d20 decode: 47.1 us
+// against 49.2 us with two buffers, 28.7 against 30.7 us with a 512-slot
+// window).
 //
 // attn_decode_tma_kernel (grouped-query attention, G > 1): one producer
 // warp streams the chunk through a ring of NST shared-memory stages with
@@ -76,7 +79,7 @@ namespace dec {
 
 constexpr int CH = 128;          // cache slots per CTA of the ring kernel (one partial result)
 constexpr int PART_SLOTS = 32;   // the workspace holds ceil(Tcap / PART_SLOTS) >= ceil(Tcap / chunk) partials
-constexpr int MAX_WARPS = 16;    // warps per CTA of the register kernel (heads beyond this many loop)
+constexpr int MAX_WARPS = 10;    // warps per CTA of the register kernel (heads beyond this many loop)
 constexpr int MAX_CWARPS = 16;   // compute warps per CTA of the ring kernel
 constexpr int BATCH = 8;         // slots per online-softmax step
 constexpr int MAX_SB = 64;       // slots per stage, at most
@@ -104,8 +107,9 @@ inline size_t smem_bytes(int Hkv, int D, int sb, int nst) {
 // of at most REG_WARPS warps, and REG_CH slots per chunk.  (Measured on the
 // d20 decode: groups of 5 warps, three CTAs per SM, and 64-slot chunks both
 // ran within one event tick (2 us) of one 10-warp CTA per 128-slot chunk,
-// or slower with a 512-slot window; so heads are split only past 16.)
-constexpr int REG_WARPS = 16;
+// or slower with a 512-slot window; so heads are split only past 10, the
+// most warps whose registers fit one SM with three buffers per warp.)
+constexpr int REG_WARPS = MAX_WARPS;
 constexpr int REG_CH = 128;
 struct RegSplit {
     int hpg;     // query heads per group (a multiple of G)
@@ -336,8 +340,11 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
     // The first batch of this warp's first head goes out before anything
     // else: its loads do not depend on qhat.  (When k_new is given, the
     // chunk that holds the new slot waits for the slot's store below.)
-    uint4 ka[NLD], va[NLD], kb[NLD], vb[NLD];
-    if (!own_new && h_lo + warp < h_hi) load_batch(head_base(h_lo + warp), s0, ka, va);
+    uint4 ka[NLD], va[NLD], kb[NLD], vb[NLD], kc[NLD], vc[NLD];
+    if (!own_new && h_lo + warp < h_hi) {
+        load_batch(head_base(h_lo + warp), s0, ka, va);
+        if (s0 + BATCH < s1) load_batch(head_base(h_lo + warp), s0 + BATCH, kb, vb);
+    }
     for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_cs[i] = rope_cos_sin(p_new, theta.t[i]);
     __syncthreads();
     // RoPE(RMSNorm(k_new)) (bf16) and v_new into slot p, key/value head hk
@@ -369,7 +376,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
             store_new(h);
             __syncwarp();  // orders the slot's stores before the warp's loads below
         }
-        if (own_new || h != h_lo + warp) load_batch(base, s0, ka, va);
+        if (own_new || h != h_lo + warp) {
+            load_batch(base, s0, ka, va);
+            if (s0 + BATCH < s1) load_batch(base, s0 + BATCH, kb, vb);
+        }
         float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -413,14 +423,17 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
                 for (int e = 0; e < 8; ++e) acc[e] = fmaf(pe, vf[e], acc[e]);
             }
         };
-        // software pipeline over two register buffers: the loads of the next
-        // batch are in flight while the current one is reduced
-        for (int j = s0; j < s1; j += 2 * BATCH) {
-            if (j + BATCH < s1) load_batch(base, j + BATCH, kb, vb);
+        // software pipeline over three register buffers: the loads of the
+        // next two batches are in flight while the current one is reduced
+        for (int j = s0; j < s1; j += 3 * BATCH) {
+            if (j + 2 * BATCH < s1) load_batch(base, j + 2 * BATCH, kc, vc);
             math_batch(j, ka, va);
             if (j + BATCH >= s1) break;
-            if (j + 2 * BATCH < s1) load_batch(base, j + 2 * BATCH, ka, va);
+            if (j + 3 * BATCH < s1) load_batch(base, j + 3 * BATCH, ka, va);
             math_batch(j + BATCH, kb, vb);
+            if (j + 2 * BATCH >= s1) break;
+            if (j + 4 * BATCH < s1) load_batch(base, j + 4 * BATCH, kb, vb);
+            math_batch(j + 2 * BATCH, kc, vc);
         }
         // add the lane groups' parts (same m)
 #pragma unroll
