@@ -207,22 +207,6 @@ int make_tmap(CUtensorMap* tm, const void* ptr, int B, int T, int H, int D, int 
     return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
 }
 
-// The backward's dS^T scratch (fp16) as rows of 64 values: each block is
-// two [128 keys][64 queries] halves (bwdq::ds_offset); boxes of 64 values x
-// 64 rows (64 keys of one half), 128-byte swizzled.
-int make_ds_tmap(CUtensorMap* tm, const void* ds, long long rows) {
-    const long long rows64 = 2 * rows;  // rows of 64 values
-    if (rows <= 0 || rows64 >= (1LL << 31)) return NC_EINVAL;  // TMA row coordinates are int32
-    const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows64)};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {64, nc::bwdq::KS};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode_fn()(tm, kF16, 2, const_cast<void*>(ds), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? NC_OK : NC_EINVAL;
-}
-
 // The RoPE table [T][D/2] (cos, sin) viewed as an fp32 [T][D] tensor: boxes
 // of 32 values x 128 rows, 128-byte swizzled.  Rows past T read as zero.
 int make_tab_tmap(CUtensorMap* tm, const float2* tab, int T, int D) {
@@ -246,8 +230,8 @@ bool params_ok(float eps, float base) { return std::isfinite(eps) && eps >= 0.f 
 size_t tab_bytes(int T, int D) { return up256(static_cast<size_t>(T) * (D / 2) * sizeof(float2)); }
 int tpad_of(int T) { return ((T + 127) / 128) * 128; }  // query blocks of 128
 
-// Rows of 128 bf16 in the backward's dS^T scratch: one [128][128] block per
-// (query tile, key tile <= query tile) of every (batch, query head).
+// Rows of 128 fp16 values in the backward's dS scratch: one 128 x 128 block
+// per (query tile, key tile <= query tile) of every (batch, query head).
 long long ds_rows(int B, int T, int H) {
     const long long n_t = (T + 127) / 128;
     return static_cast<long long>(B) * H * (n_t * (n_t + 1) / 2) * 128;
@@ -427,13 +411,13 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
             reinterpret_cast<const __nv_bfloat16*>(v), lse, delta, lse2, gmax, B, T, H, Hkv, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tds, tk64;
+    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tk64;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, Hkv, D, 128, kF16) ||
         make_tmap(&tv, v, B, T, Hkv, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
         make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, Hkv, D, 128) ||
         make_tab_tmap(&ttab, tab, T, D) || make_tmap(&tdq, dq, B, T, H, D, 128) ||
         make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128) ||
-        make_ds_tmap(&tds, ds, ds_rows(B, T, H)) || make_tmap(&tk64, khat, B, T, Hkv, D, nc::bwdq::KS, kF16))
+        make_tmap(&tk64, khat, B, T, Hkv, D, nc::bwdq::KS, kF16))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -461,7 +445,8 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
         const int grid = static_cast<int>(n_tiles < g_sm_count[dev] ? n_tiles : g_sm_count[dev]);
         ProfScope ps("attn_bwd_dq", s);
         nc::bwdq::attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid), nc::bwdq::NUM_THREADS,
-                                          nc::bwdq::Smem<D>::ALLOC, s>>>(tds, tk64, tqr, tab, tdq, gmax, gmax + 2, T,
+                                          nc::bwdq::Smem<D>::ALLOC, s>>>(reinterpret_cast<const __half*>(ds), tk64, tqr, tab, tdq,
+                                                                         gmax, gmax + 2, T,
                                                                          H, B, group, float(scale), eps, W, G);
     }
     return launch_status();
@@ -859,7 +844,7 @@ int nc_attn_bwd_ex(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const i
     for (const void* p : b16)
         if (!aligned16(p)) return NC_EINVAL;
     if (!aligned256(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return NC_EINVAL;
-    if (2 * ds_rows(B, T, H) >= (1LL << 31)) return NC_EINVAL;  // the dS^T scratch's TMA row coordinates
+    if (2 * ds_rows(B, T, H) >= (1LL << 31)) return NC_EINVAL;  // 2^24 dS blocks: the limit the header states
     if (workspace_bytes < nc_attn_workspace_size(NC_OP_BWD, B, T, H, D)) return NC_EINVAL;
     int rc = device_ready();
     if (rc) return rc;

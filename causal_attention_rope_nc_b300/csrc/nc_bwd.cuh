@@ -341,8 +341,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
                             float p[4];
 #pragma unroll
+                            for (int i = 0; i < 4; i += 2) {
+                                const float2 x2 = ffma2(make_float2(__uint_as_float(r[c][e4 * 4 + i]),
+                                                                    __uint_as_float(r[c][e4 * 4 + i + 1])),
+                                                        make_float2(scale_log2, scale_log2),
+                                                        make_float2(-lv[i], -lv[i + 1]));
+                                p[i] = ex2(x2.x);
+                                p[i + 1] = ex2(x2.y);
+                            }
+#pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                p[i] = ex2(fmaf(__uint_as_float(r[c][e4 * 4 + i]), scale_log2, -lv[i]));
                                 if constexpr (decltype(masked)::value) {
                                     const int dd = d0 + c * 32 + e4 * 4 + i;  // visible: 0 <= dd < W
                                     if (dd < 0 || dd >= W) p[i] = 0.f;
@@ -382,10 +390,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
                         float ds[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < 4; i += 2) {
+                            // alpha p (dP - delta), two columns per paired instruction
                             const uint32_t pw = pk[c * 16 + e4 * 2 + (i >> 1)];
-                            const float p = __uint_as_float((i & 1) ? (pw & 0xffff0000u) : (pw << 16));
-                            ds[i] = alpha * p * (__uint_as_float(r[c][e4 * 4 + i]) - dv4[i]);
+                            const float2 p2 = make_float2(__uint_as_float(pw << 16), __uint_as_float(pw & 0xffff0000u));
+                            const float2 t2 = ffma2(make_float2(1.f, 1.f),
+                                                    make_float2(__uint_as_float(r[c][e4 * 4 + i]),
+                                                                __uint_as_float(r[c][e4 * 4 + i + 1])),
+                                                    make_float2(-dv4[i], -dv4[i + 1]));
+                            const float2 d2 = fmul2(fmul2(make_float2(alpha, alpha), p2), t2);
+                            ds[i] = d2.x;
+                            ds[i + 1] = d2.y;
                         }
                         w[c * 16 + e4 * 2] = pack_f16x2(ds[0], ds[1]);
                         w[c * 16 + e4 * 2 + 1] = pack_f16x2(ds[2], ds[3]);
@@ -394,24 +409,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_st16(tdp + cbase, w);
                 tmem_st16(tdp + cbase + 16, w + 16);
                 // the same fp16 alpha dS^T row half into the scratch block
-                // (query tile qb, key tile kt) of query head h.  Transposed in
-                // 16-byte chunks across each 4-lane group first, so that each
-                // warp store writes 64 contiguous bytes of each of 8 rows
-                // instead of 16 bytes of 32 rows.  (A full 8 x 8 transpose,
-                // whole 128-byte rows per store, measured slower: its extra
-                // shuffle stage costs more than the half-line stores save.)
-                uint4 ch[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) ch[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-                transpose4_chunks(ch);
+                // (query tile qb, key tile kt) of query head h: 8 chunks of 8
+                // queries, each a 16-byte store; in the scratch layout
+                // (bwdq::ds_offset) the 32 key rows of the warp are 32
+                // consecutive 16-byte slots, so every warp store writes 512
+                // contiguous bytes.  (The earlier [key][query] layout needed a
+                // 4-lane shuffle transpose of the chunks to coalesce.)
                 const int h = hk * G + it / n_it;
                 __half* blk = ds_out + bwdq::ds_block(static_cast<long long>(b) * H + h, nqb, qb, kt) * (BN * BM);
-                const int key0 = quarter * 32 + 4 * (lane >> 2);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    // lane 4j + c now holds (row 4j + (k & 3), chunk c + 4 (k >> 2)) in ch[k]
-                    __half* p = blk + bwdq::ds_offset(key0 + (k & 3), cbase + 8 * ((lane & 3) + 4 * (k >> 2)));
-                    if (NC_IN_RANGE(p, 16, 0x412)) *reinterpret_cast<uint4*>(p) = ch[k];
+                for (int g = 0; g < 8; ++g) {
+                    __half* p = blk + bwdq::ds_offset(row, cbase + 8 * g);
+                    if (NC_IN_RANGE(p, 16, 0x412))
+                        *reinterpret_cast<uint4*>(p) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
                 }
             }
             tmem_wait_st();

@@ -4,11 +4,13 @@
 //
 // The key-side kernel (nc_bwd.cuh) forms every visible block of
 //   dS = P o (dP - delta)
-// anyway (for dK), and writes it once, transposed (keys on rows), to a
-// scratch buffer in HBM: the dS^T block of (query tile i, key tile j) of one
-// (batch, query head) is a [128 keys][128 queries] fp16 tile holding
-// alpha * dS (alpha: the call's one power-of-two scale, ds_scale_global,
-// undone in the epilogue).  This kernel is then a streaming GEMM per query
+// anyway (for dK), and writes it once to a scratch buffer in HBM: the block
+// of (query tile i, key tile j) of one (batch, query head) is 128 keys x 128
+// queries of alpha * dS in fp16 (alpha: the call's one power-of-two scale,
+// ds_scale_global, undone in the epilogue), laid out (ds_offset) so that
+// the key side's stores coalesce without a transpose and each 64-key half
+// is one contiguous 16 KB piece in the tensor core's no-swizzle operand
+// layout.  This kernel is then a streaming GEMM per query
 // tile,
 //   dQhat_i = sum_j dS_ij khat_j          (M=128 queries, N=D, K=64 keys per stage),
 // that reads each dS block once (32 KB per 128 x D x 128 product: it is HBM
@@ -17,19 +19,28 @@
 //
 // Persistent: one CTA per SM takes query tiles until none are left, so that a
 // tile's epilogue overlaps the next tile's loads and products:
-//   warp 8      TMA producer: (dS^T half-block, khat half-tile) pairs of 64
-//               keys into an NST-stage ring, tile after tile
+//   warp 8      producer of the dS stream: one 16 KB bulk copy per half-block
+//               of 64 keys into an NSD-stage ring, tile after tile (it also
+//               takes the tiles from the global counter)
+//   warp 11     TMA producer of the khat stream: the matching 64 khat rows
+//               into an NSK-stage ring
 //   warp 10     TMA producer of the epilogue tile: the tile's raw q rows,
 //               once the previous tile's epilogue is done
-//   warp 9      MMA issuer (one thread): A = alpha dS (the MN-major view of
-//               the dS^T stage), B = khat (MN-major), both fp16; the fp32
+//   warp 9      MMA issuer (one thread): A = alpha dS (MN-major, no swizzle:
+//               the stage as it came from HBM), B = khat (MN-major,
+//               128-byte swizzled by TMA), both fp16; the fp32
 //               accumulator alternates between two TMEM buffers
 //   warps 0-7   epilogue: two threads per query row apply RoPE^T and the
 //               RMSNorm backward to dQhat, overwrite the raw q rows with dq
 //               (each thread only the columns it read) and store them by TMA;
 //               the RoPE table rows come from L2 (the table is T x D floats),
-//               which leaves the shared memory to the ring: six stages of 32 KB
-//               in flight per SM keep the dS stream near the HBM rate
+//               which leaves the shared memory to the rings.
+// The dS blocks come from HBM, the khat rows mostly from L2 (a (b, h)'s
+// tiles share them), so the two streams have rings of their own: nine 16 KB
+// dS stages keep 144 KB of the HBM stream in flight per SM, three khat
+// stages cover the shorter L2 latency.  (One ring of six 32 KB (dS, khat)
+// pairs, 96 KB of dS in flight, measured the same 393 us at d20: the bytes
+// in flight are not what holds the stream at 4.5 TB/s.)
 // Tile order: the grouped order of the other kernels ((batch, head) pairs
 // in groups of about one wave, the longest walks first inside a group, so
 // that a group's khat tiles stay in L2), handed out dynamically: the ring
@@ -51,18 +62,22 @@ namespace bwdq {
 constexpr int BM = 128;    // queries per tile
 constexpr int BN = 128;    // keys per dS block
 constexpr int KS = 64;     // keys per ring stage (half a block)
-constexpr int NST = 6;     // ring stages
+constexpr int NSD = 9;     // dS ring stages
+constexpr int NSK = 3;     // khat ring stages
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int WARP_EPI_TMA = 10;
-constexpr int NUM_THREADS = 11 * 32;
+constexpr int WARP_K_TMA = 11;
+constexpr int NUM_THREADS = 12 * 32;
 
 constexpr int NQ = 4;      // tile-index queue slots
 
 enum Bar {
-    FULL = 0,                  // +stage
-    EMPTY = FULL + NST,        // +stage
-    DQ_FULL = EMPTY + NST,     // +buffer: the tile's dQhat is in TMEM
+    FULL = 0,                  // +dS stage
+    EMPTY = FULL + NSD,        // +dS stage
+    KFULL = EMPTY + NSD,       // +khat stage
+    KEMPTY = KFULL + NSK,      // +khat stage
+    DQ_FULL = KEMPTY + NSK,    // +buffer: the tile's dQhat is in TMEM
     DQ_EMPTY = DQ_FULL + 2,    // +buffer: the epilogue has read it
     EPI_FULL = DQ_EMPTY + 2,   // raw q tile of the tile staged
     EPI_EMPTY = EPI_FULL + 1,  // the previous tile's epilogue is done with it
@@ -71,7 +86,7 @@ enum Bar {
     TQ_EMPTY = TQ_FULL + NQ,   // +slot: every consumer has read it
     NUM_BARS = TQ_EMPTY + NQ
 };
-constexpr int TQ_READERS = 10;  // the MMA thread, the epilogue producer, 8 epilogue warps
+constexpr int TQ_READERS = 11;  // the MMA thread, the two other producers, 8 epilogue warps
 
 // Index of the dS^T block (query tile i, key tile j <= i) of one (batch,
 // query head) bh in the scratch: the causal triangle of each (b, h), in
@@ -80,20 +95,27 @@ __host__ __device__ __forceinline__ long long ds_block(long long bh, int n_t, in
     return bh * (static_cast<long long>(n_t) * (n_t + 1) / 2) + static_cast<long long>(i) * (i + 1) / 2 + j;
 }
 
-// Element offset inside one 16384-element dS^T block of dS^T[key][query]:
-// the block is two [128 keys][64 queries] row-major halves (queries
-// 64 h .. 64 h + 63), so that a 128-byte TMA box row is one key's 64 queries.
+// Element offset of (key, query) inside one 16384-element dS block:
+// [key half (2)][query chunk of 8 (16)][key within the half (64)][query
+// within the chunk (8)].  The key side's thread for one key row stores its
+// 8-query chunks as 16-byte pieces, and the 32 keys of a warp fill 512
+// contiguous bytes.  A 64-key half is 16 KB of 8-key x 8-query core
+// matrices (128 contiguous bytes, keys along rows): the no-swizzle MN-major
+// layout of the dQ product's A operand, with core matrices 128 bytes apart
+// along K (keys) and 1024 bytes apart along M (query chunks).
 __host__ __device__ __forceinline__ int ds_offset(int key, int query) {
-    return (query >> 6) * 8192 + key * 64 + (query & 63);
+    return (key >> 6) * 8192 + (query >> 3) * 512 + (key & 63) * 8 + (query & 7);
 }
+constexpr uint32_t DS_LBO = 128;   // core-matrix stride along K (keys)
+constexpr uint32_t DS_SBO = 1024;  // core-matrix stride along M (query chunks)
 
 template <int D>
 struct Smem {
     static constexpr int DSBYTES = KS * BM * 2;  // 64 keys x 128 queries of dS^T (two 8 KB query halves)
     static constexpr int KBYTES = KS * D * 2;    // 64 keys of khat (D/64 halves of 8 KB)
-    static constexpr int STAGE = DSBYTES + KBYTES;
-    static constexpr int OFF_RING = 0;
-    static constexpr int OFF_X = OFF_RING + NST * STAGE;  // raw q [128][D] bf16 (TMA box layout), then dq
+    static constexpr int OFF_RING = 0;           // NSD dS stages
+    static constexpr int OFF_KRING = OFF_RING + NSD * DSBYTES;  // NSK khat stages
+    static constexpr int OFF_X = OFF_KRING + NSK * KBYTES;  // raw q [128][D] bf16 (TMA box layout), then dq
     static constexpr int XBYTES = BM * D * 2;
     static constexpr int OFF_XCH = OFF_X + XBYTES;  // row-half exchange, 2 x 128 float2
     static constexpr int OFF_BAR = OFF_XCH + 2 * BM * 8;
@@ -123,7 +145,7 @@ __device__ __forceinline__ DqTile dq_tile(int idx, int n_qt, int nbh, int group)
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_k,
+    attn_bwd_dq_kernel(const __half* __restrict__ ds, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_qraw, const float2* __restrict__ tab,
                        const __grid_constant__ CUtensorMap tm_dq, const unsigned int* __restrict__ gmax,
                        unsigned int* __restrict__ tile_counter, int T, int H, int B, int group, float scale, float eps,
@@ -142,7 +164,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int nbh = B * H;
     const int n_tiles = n_qt * nbh;
     auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8 * i; };
-    auto stage = [&](int s) -> uint32_t { return sb + S::OFF_RING + s * S::STAGE; };
+    auto dstage = [&](int s) -> uint32_t { return sb + S::OFF_RING + s * S::DSBYTES; };
+    auto kstage = [&](int s) -> uint32_t { return sb + S::OFF_KRING + s * S::KBYTES; };
     auto kt_lo_of = [&](int qt) { return max(0, qt * BM - W + 1) / BN; };  // W >= 2^30: none cut
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TSLOT);
     volatile int* tq = reinterpret_cast<volatile int*>(smem + S::OFF_TQ);
@@ -161,9 +184,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NSD; ++s) {
             mbar_init(bar(FULL + s), 1);
             mbar_init(bar(EMPTY + s), 1);
+        }
+        for (int s = 0; s < NSK; ++s) {
+            mbar_init(bar(KFULL + s), 1);
+            mbar_init(bar(KEMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(DQ_FULL + i), 1);
@@ -188,11 +215,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tslot;
 
     if (warp == WARP_TMA) {
-        // -------------------------------------------- ring producer ----
+        // ------------------------------------------ dS ring producer ----
         if (lane == 0) {
             int x = 0;  // stages filled so far (all tiles)
-            int issued[NST];
-            for (int s = 0; s < NST; ++s) issued[s] = 0;
+            int issued[NSD];
+            for (int s = 0; s < NSD; ++s) issued[s] = 0;
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 // take the next tile and publish it to the other roles
@@ -204,31 +231,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive(bar(TQ_FULL + q));
                 if (idx < 0) break;
                 const DqTile tl = dq_tile(idx, n_qt, nbh, group);
-                const int b = tl.bh / H, hk = (tl.bh % H) / G;
                 const int kt_lo = kt_lo_of(tl.qt);
                 const long long blk0 = ds_block(tl.bh, n_qt, tl.qt, 0);
                 for (int kt = kt_lo; ok && kt <= tl.qt; ++kt) {
                     for (int half = 0; half < 2; ++half, ++x) {
-                        const int s = x % NST, use = x / NST;
-                        if (x >= NST && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, 0x121)) {
+                        const int s = x % NSD, use = x / NSD;
+                        if (x >= NSD && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, 0x121)) {
                             ok = false;
                             break;
                         }
-                        mbar_expect_tx(bar(FULL + s), S::STAGE);
-                        // keys kt*128 + 64 half .. + 63: rows of both query halves of the block
-                        const int row = static_cast<int>((blk0 + kt) * 2 * BN) + half * KS;  // < 2^31 (host check)
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_2d(stage(s) + c * (KS * 128), &tm_ds, 0, row + c * BN, bar(FULL + s));
-                        for (int c = 0; c < NC; ++c)
-                            tma_load_4d(stage(s) + S::DSBYTES + c * (KS * 128), &tm_k, c * 64, hk,
-                                        kt * BN + half * KS, b, bar(FULL + s));
+                        // keys kt*128 + 64 half .. + 63 of the block: one contiguous 16 KB piece
+                        const __half* src = ds + (blk0 + kt) * (BN * BM) + half * (KS * BM);
+                        if (NC_IN_RANGE_LOAD(src, S::DSBYTES, 0x129)) {
+                            mbar_expect_tx(bar(FULL + s), S::DSBYTES);
+                            bulk_load(dstage(s), src, S::DSBYTES, bar(FULL + s));
+                        } else {
+                            mbar_arrive(bar(FULL + s));  // recorded; the stage keeps what it held
+                        }
                         ++issued[s];
                     }
                 }
             }
             // never leave the CTA with a bulk copy still in flight
-            for (int s = 0; s < NST; ++s)
+            for (int s = 0; s < NSD; ++s)
                 if (issued[s]) mbar_wait(bar(FULL + s), (issued[s] - 1) & 1, 0x124);
+        }
+        __syncwarp();
+    } else if (warp == WARP_K_TMA) {
+        // ---------------------------------------- khat ring producer ----
+        if (lane == 0) {
+            int x = 0;  // stages filled so far (all tiles), in step with the dS ring
+            int issued[NSK];
+            for (int s = 0; s < NSK; ++s) issued[s] = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int idx = next_tile(n, false);
+                if (idx < 0) break;
+                const DqTile tl = dq_tile(idx, n_qt, nbh, group);
+                const int b = tl.bh / H, hk = (tl.bh % H) / G;
+                for (int kt = kt_lo_of(tl.qt); ok && kt <= tl.qt; ++kt) {
+                    for (int half = 0; half < 2; ++half, ++x) {
+                        const int s = x % NSK, use = x / NSK;
+                        if (x >= NSK && !mbar_wait(bar(KEMPTY + s), (use - 1) & 1, 0x125)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(bar(KFULL + s), S::KBYTES);
+                        for (int c = 0; c < NC; ++c)
+                            tma_load_4d(kstage(s) + c * (KS * 128), &tm_k, c * 64, hk, kt * BN + half * KS, b,
+                                        bar(KFULL + s));
+                        ++issued[s];
+                    }
+                }
+            }
+            for (int s = 0; s < NSK; ++s)
+                if (issued[s]) mbar_wait(bar(KFULL + s), (issued[s] - 1) & 1, 0x126);
         }
         __syncwarp();
     } else if (warp == WARP_EPI_TMA) {
@@ -267,18 +324,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t acc = tmem + buf * 128;
                 const int steps = 2 * (tl.qt - kt_lo_of(tl.qt) + 1);
                 for (int j = 0; j < steps; ++j, ++x) {
-                    const int s = x % NST;
-                    if (!mbar_wait(bar(FULL + s), (x / NST) & 1, 0x221)) {
+                    const int s = x % NSD, sk = x % NSK;
+                    if (!mbar_wait(bar(FULL + s), (x / NSD) & 1, 0x221) ||
+                        !mbar_wait(bar(KFULL + sk), (x / NSK) & 1, 0x226)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < KS / 16; ++kk)
-                        mma_bf16(acc, sdesc_sw128(stage(s) + kk * (16 * 128), KS * 128, 1024),
-                                 sdesc_sw128(stage(s) + S::DSBYTES + kk * (16 * 128), KS * 128, 1024), IDESC,
+                        mma_bf16(acc, sdesc_noswz(dstage(s) + kk * (2 * DS_LBO), DS_LBO, DS_SBO),
+                                 sdesc_sw128(kstage(sk) + kk * (16 * 128), KS * 128, 1024), IDESC,
                                  (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(bar(EMPTY + s));
+                    mma_commit(bar(KEMPTY + sk));
                 }
                 if (ok) mma_commit(bar(DQ_FULL + buf));
             }

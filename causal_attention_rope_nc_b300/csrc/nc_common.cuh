@@ -168,34 +168,6 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4& u, float (&x)[8]) {
     }
 }
 
-// Two 4 x 4 transposes of 16-byte chunks inside each group of 4 lanes
-// (lanes 4j .. 4j + 3), one over chunks 0-3 and one over chunks 4-7: before,
-// lane 4j + r holds chunks (r, 0..7) in c[0..7]; after, lane 4j + k holds
-// chunks (r, k) in c[r] and (r, 4 + k) in c[4 + r], r = 0..3.  Two butterfly
-// stages (xor 2, 1), each trading half of the chunks with the partner lane.
-// All 32 lanes must take part.
-__device__ __forceinline__ void transpose4_chunks(uint4 (&c)[8]) {
-    const int r = threadIdx.x & 3;
-#pragma unroll
-    for (int d = 2; d > 0; d >>= 1) {
-        const bool up = (r & d) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i & d) continue;
-            const int j = i | d;
-            const uint4 send = up ? c[i] : c[j];
-            uint4 got;
-            got.x = __shfl_xor_sync(0xffffffffu, send.x, d);
-            got.y = __shfl_xor_sync(0xffffffffu, send.y, d);
-            got.z = __shfl_xor_sync(0xffffffffu, send.z, d);
-            got.w = __shfl_xor_sync(0xffffffffu, send.w, d);
-            if (up)
-                c[i] = got;
-            else
-                c[j] = got;
-        }
-    }
-}
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled tile whose rows are 128 bytes: the layout that a TMA
@@ -371,6 +343,40 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= 1ull << 46;  // descriptor version for tcgen05
     d |= 2ull << 61;  // SWIZZLE_128B
     return d;
+}
+
+// Paired fp32 arithmetic (one instruction for two lanes of work on sm_100+):
+// each component is rounded exactly as the scalar operation would round it.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Shared-memory matrix descriptor without swizzling: the operand is made of
+// 8 x 16-byte core matrices (128 contiguous bytes each); lbo and sbo are the
+// byte strides between core matrices along the two dimensions (for an
+// MN-major operand: lbo along K, sbo along M/N).
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // descriptor version for tcgen05
+    return d;         // layout type 0: no swizzle
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

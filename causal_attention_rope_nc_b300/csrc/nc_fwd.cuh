@@ -302,8 +302,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint32_t w[16], wl[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2(fmaf(__uint_as_float(rc[e]), scale_log2, -mfix_log2));
-                        float p1 = ex2(fmaf(__uint_as_float(rc[e + 1]), scale_log2, -mfix_log2));
+                        const float2 x2 = ffma2(make_float2(__uint_as_float(rc[e]), __uint_as_float(rc[e + 1])),
+                                                make_float2(scale_log2, scale_log2),
+                                                make_float2(-mfix_log2, -mfix_log2));
+                        float p0 = ex2(x2.x);
+                        float p1 = ex2(x2.y);
                         if constexpr (decltype(masked)::value) {
                             // visible: 0 <= query - key < W
                             const int dd = d0 - (c * 32 + e);

@@ -337,10 +337,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int e = 0; e < 128; e += 4) {
                         float p[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            p[i] = ex2(fmaf(__uint_as_float(r[e + i]), c_log2, off));
-                            if (decltype(masked)::value && !vis(e + i)) p[i] = 0.f;
+                        for (int i = 0; i < 4; i += 2) {
+                            const float2 x2 = ffma2(make_float2(__uint_as_float(r[e + i]), __uint_as_float(r[e + i + 1])),
+                                                    make_float2(c_log2, c_log2), make_float2(off, off));
+                            p[i] = ex2(x2.x);
+                            p[i + 1] = ex2(x2.y);
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (decltype(masked)::value && !vis(e + i)) p[i] = 0.f;
                         const int a = (e >> 2) & 3;
                         lx[a] += (p[0] + p[1]) + (p[2] + p[3]);
                         const uint32_t lo2 = e4m3x2(p[0], p[1]), hi2 = e4m3x2(p[2], p[3]);

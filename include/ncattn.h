@@ -155,10 +155,10 @@ int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int3
  * Workspace: NC_OP_BWD, overwritten by every call: the RoPE table, per-row
  * delta and lse, and the dS scratch.  The key-side kernel forms each
  * visible 128 x 128 block of dS = P o (dP - delta) once and writes it there
- * (bf16) for the query side's dq = dS khat, so the workspace grows with
- * B * H * n(n+1)/2 blocks of 32 KB, n = ceil(T / 128) (1.4 GB at B = 32,
- * T = 2048, H = 10).  Problems with B * H * n(n+1)/2 >= 2^24 blocks are
- * NC_EINVAL. */
+ * (fp16, times one power of two for the whole call) for the query side's
+ * dq = dS khat, so the workspace grows with B * H * n(n+1)/2 blocks of
+ * 32 KB, n = ceil(T / 128) (1.4 GB at B = 32, T = 2048, H = 10).  Problems
+ * with B * H * n(n+1)/2 >= 2^24 blocks (512 GB of scratch) are NC_EINVAL. */
 int nc_attn_bwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, const nc_bf16 *out,
                 const float *lse, const nc_f16 *qhat, const nc_f16 *khat, const nc_bf16 *dout, nc_bf16 *dq,
                 nc_bf16 *dk, nc_bf16 *dv, void *workspace, size_t workspace_bytes, int B, int T, int H, int D,
