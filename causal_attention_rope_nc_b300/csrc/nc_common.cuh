@@ -95,23 +95,6 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
     return __half22float2(v);
 }
 
-// acc + the low / high bf16 half of w, in one mixed-precision add (the
-// bf16 value converts to fp32 exactly, so this is the fp32 sum of the
-// unpacked value, rounded once).
-__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w) {
-    float r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %1;\n\t}"
-        : "=f"(r)
-        : "f"(acc), "r"(w));
-    return r;
-}
-__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t w) {
-    float r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, hi, %1;\n\t}"
-        : "=f"(r)
-        : "f"(acc), "r"(w));
-    return r;
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -354,6 +337,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
