@@ -308,11 +308,11 @@ def bench_ours(args, ws_n, rank, local):
 # from one ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum, summarised under profiles/ with its command).
 # Must go back to None whenever that kernel's code changes.
-DRAM_TRAFFIC = {"attn_bwd_dkdv": None, "attn_bwd_dq": None,
-                "attn_fwd": None}
+DRAM_TRAFFIC = {"attn_bwd_dkdv": 887.09e6 + 1.71e9, "attn_bwd_dq": 1.79e9 + 157.83e6,
+                "attn_fwd": 507.45e6 + 148.52e6}
 # The same for the decode kernels at the d20 decode workload (plain multi-head
 # attention, and 2 key/value heads).
-DECODE_TRAFFIC = {"mha": None, "gqa2": 35.88e6 + 0.0}
+DECODE_TRAFFIC = {"mha": 176.36e6 + 1.46e6, "gqa2": 35.88e6 + 0.0}
 
 
 def band_pairs(T, W):
