@@ -271,12 +271,21 @@ int tile_group(int n_t, int nbh) {
     return g < 1 ? 1 : g;
 }
 
+// RoPE frequencies theta_i = base^(-2i/D), i < D/2, in double precision:
+// the one set of values the tables, the decode and the prefill all use.
+nc::Theta rope_thetas(int D, float base) {
+    nc::Theta th{};
+    for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
+    return th;
+}
+
 int launch_rope_table(float2* tab, const int32_t* pos, int T, int D, float base, cudaStream_t s) {
     const long long n = static_cast<long long>(T) * (D / 2);
     int grid = static_cast<int>((n + 255) / 256);
     if (grid > 148 * 8) grid = 148 * 8;
+    const nc::Theta th = rope_thetas(D, base);
     ProfScope ps("rope_table", s);
-    nc::rope_table_kernel<<<grid, 256, (D / 2) * sizeof(double), s>>>(tab, pos, T, D, std::log2(double(base)));
+    nc::rope_table_kernel<<<grid, 256, 0, s>>>(tab, pos, T, D, th);
     return launch_status();
 }
 
@@ -364,8 +373,7 @@ template <int D>
 int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t* start, nc_bf16* kcache,
                  nc_bf16* vcache, nc_bf16* out, float* lse, void* ws, int B, int C, int H, int Hkv, int Tcap,
                  float eps, float base, int W, cudaStream_t s) {
-    nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
-    for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
+    const nc::Theta th = rope_thetas(D, base);
     __nv_bfloat16* qhat = reinterpret_cast<__nv_bfloat16*>(ws);
     {
         ProfScope ps("prefill_norm_rope", s);
@@ -605,8 +613,7 @@ int decode_impl(const nc_bf16* q, const nc_bf16* k_new, const nc_bf16* v_new, nc
                 const int32_t* lens, nc_bf16* out, const DecodeWs& ws, int B, int H, int Hkv, int Tcap, float eps,
                 float base, int W, cudaStream_t s) {
     const float scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
-    nc::Theta th{};  // theta_i = base^(-2i/D), the same formula as the device-side RoPE tables
-    for (int i = 0; i < D / 2; ++i) th.t[i] = std::exp2(-(2.0 * i / D) * std::log2(double(base)));
+    const nc::Theta th = rope_thetas(D, base);
     if (Hkv == H) {
         // multi-head attention: the register-pipelined kernel, one warp per
         // head, the heads split over head groups

@@ -555,14 +555,12 @@ __device__ __forceinline__ TileCoord grouped_tile(int id, int nbh, int n_t, int 
     return c;
 }
 
+
 // --------------------------------------------------------------------- RoPE --
 // Rotation (cos, sin) of pair i at position p: angle p * theta_i with
 // theta_i = base^(-2i/D).  The angle is formed and reduced modulo 2*pi in
 // double precision, so the fp32 sin/cos that follow see an argument in
 // [-pi, pi] and the rotation is accurate to fp32 rounding for any position.
-__device__ __forceinline__ double rope_theta(int i, int D, double log2_base) {
-    return exp2(-(2.0 * i / D) * log2_base);
-}
 
 // RoPE frequencies theta_i = base^(-2i/D), i < D/2, formed on the host in
 // double precision and passed by value.

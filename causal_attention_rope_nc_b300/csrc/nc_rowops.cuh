@@ -47,20 +47,18 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 // ------------------------------------------------------------ RoPE table --
-// tab[t][i] = (cos, sin) of angle pos[t] * base^(-2i/D), t < T, i < D/2.
-// pos == nullptr means pos[t] = t.
+// tab[t][i] = (cos, sin) of angle pos[t] * theta_i, t < T, i < D/2, with
+// theta_i = base^(-2i/D) formed on the host in double precision (the same
+// values every kernel of the library uses).  pos == nullptr means pos[t] = t.
 __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restrict__ pos, int T, int D,
-                                  double log2_base) {
-    extern __shared__ double s_theta[];  // D/2 entries
+                                  const __grid_constant__ Theta theta) {
     const int half = D / 2;
-    for (int i = threadIdx.x; i < half; i += blockDim.x) s_theta[i] = rope_theta(i, D, log2_base);
-    __syncthreads();
     const long long n = static_cast<long long>(T) * half;
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int t = static_cast<int>(e / half), i = static_cast<int>(e % half);
         const int p = pos ? pos[t] : t;
-        if (NC_IN_RANGE(tab + e, sizeof(float2), 0x401)) tab[e] = rope_cos_sin(p, s_theta[i]);
+        if (NC_IN_RANGE(tab + e, sizeof(float2), 0x401)) tab[e] = rope_cos_sin(p, theta.t[i]);
     }
 }
 
