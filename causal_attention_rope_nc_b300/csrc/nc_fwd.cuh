@@ -298,13 +298,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld();
             const int kt = (t ? lo1 : lo0) + j;            // key tile
             const int d0 = qpos0 + qt * BM + row - kt * BN;  // query - key position at column 0 of the tile
-            auto exp_tile = [&](auto masked, auto split) {
+            auto exp_tile = [&](auto masked) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     // the load of chunk c+1 overlaps the exponentials of chunk c
                     if (c + 1 < BN / 32) tmem_ld32(ts + (c + 1) * 32, r[(c + 1) & 1]);
                     const uint32_t* rc = r[c & 1];
-                    uint32_t w[16], wl[16];
+                    uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const float2 x2 = ffma2(make_float2(__uint_as_float(rc[e]), __uint_as_float(rc[e + 1])),
@@ -318,34 +318,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             if (dd < 0 || dd >= W) p0 = 0.f;
                             if (dd - 1 < 0 || dd - 1 >= W) p1 = 0.f;
                         }
-                        const uint32_t wv = pack_bf16x2(p0, p1);
+                        w[e / 2] = pack_bf16x2(p0, p1);
                         l2 = fadd2(l2, make_float2(p0, p1));
-                        w[e / 2] = wv;
-                        if constexpr (decltype(split)::value) {
-                            const float2 ph = unpack_bf16x2(wv);
-                            wl[e / 2] = pack_bf16x2(p0 - ph.x, p1 - ph.y);
-                        }
                     }
-                    // chunk c lands in packed columns [32c, 32c+16) (P_lo in
-                    // [32c+16, 32c+32)): its own, already read
+                    // chunk c lands in packed columns [32c, 32c+16): its own, already read
                     tmem_st16(ts + c * 32, w);
-                    if constexpr (decltype(split)::value) tmem_st16(ts + c * 32 + 16, wl);
                     if (c + 1 < BN / 32) tmem_wait_ld();
                 }
             };
-            // every (query, key) pair of the tile visible: the plain loop; the
-            // split form whenever the MMA thread issues the P_lo product
+            // The split form (P_hi in packed columns [32c, 32c+16), P_lo in
+            // [32c+16, 32c+32)) runs on few tiles (the first query tile of
+            // each (b, h)), so it is a compact loop, one chunk at a time and
+            // always with the visibility test (d20: 373-376 us against 378 us
+            // with two more fully unrolled copies of the loop above, 271
+            // against 280 us with a 512-key window).
+            auto exp_split = [&]() {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t rc[32];
+                    tmem_ld32(ts + c * 32, rc);
+                    tmem_wait_ld();
+                    uint32_t w[16], wl[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 x2 = ffma2(make_float2(__uint_as_float(rc[e]), __uint_as_float(rc[e + 1])),
+                                                make_float2(scale_log2, scale_log2),
+                                                make_float2(-mfix_log2, -mfix_log2));
+                        float p0 = ex2(x2.x);
+                        float p1 = ex2(x2.y);
+                        const int dd = d0 - (c * 32 + e);
+                        if (dd < 0 || dd >= W) p0 = 0.f;
+                        if (dd - 1 < 0 || dd - 1 >= W) p1 = 0.f;
+                        const uint32_t wv = pack_bf16x2(p0, p1);
+                        const float2 ph = unpack_bf16x2(wv);
+                        w[e / 2] = wv;
+                        wl[e / 2] = pack_bf16x2(p0 - ph.x, p1 - ph.y);
+                        l2 = fadd2(l2, make_float2(p0, p1));
+                    }
+                    tmem_st16(ts + c * 32, w);
+                    tmem_st16(ts + c * 32 + 16, wl);
+                }
+            };
+            // every (query, key) pair of the tile visible: the plain loop
             const bool full = kt * BN + BN - 1 <= qpos0 + qt * BM && qpos0 + qt * BM + BM - 1 - kt * BN < W;
-            if (split_tile(t)) {
-                if (full)
-                    exp_tile(std::false_type{}, std::true_type{});
-                else
-                    exp_tile(std::true_type{}, std::true_type{});
-            } else if (full) {
-                exp_tile(std::false_type{}, std::false_type{});
-            } else {
-                exp_tile(std::true_type{}, std::false_type{});
-            }
+            if (split_tile(t))
+                exp_split();
+            else if (full)
+                exp_tile(std::false_type{});
+            else
+                exp_tile(std::true_type{});
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive_warp(bar(P_FULL + t));
