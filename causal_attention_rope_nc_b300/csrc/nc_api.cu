@@ -13,6 +13,7 @@
 #include "nc_common.cuh"
 #include "nc_decode.cuh"
 #include "nc_fwd.cuh"
+#include "nc_fwd_persist.cuh"
 #include "nc_fwd_fp8.cuh"
 #include "nc_rowops.cuh"
 
@@ -76,8 +77,8 @@ int device_ready() {
         cudaError_t x = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (x != cudaSuccess) r = x;
     };
-    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64, false>), nc::fwd::Smem<64>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128, false>), nc::fwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwdp::attn_fwd_persistent_kernel<64>), nc::fwdp::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::fwdp::attn_fwd_persistent_kernel<128>), nc::fwdp::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64, true>), nc::fwd::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd8::attn_fwd_fp8_kernel), nc::fwd8::Smem::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128, true>), nc::fwd::Smem<128>::ALLOC);
@@ -357,13 +358,29 @@ int fwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     if (rc) return rc;
     rc = launch_norm_rope<D, __half>(q, k, tab, qhat, khat, rstd, B, T, H, Hkv, eps, s);
     if (rc) return rc;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (make_tmap(&tq, qhat, B, T, H, D, nc::fwd::BM, kF16) ||
-        make_tmap(&tk, khat, B, T, Hkv, D, nc::fwd::BN, kF16) || make_tmap(&tv, v, B, T, Hkv, D, nc::fwd::BN) ||
-        make_tmap(&to, out, B, T, H, D, nc::fwd::BM))
+        make_tmap(&tk, khat, B, T, Hkv, D, nc::fwd::BN, kF16) || make_tmap(&tv, v, B, T, Hkv, D, nc::fwd::BN))
         return NC_EINVAL;
-    // one CTA per pair of query tiles
-    return launch_fwd<D, false>(tq, tk, tv, to, lse, T, H, B, Hkv, W, nullptr, T, "attn_fwd", s);
+    // persistent: one CTA per SM takes pairs of query tiles from a counter
+    unsigned int* counter = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(ws) + tab_bytes(T, D));
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    const int n_qt = (T + nc::fwd::BM - 1) / nc::fwd::BM;
+    const int n_pairs = (n_qt + 1) / 2;
+    const long long n_items = static_cast<long long>(n_pairs) * B * H;
+    if (n_items > 0x7fffffffLL) return NC_EINVAL;
+    const double scale = 1.0 / std::sqrt(double(D));
+    const double log2e = 1.4426950408889634;
+    const double mfix = std::sqrt(double(D)) * 1.0079;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int grid = static_cast<int>(n_items < g_sm_count[dev] ? n_items : g_sm_count[dev]);
+    ProfScope ps("attn_fwd", s);
+    nc::fwdp::attn_fwd_persistent_kernel<D><<<static_cast<unsigned>(grid), nc::fwdp::NUM_THREADS,
+                                              nc::fwdp::Smem<D>::ALLOC, s>>>(
+        tq, tk, tv, reinterpret_cast<__nv_bfloat16*>(out), lse, T, H, B, n_qt, tile_group(n_pairs, B * H),
+        float(scale * log2e), float(mfix * log2e), float(mfix), W, H / Hkv, counter);
+    return launch_status();
 }
 
 // Chunk prefill: the prologue writes qhat (workspace) and the chunk's keys
@@ -736,7 +753,7 @@ size_t nc_attn_workspace_size(int op, int B, int T, int H, int D) {
     if (!shape_ok(B, T, H, D)) return 0;
     switch (op) {
         case NC_OP_NORM_ROPE:
-        case NC_OP_FWD: return tab_bytes(T, D);
+        case NC_OP_FWD: return tab_bytes(T, D) + 256;  // RoPE table, pair counter
         case NC_OP_BWD: return bwd_ws_bytes(B, T, H, D);
         case NC_OP_DECODE: return decode_ws_layout(B, H, D, T, nullptr, nullptr);
         case NC_OP_PREFILL: return up256(static_cast<size_t>(B) * T * H * D * 2);  // qhat of the chunk

@@ -141,7 +141,8 @@ int nc_qk_norm_rope(const nc_bf16 *x, const int32_t *pos, nc_bf16 *xhat, float *
 /* Forward.  In: q, k, v [B][T][H][D]; pos [T] or NULL (0..T-1).
  * Out: out [B][T][H][D]; lse [B][H][T]; qhat, khat [B][T][H][D] (the
  * normalised, rotated q and k in fp16, kept for the backward); rstd
- * optional [2][B][T][H] (q then k).  Scale 1/sqrt(D).  Workspace: NC_OP_FWD. */
+ * optional [2][B][T][H] (q then k).  Scale 1/sqrt(D).  Workspace: NC_OP_FWD (the RoPE
+ * table and the counter the persistent kernel's CTAs take tile pairs from). */
 int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int32_t *pos, nc_bf16 *out,
                 float *lse, nc_f16 *qhat, nc_f16 *khat, float *rstd, void *workspace, size_t workspace_bytes,
                 int B, int T, int H, int D, float eps, float rope_base, nc_stream_t stream);

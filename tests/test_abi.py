@@ -56,7 +56,7 @@ def test_workspace_sizes(lib):
     f.argtypes = [ctypes.c_int] * 5
     B, T, H, D = 32, 2048, 10, 128
     tab = T * (D // 2) * 8
-    assert f(0, B, T, H, D) == tab
+    assert f(0, B, T, H, D) == tab + 256  # RoPE table, the forward's pair counter
     n_t = T // 128
     assert f(1, B, T, H, D) == tab + 2 * B * H * T * 4 + 256 + B * H * (n_t * (n_t + 1) // 2) * 128 * 128 * 2
     assert f(2, B, T, H, D) > 0
