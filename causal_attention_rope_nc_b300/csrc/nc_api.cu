@@ -82,8 +82,8 @@ int device_ready() {
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<64, true>), nc::fwd::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd8::attn_fwd_fp8_kernel), nc::fwd8::Smem::ALLOC);
     optin(reinterpret_cast<const void*>(nc::fwd::attn_fwd_kernel<128, true>), nc::fwd::Smem<128>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<64>), nc::bwd::Smem<64>::ALLOC);
-    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_kernel<128>), nc::bwd::Smem<128>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_persistent_kernel<64>), nc::bwd::Smem<64>::ALLOC);
+    optin(reinterpret_cast<const void*>(nc::bwd::attn_bwd_dkdv_persistent_kernel<128>), nc::bwd::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<64>), nc::bwdq::Smem<64>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::bwdq::attn_bwd_dq_kernel<128>), nc::bwdq::Smem<128>::ALLOC);
     optin(reinterpret_cast<const void*>(nc::dec::attn_decode_tma_kernel<64, 1>), kDecodeSmemMax);
@@ -422,12 +422,13 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
     float* lse2 = reinterpret_cast<float*>(w);
     w += up256(static_cast<size_t>(B) * H * Tpad * 4);
-    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);  // max ||dout_t||, max ||v_t||, dq tile counter
+    // max ||dout_t||, max ||v_t||, the query side's and the key side's tile counters
+    unsigned int* gmax = reinterpret_cast<unsigned int*>(w);
     w += 256;
     nc_f16* ds = reinterpret_cast<nc_f16*>(w);
     int rc = launch_rope_table(tab, pos, T, D, base, s);
     if (rc) return rc;
-    if (cudaMemsetAsync(gmax, 0, 3 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
+    if (cudaMemsetAsync(gmax, 0, 4 * sizeof(unsigned int), s) != cudaSuccess) return launch_status();
     const long long rows = static_cast<long long>(B) * T * H;
     {
         ProfScope ps("attn_bwd_pre", s);
@@ -436,13 +437,12 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
             reinterpret_cast<const __nv_bfloat16*>(v), lse, delta, lse2, gmax, B, T, H, Hkv, Tpad);
     }
     if ((rc = launch_status())) return rc;
-    CUtensorMap tq, tk, tv, tdo, tqr, tkr, ttab, tdq, tdk, tdv, tk64;
+    CUtensorMap tq, tk, tv, tdo, tqr, ttab, tdq, tdk, tdv, tk64;
     if (make_tmap(&tq, qhat, B, T, H, D, 128, kF16) || make_tmap(&tk, khat, B, T, Hkv, D, 128, kF16) ||
         make_tmap(&tv, v, B, T, Hkv, D, 128) || make_tmap(&tdo, dout, B, T, H, D, 128) ||
-        make_tmap(&tqr, q, B, T, H, D, 128) || make_tmap(&tkr, k, B, T, Hkv, D, 128) ||
-        make_tab_tmap(&ttab, tab, T, D) || make_tmap(&tdq, dq, B, T, H, D, 128) ||
-        make_tmap(&tdk, dk, B, T, Hkv, D, 128) || make_tmap(&tdv, dv, B, T, Hkv, D, 128) ||
-        make_tmap(&tk64, khat, B, T, Hkv, D, nc::bwdq::KS, kF16))
+        make_tmap(&tqr, q, B, T, H, D, 128) || make_tab_tmap(&ttab, tab, T, D) ||
+        make_tmap(&tdq, dq, B, T, H, D, 128) || make_tmap(&tdk, dk, B, T, Hkv, D, 128) ||
+        make_tmap(&tdv, dv, B, T, Hkv, D, 128) || make_tmap(&tk64, khat, B, T, Hkv, D, nc::bwdq::KS, kF16))
         return NC_EINVAL;
     const long long n_t = (T + 127) / 128;
     const long long nblk = n_t * B * H;
@@ -451,21 +451,25 @@ int bwd_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int32_t
     const double scale = 1.0 / std::sqrt(double(D));
     const int G = H / Hkv;
     const int group = tile_group(static_cast<int>(n_t), B * H);
+    int dev = 0;
+    cudaGetDevice(&dev);
     {
-        // key side: dk, dv (one CTA per key tile of a key/value head, longest
-        // walks first; it walks the query blocks of all G heads that share it)
+        // key side: dk, dv; one persistent CTA per SM takes the key tiles of
+        // the key/value heads (longest walks first in a group) from a counter
+        // and walks the query blocks of all G heads that share each
+        const int grid = static_cast<int>(nblk_kv < g_sm_count[dev] ? nblk_kv : g_sm_count[dev]);
         ProfScope ps("attn_bwd_dkdv", s);
-        nc::bwd::attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(nblk_kv), nc::bwd::NUM_THREADS,
-                                           nc::bwd::Smem<D>::ALLOC, s>>>(
-            tq, tk, tv, tdo, tkr, ttab, tdk, tdv, lse2, delta, gmax, reinterpret_cast<__half*>(ds), T, H, B, Tpad,
-            tile_group(static_cast<int>(n_t), B * Hkv), float(scale), float(scale * 1.4426950408889634), eps, W, G);
+        nc::bwd::attn_bwd_dkdv_persistent_kernel<D><<<static_cast<unsigned>(grid), nc::bwd::NUM_THREADS,
+                                                       nc::bwd::Smem<D>::ALLOC, s>>>(
+            tq, tk, tv, tdo, ttab, tdk, tdv, reinterpret_cast<const __nv_bfloat16*>(k), lse2, delta, gmax,
+            reinterpret_cast<__half*>(ds), T, H, B, Tpad,
+            tile_group(static_cast<int>(n_t), B * Hkv), float(scale), float(scale * 1.4426950408889634), eps, W, G,
+            gmax + 3);
     }
     if ((rc = launch_status())) return rc;
     {
         // query side: dq = dS khat from the key side's dS^T scratch, one
         // persistent CTA per SM over all query tiles
-        int dev = 0;
-        cudaGetDevice(&dev);
         const long long n_tiles = n_t * B * H;
         const int grid = static_cast<int>(n_tiles < g_sm_count[dev] ? n_tiles : g_sm_count[dev]);
         ProfScope ps("attn_bwd_dq", s);
