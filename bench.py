@@ -308,8 +308,8 @@ def bench_ours(args, ws_n, rank, local):
 # from one ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum, summarised under profiles/ with its command).
 # Must go back to None whenever that kernel's code changes.
-DRAM_TRAFFIC = {"attn_bwd_dkdv": 887.09e6 + 1.71e9, "attn_bwd_dq": 1.79e9 + 157.83e6,
-                "attn_fwd": None}
+DRAM_TRAFFIC = {"attn_bwd_dkdv": 881.08e6 + 1.71e9, "attn_bwd_dq": 1.79e9 + 157.83e6,
+                "attn_fwd": 505.57e6 + 145.83e6}
 # The same for the decode kernels at the d20 decode workload (plain multi-head
 # attention, and 2 key/value heads).
 DECODE_TRAFFIC = {"mha": 176.36e6 + 1.46e6, "gqa2": 35.88e6 + 0.0}
