@@ -45,7 +45,8 @@
 // Persistence.  One CTA per SM takes the key tiles from a global counter in
 // the grouped order (longest walks first in a group) and keeps its barriers,
 // tensor memory and pipelines across them.
-// Measured per key tile of a one-CTA-per-tile form (d20, SM cycles):
+// Measured per key tile of a one-CTA-per-tile form (B=32, T=2048, H=10,
+// D=128; SM cycles):
 // about 1.1K between one CTA's exit and the next one's entry, 1.5K of
 // barrier and TMEM setup, 3.7K waiting for the first K, V, qhat and dout
 // tiles, and 4.7K of epilogue, against 3.1-3.5K per query block of the walk

@@ -39,7 +39,7 @@
 // tiles share them), so the two streams have rings of their own: nine 16 KB
 // dS stages keep 144 KB of the HBM stream in flight per SM, three khat
 // stages cover the shorter L2 latency.  (One ring of six 32 KB (dS, khat)
-// pairs, 96 KB of dS in flight, measured the same 393 us at d20: the bytes
+// pairs, 96 KB of dS in flight, measured the same 393 us at B=32, T=2048, H=10, D=128: the bytes
 // in flight are not what holds the stream at 4.5 TB/s.)
 // Tile order: the grouped order of the other kernels ((batch, head) pairs
 // in groups of about one wave, the longest walks first inside a group, so

@@ -76,7 +76,7 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // token's rotation row from the table once and walks the token's H heads,
 // HC heads at a time with every load of a chunk issued before any math, so
 // each lane keeps HC 16-byte loads in flight.  Tokens are enumerated q
-// tokens first, then k tokens.  (d20, 671 MB: 135 us with HC = 4, 140 us
+// tokens first, then k tokens.  (B=32, T=2048, H=10, D=128, 671 MB: 135 us with HC = 4, 140 us
 // with 8, 196 us with 16: more loads in flight per lane cost occupancy.)
 constexpr int NORM_HC = 4;
 
