@@ -732,6 +732,18 @@ def bench_leg(args):
         res = bench_decode(nc, dev, args, 0, kv_heads=GQA_KV_HEADS)
     elif args.leg == "decode-window":
         res = bench_decode(nc, dev, args, 0, window=workloads.D20.T // 4)
+    elif args.leg == "window":
+        w = workloads.ATTN_WORKLOADS[args.workload]
+        q, k, v, dout = workloads.attn_inputs(w.B, w.T, w.H, w.D, w.seed)
+        qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, dout))
+        out = torch.empty_like(qd)
+        qh, kh = torch.empty_like(qd, dtype=torch.float16), torch.empty_like(kd, dtype=torch.float16)
+        lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws_f = nc.new_workspace(nc.NC_OP_FWD, w.B, w.T, w.H, w.D, dev)
+        ws_b = nc.new_workspace(nc.NC_OP_BWD, w.B, w.T, w.H, w.D, dev)
+        res = bench_window(nc, dev, args, w, qd, kd, vd, dod, out, lse, qh, kh, dq, dk, dv, ws_f, ws_b,
+                           torch.cuda.current_stream(dev))
     else:  # fp8
         w = workloads.ATTN_WORKLOADS[args.workload]
         q, k, v, _ = workloads.attn_inputs(w.B, w.T, w.H, w.D, w.seed)
@@ -752,7 +764,7 @@ def main():
                     help="fwd+bwd shape (the headline metric is quoted on d20; others for profiling)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the decode and end-to-end legs (short runs under a profiler)")
-    ap.add_argument("--leg", choices=["all", "decode", "decode-gqa", "decode-window", "fp8"], default="all",
+    ap.add_argument("--leg", choices=["all", "decode", "decode-gqa", "decode-window", "window", "fp8"], default="all",
                     help="run one side leg alone and print its object (profiling); default: the full line")
     args = ap.parse_args()
     if args.warmup < 3:
