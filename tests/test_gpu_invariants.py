@@ -37,7 +37,7 @@ def nc():
     return m
 
 
-@pytest.mark.parametrize("window,kv_heads", [(0, None), (512, None), (0, 2)])
+@pytest.mark.parametrize("window,kv_heads", [(0, None), (512, None), (0, 2), (512, 2)])
 def test_d20_invariants_every_slice(nc, window, kv_heads):
     w = workloads.D20
     q, k, v, dout = workloads.workload_inputs(w)
