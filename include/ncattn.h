@@ -154,7 +154,9 @@ int nc_attn_fwd(const nc_bf16 *q, const nc_bf16 *k, const nc_bf16 *v, const int3
  * computed by one CTA (a key-side kernel writes dk and dv, a query-side
  * kernel dq): no atomics, bit-identical results on repeated calls.
  * Workspace: NC_OP_BWD, overwritten by every call: the RoPE table, per-row
- * delta and lse, and the dS scratch.  The key-side kernel forms each
+ * delta and lse, two maxima and the two counters that the persistent
+ * kernels' CTAs take tiles from, and the dS scratch.  The key-side kernel
+ * forms each
  * visible 128 x 128 block of dS = P o (dP - delta) once and writes it there
  * (fp16, times one power of two for the whole call) for the query side's
  * dq = dS khat, so the workspace grows with B * H * n(n+1)/2 blocks of
