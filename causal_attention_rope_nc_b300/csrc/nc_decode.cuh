@@ -472,8 +472,19 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1) attn_decode_kernel(
 // counters [B] u32 (zero between calls).  blockDim = (compute warps + 1) * 32,
 // compute warps = ceil(H / HPW) <= MAX_CWARPS; dynamic shared memory
 // smem_bytes(Hkv, D, SB, NST).
+// Registers.  A block of MAX_CWARPS + 1 = 17 warps puts five on one of the
+// four schedulers, whose 16K registers then allow 96 per thread (allocated
+// in steps of 8), the cap with several query heads per warp.  One head per
+// warp fits 80 without spilling, which lets two CTAs of up to 11 warps
+// share an SM (2 x 352 x 80 registers; six warps x 32 x 80 on one
+// scheduler) beside their two shared-memory rings.
+template <int HPW>
+constexpr int decode_tma_maxnreg() {
+    return HPW == 1 ? 80 : 16384 / (((MAX_CWARPS + 1 + 3) / 4) * 32) / 8 * 8;
+}
+
 template <int D, int HPW>
-__global__ void __launch_bounds__((MAX_CWARPS + 1) * 32) attn_decode_tma_kernel(
+__global__ void __maxnreg__(decode_tma_maxnreg<HPW>()) attn_decode_tma_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* kcache, __nv_bfloat16* vcache,
