@@ -263,17 +263,17 @@ int resident_256(Kern kernel) {
     return n;
 }
 
-// One token per D/8-lane group, 256 threads per block: enough blocks for
-// every token, at most the blocks the SMs hold at once (per_sm each), so
+// One token per group of `lanes` lanes, 256 threads per block: enough
+// blocks for every token, at most the blocks the SMs hold at once (per_sm each), so
 // that a grid-stride walk runs as one wave with an even share per block
 // instead of a partial last wave.  (Measured for the QK norm prologue at
 // B=32, T=2048, H=10, D=128, whose 80 registers leave room for 3 blocks per
 // SM: a grid sized for 8 ran 2.7 waves.)
-int tok_grid(long long toks, int D, int per_sm) {
+int tok_grid(long long toks, int lanes, int per_sm) {
     int dev = 0;
     cudaGetDevice(&dev);
     const long long cap = static_cast<long long>(g_sm_count[dev] > 0 ? g_sm_count[dev] : 148) * per_sm;
-    const long long groups = 256 / (D / 8);
+    const long long groups = 256 / lanes;
     long long g = (toks + groups - 1) / groups;
     if (g > cap) g = cap;
     if (g < 1) g = 1;
@@ -316,17 +316,17 @@ int launch_norm_rope(const nc_bf16* q, const nc_bf16* k, const float2* tab, void
     static const int per_sm = resident_256(nc::qk_norm_rope_kernel<D, OutT>);
     ProfScope ps("qk_norm_rope", s, (!k || Hkv == H) ? 1 : 2);
     if (!k || Hkv == H) {
-        nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks * (k ? 2 : 1), D, per_sm), 256, 0, s>>>(
+        nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks * (k ? 2 : 1), D / 16, per_sm), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k), tab,
             reinterpret_cast<OutT*>(qh), reinterpret_cast<OutT*>(kh), rstd, toks, T, H, eps, out_scale);
         return launch_status();
     }
-    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D, per_sm), 256, 0, s>>>(
+    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D / 16, per_sm), 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(q), nullptr, tab, reinterpret_cast<OutT*>(qh), nullptr, rstd, toks,
         T, H, eps, out_scale);
     int rc = launch_status();
     if (rc) return rc;
-    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D, per_sm), 256, 0, s>>>(
+    nc::qk_norm_rope_kernel<D, OutT><<<tok_grid(toks, D / 16, per_sm), 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(k), nullptr, tab, reinterpret_cast<OutT*>(kh), nullptr,
         rstd ? rstd + toks * H : nullptr, toks, T, Hkv, eps, out_scale);
     return launch_status();
@@ -412,7 +412,7 @@ int prefill_impl(const nc_bf16* q, const nc_bf16* k, const nc_bf16* v, const int
     {
         ProfScope ps("prefill_norm_rope", s);
         static const int per_sm = resident_256(nc::prefill_norm_rope_kernel<D>);
-        nc::prefill_norm_rope_kernel<D><<<tok_grid(static_cast<long long>(B) * C, D, per_sm), 256, 0, s>>>(
+        nc::prefill_norm_rope_kernel<D><<<tok_grid(static_cast<long long>(B) * C, D / 8, per_sm), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
             reinterpret_cast<const __nv_bfloat16*>(v), start, qhat, reinterpret_cast<__nv_bfloat16*>(kcache),
             reinterpret_cast<__nv_bfloat16*>(vcache), B, C, H, Hkv, Tcap, eps, th);

@@ -72,13 +72,17 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, const int* __restric
 // heads the host runs one launch per tensor, each with its own head count
 // and its own part of rstd.)
 //
-// One group of D/8 lanes owns one token (b, t) of one tensor: it reads the
+// One group of D/16 lanes owns one token (b, t) of one tensor: lane j holds
+// the 8 rotation pairs (i, i + D/2) for i in [8j, 8j + 8), i.e. 16 bytes of
+// each half of a head row, so the rotation needs no data from another lane
+// and only the row's sum of squares crosses lanes.  The group reads the
 // token's rotation row from the table once and walks the token's H heads,
-// HC heads at a time with every load of a chunk issued before any math, so
-// each lane keeps HC 16-byte loads in flight.  Tokens are enumerated q
-// tokens first, then k tokens.  (B=32, T=2048, H=10, D=128, 671 MB: 135 us with HC = 4, 140 us
-// with 8, 196 us with 16: more loads in flight per lane cost occupancy.)
-constexpr int NORM_HC = 4;
+// NORM_HC heads at a time with every load of a chunk issued before any
+// math.  Tokens are enumerated q tokens first, then k tokens.  (B=32,
+// T=2048, H=10, D=128: the earlier layout, 16 lanes per token with the
+// partner half fetched by 8 shuffles per head, ran with its issue slots 57 %
+// busy; HC = 4 there took 135 us, 8 took 140 us, 16 took 196 us.)
+constexpr int NORM_HC = 2;
 
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q,
@@ -88,16 +92,17 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
                                                            OutT* __restrict__ khat,
                                                            float* __restrict__ rstd, long long tokens_per_tensor,
                                                            int T, int H, float eps, float out_scale = 1.f) {
-    using L = RowLanes<D>;
-    const int sub = threadIdx.x % L::LPR;
-    const long long groups = blockDim.x / L::LPR;
+    static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+    constexpr int LPR = D / 16;  // lanes per token
+    constexpr int HALF = D / 2;
+    const int sub = threadIdx.x % LPR;
+    const long long groups = blockDim.x / LPR;
     const long long ntok = (k ? 2 : 1) * tokens_per_tensor;
-    const long long first = blockIdx.x * groups + threadIdx.x / L::LPR;
+    const long long first = blockIdx.x * groups + threadIdx.x / LPR;
     const long long stride = static_cast<long long>(gridDim.x) * groups;
     // every lane of a warp runs the same number of iterations (shuffles)
-    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / L::LPR;
-    const int i0 = (sub % L::HALF) * 8;
-    const bool lo = sub < L::HALF;
+    const long long warp_first = blockIdx.x * groups + (threadIdx.x & ~31) / LPR;
+    const int i0 = sub * 8;  // this lane's pairs: columns [i0, i0 + 8) and [HALF + i0, HALF + i0 + 8)
     for (long long base = warp_first, tok = first; base < ntok; base += stride, tok += stride) {
         const bool valid = tok < ntok;
         const bool is_k = valid && tok >= tokens_per_tensor;
@@ -112,35 +117,45 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* 
                 c[2 * e2] = v.x, sn[2 * e2] = v.y, c[2 * e2 + 1] = v.z, sn[2 * e2 + 1] = v.w;
             }
         }
-        const __nv_bfloat16* src = (is_k ? k : q) + r * H * D + sub * 8;
-        OutT* dst = (is_k ? khat : qhat) + r * H * D + sub * 8;
+        const __nv_bfloat16* src = (is_k ? k : q) + r * H * D + i0;
+        OutT* dst = (is_k ? khat : qhat) + r * H * D + i0;
         for (int h0 = 0; h0 < H; h0 += NORM_HC) {
-            uint4 u[NORM_HC];
+            uint4 ul[NORM_HC], uh[NORM_HC];
 #pragma unroll
-            for (int j = 0; j < NORM_HC; ++j)
-                u[j] = (valid && h0 + j < H) ? *reinterpret_cast<const uint4*>(src + (h0 + j) * D)
-                                             : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < NORM_HC; ++j) {
+                const bool in = valid && h0 + j < H;
+                ul[j] = in ? *reinterpret_cast<const uint4*>(src + (h0 + j) * D) : make_uint4(0, 0, 0, 0);
+                uh[j] = in ? *reinterpret_cast<const uint4*>(src + (h0 + j) * D + HALF) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
             for (int j = 0; j < NORM_HC; ++j) {
                 if (h0 + j >= H) break;  // uniform: H is the same for every lane
-                float x[8];
-                bf16x8_to_f32(u[j], x);
+                float a[8], b[8];
+                bf16x8_to_f32(ul[j], a);
+                bf16x8_to_f32(uh[j], b);
                 float ss = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-                ss = group_sum<L::LPR>(ss);
+                for (int e = 0; e < 8; ++e) ss = fmaf(a[e], a[e], ss);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(b[e], b[e], ss);
+                ss = group_sum<LPR>(ss);
                 const float rs = rsqrtf(ss / D + eps);
-                float y[8], o[8];
+                float lo[8], hi[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] *= rs;
+                for (int e = 0; e < 8; ++e) {
+                    a[e] *= rs;
+                    b[e] *= rs;
+                }
+                // (a, b) = (x_i, x_{i + D/2}) rotated by the pair's angle
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], L::HALF);
-                // low half holds a = x_i (partner b = x_{i+D/2}); high half the reverse
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = lo ? x[e] * c[e] - y[e] * sn[e] : y[e] * sn[e] + x[e] * c[e];
+                for (int e = 0; e < 8; ++e) {
+                    lo[e] = a[e] * c[e] - b[e] * sn[e];
+                    hi[e] = a[e] * sn[e] + b[e] * c[e];
+                }
                 if (valid) {
-                    if (NC_IN_RANGE(dst + (h0 + j) * D, 8 * sizeof(OutT), 0x402))
-                        store8<OutT>(dst + (h0 + j) * D, o, out_scale);
+                    OutT* d = dst + (h0 + j) * D;
+                    if (NC_IN_RANGE(d, 8 * sizeof(OutT), 0x402)) store8<OutT>(d, lo, out_scale);
+                    if (NC_IN_RANGE(d + HALF, 8 * sizeof(OutT), 0x4f1)) store8<OutT>(d + HALF, hi, out_scale);
                     float* rp = rstd + ((is_k ? tokens_per_tensor : 0) + r) * H + h0 + j;
                     if (rstd && sub == 0 && NC_IN_RANGE(rp, 4, 0x403)) *rp = rs;
                 }
